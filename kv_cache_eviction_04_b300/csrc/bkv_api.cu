@@ -1,0 +1,285 @@
+// C ABI of the BeaconKV eviction step (declared in include/bkv.h): argument
+// validation, workspace layout, TMA descriptors and kernel launches.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bkv {
+size_t select_smem_bytes(int B, int row_bytes);
+size_t fps_smem_bytes(int C);
+}  // namespace bkv
+
+namespace {
+
+using bkv::WsHeader;
+
+constexpr int kMaxSmem = 232448;  // bytes of shared memory a CTA may opt into on sm_103
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate(const bkv_dims* d) {
+  if (d == nullptr) return BKV_EINVAL;
+  if (d->U < 1 || d->G < 1 || d->G > 16 || (d->d != 64 && d->d != 128)) return BKV_EINVAL;
+  if (d->W < 0 || d->W > 64 || d->M < 0 || d->M > 64) return BKV_EINVAL;
+  if (d->C < 2 || d->M >= d->C) return BKV_EINVAL;
+  if (d->B_KV < 1 || d->B_KV > 16384 || d->R < 0 || d->R > d->B_KV) return BKV_EINVAL;
+  if (d->L_cap < d->B_KV || d->L_cap > (1 << 24)) return BKV_EINVAL;
+  if (d->agg != BKV_AGG_MAX && d->agg != BKV_AGG_MEAN) return BKV_EINVAL;
+  if (d->causal_recent != 0 && d->causal_recent != 1) return BKV_EINVAL;
+  if (d->reserved != 0) return BKV_EINVAL;
+  if (!(d->rope_theta > 1.0) || !std::isfinite(d->rope_theta)) return BKV_EINVAL;
+  if (d->W + d->M < 1 || (d->W + d->M) * d->G > 512) return BKV_EINVAL;
+  if (static_cast<int64_t>(d->U) * d->L_cap * d->d >= (int64_t(1) << 40)) return BKV_EINVAL;
+  if (d->C > 256) return BKV_EUNSUPPORTED;
+  return BKV_OK;
+}
+
+int sm_count() {
+  static int n = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      return 148;
+    return v;
+  }();
+  return n;
+}
+
+struct ScoreShape {
+  int NQ, NQ16, nrows_part, ngrp, ntiles, tiles_per_split, nsplit;
+};
+
+ScoreShape score_shape(const bkv_dims* d) {
+  ScoreShape s{};
+  s.NQ = (d->W + d->M) * d->G;
+  s.NQ16 = (s.NQ + 15) & ~15;
+  s.nrows_part = (s.NQ + 127) / 128 * 128;
+  s.ngrp = (s.NQ16 + 255) / 256;
+  s.ntiles = (d->L_cap + 127) / 128;
+  // about four CTAs per SM in the first pass, at least two tiles each
+  const int64_t work = static_cast<int64_t>(d->U) * (s.nrows_part / 128) * s.ntiles;
+  const int64_t target = 4ll * sm_count();
+  int64_t tps = (work + target - 1) / target;
+  if (tps < 2) tps = 2;
+  if (tps > s.ntiles) tps = s.ntiles;
+  if (tps < 1) tps = 1;
+  s.tiles_per_split = static_cast<int>(tps);
+  s.nsplit = (s.ntiles + s.tiles_per_split - 1) / s.tiles_per_split;
+  if (s.nsplit < 1) s.nsplit = 1;
+  return s;
+}
+
+struct WsLayout {
+  size_t unit_done, part, total;
+};
+
+WsLayout ws_layout(const bkv_dims* d) {
+  WsLayout w{};
+  const ScoreShape s = score_shape(d);
+  w.unit_done = bkv::kWsHeaderBytes;
+  w.part = w.unit_done + ((static_cast<size_t>(d->U) * 4 + 255) & ~static_cast<size_t>(255));
+  w.total = w.part + static_cast<size_t>(d->U) * s.nsplit * s.nrows_part * sizeof(float2);
+  return w;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor map over [n2][n1][n0] (n0 contiguous), box {64, box1, 1},
+// 128-byte swizzle, zero fill out of bounds.
+int make_map(CUtensorMap* map, const void* base, uint64_t n0, uint64_t n1, uint64_t n2,
+             uint32_t box1) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return BKV_ECUDA;
+  const cuuint64_t dims[3] = {n0, n1, n2};
+  const cuuint64_t strides[2] = {n0 * 2, n0 * n1 * 2};
+  const cuuint32_t box[3] = {64, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BKV_OK : BKV_ECUDA;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? BKV_OK : BKV_ECUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int bkv_version(void) { return 1; }
+
+const char* bkv_strerror(int code) {
+  switch (code) {
+    case BKV_OK: return "ok";
+    case BKV_EINVAL: return "invalid argument";
+    case BKV_ECUDA: return "CUDA runtime or launch failure";
+    case BKV_ETIMEOUT: return "a device-side wait timed out";
+    case BKV_EDEVICE: return "invalid per-unit device data";
+    case BKV_EUNSUPPORTED: return "shape not supported by this build";
+    default: return "unknown error code";
+  }
+}
+
+int bkv_workspace_size(const bkv_dims* dims, size_t* bytes) {
+  const int v = validate(dims);
+  if (v != BKV_OK) return v;
+  if (bytes == nullptr) return BKV_EINVAL;
+  *bytes = ws_layout(dims).total;
+  return BKV_OK;
+}
+
+int bkv_workspace_init(void* workspace, size_t bytes, bkv_stream_t stream) {
+  if (workspace == nullptr || bytes < bkv::kWsHeaderBytes) return BKV_EINVAL;
+  return cuda_rc(cudaMemsetAsync(workspace, 0, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bkv_fps_update(const bkv_dims* dims, const void* q_new, int64_t step, void* recent_q,
+                   void* buf, int32_t* cnt, int32_t want_beacons, int32_t* beacon_idx,
+                   void* beacons, int32_t* n_beacons, void* workspace, bkv_stream_t stream) {
+  int v = validate(dims);
+  if (v != BKV_OK) return v;
+  if (buf == nullptr || cnt == nullptr || workspace == nullptr || step < 0) return BKV_EINVAL;
+  if (q_new != nullptr && dims->W > 0 && recent_q == nullptr) return BKV_EINVAL;
+  if (!aligned16(buf) || (q_new && !aligned16(q_new)) || (recent_q && !aligned16(recent_q)) ||
+      (beacons && !aligned16(beacons)))
+    return BKV_EINVAL;
+  if (bkv::fps_smem_bytes(dims->C) > static_cast<size_t>(kMaxSmem)) return BKV_EUNSUPPORTED;
+  const int D = dims->G * dims->d;
+  bkv::FpsParams p{};
+  p.q_new = static_cast<const uint16_t*>(q_new);
+  p.recent_q = static_cast<uint16_t*>(recent_q);
+  p.buf = static_cast<uint16_t*>(buf);
+  p.cnt = cnt;
+  p.beacon_idx = beacon_idx;
+  p.beacons = static_cast<uint16_t*>(beacons);
+  p.n_beacons = n_beacons;
+  p.ws = static_cast<WsHeader*>(workspace);
+  p.step = step;
+  p.U = dims->U;
+  p.D = D;
+  p.W = dims->W;
+  p.M = dims->M;
+  p.C = dims->C;
+  p.want_beacons = want_beacons != 0;
+  CUtensorMap map;
+  const uint32_t box_rows = static_cast<uint32_t>(std::min(256, (dims->C + 15) & ~15));
+  v = make_map(&map, buf, static_cast<uint64_t>(D), static_cast<uint64_t>(dims->C),
+               static_cast<uint64_t>(dims->U), box_rows);
+  if (v != BKV_OK) return v;
+  return cuda_rc(bkv::launch_fps(p, map, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bkv_score(const bkv_dims* dims, const void* K, const int32_t* L, const int32_t* kpos,
+              const void* recent_q, int64_t step, const void* beacons,
+              const int32_t* n_beacons, const int32_t* cur_pos, float* scores,
+              void* workspace, bkv_stream_t stream) {
+  int v = validate(dims);
+  if (v != BKV_OK) return v;
+  if (K == nullptr || L == nullptr || kpos == nullptr || cur_pos == nullptr ||
+      scores == nullptr || workspace == nullptr || step < 0)
+    return BKV_EINVAL;
+  if (dims->W > 0 && recent_q == nullptr) return BKV_EINVAL;
+  if (dims->M > 0 && (beacons == nullptr || n_beacons == nullptr)) return BKV_EINVAL;
+  if (!aligned16(K) || (recent_q && !aligned16(recent_q)) || (beacons && !aligned16(beacons)))
+    return BKV_EINVAL;
+  const ScoreShape s = score_shape(dims);
+  if (bkv::score_smem_bytes(dims->d, s.NQ16, dims->W) > static_cast<size_t>(kMaxSmem))
+    return BKV_EUNSUPPORTED;
+  const WsLayout w = ws_layout(dims);
+  bkv::ScoreParams p{};
+  p.L = L;
+  p.kpos = kpos;
+  p.recent_q = static_cast<const uint16_t*>(recent_q);
+  p.beacons = static_cast<const uint16_t*>(beacons);
+  p.n_beacons = n_beacons;
+  p.cur_pos = cur_pos;
+  p.scores = scores;
+  p.part = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + w.part);
+  p.ws = static_cast<WsHeader*>(workspace);
+  p.step = step;
+  p.U = dims->U;
+  p.G = dims->G;
+  p.d = dims->d;
+  p.W = dims->W;
+  p.M = dims->M;
+  p.L_cap = dims->L_cap;
+  p.NQ = s.NQ;
+  p.NQ16 = s.NQ16;
+  p.nrows_part = s.nrows_part;
+  p.ngrp = s.ngrp;
+  p.nsplit = s.nsplit;
+  p.tiles_per_split = s.tiles_per_split;
+  p.agg = dims->agg;
+  p.causal = dims->causal_recent;
+  p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dims->d)));
+  for (int i = 0; i < dims->d / 2; ++i) {
+    const double f = std::pow(dims->rope_theta, -2.0 * i / static_cast<double>(dims->d));
+    p.freq_hi[i] = static_cast<float>(f);
+    p.freq_lo[i] = static_cast<float>(f - static_cast<double>(p.freq_hi[i]));
+  }
+  CUtensorMap map;
+  v = make_map(&map, K, static_cast<uint64_t>(dims->d), static_cast<uint64_t>(dims->L_cap),
+               static_cast<uint64_t>(dims->U), 128);
+  if (v != BKV_OK) return v;
+  return cuda_rc(bkv::launch_score(p, map, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bkv_select_compact(const bkv_dims* dims, const float* scores, void* K, void* V,
+                       int32_t* kpos, int32_t* L, int32_t* kept, void* workspace,
+                       bkv_stream_t stream) {
+  const int v = validate(dims);
+  if (v != BKV_OK) return v;
+  if (scores == nullptr || K == nullptr || V == nullptr || kpos == nullptr || L == nullptr ||
+      workspace == nullptr)
+    return BKV_EINVAL;
+  if (!aligned16(K) || !aligned16(V)) return BKV_EINVAL;
+  if (bkv::select_smem_bytes(dims->B_KV, dims->d * 2) > static_cast<size_t>(kMaxSmem))
+    return BKV_EUNSUPPORTED;
+  const WsLayout w = ws_layout(dims);
+  bkv::SelectParams p{};
+  p.scores = scores;
+  p.K = static_cast<uint8_t*>(K);
+  p.V = static_cast<uint8_t*>(V);
+  p.kpos = kpos;
+  p.L = L;
+  p.kept = kept;
+  p.unit_done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + w.unit_done);
+  p.ws = static_cast<WsHeader*>(workspace);
+  p.U = dims->U;
+  p.L_cap = dims->L_cap;
+  p.B = dims->B_KV;
+  p.R = dims->R;
+  p.row_bytes = dims->d * 2;
+  return cuda_rc(bkv::launch_select_compact(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bkv_get_status(void* workspace, bkv_stream_t stream, int32_t* device_status) {
+  if (workspace == nullptr || device_status == nullptr) return BKV_EINVAL;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return BKV_ECUDA;
+  WsHeader h{};
+  if (cudaMemcpy(&h, workspace, 8, cudaMemcpyDeviceToHost) != cudaSuccess) return BKV_ECUDA;
+  if (cudaMemset(workspace, 0, 8) != cudaSuccess) return BKV_ECUDA;
+  *device_status = h.status;
+  return BKV_OK;
+}
+
+}  // extern "C"

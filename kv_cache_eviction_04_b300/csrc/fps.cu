@@ -1,0 +1,496 @@
+// Continual farthest-point-sampling beacon buffer: per-step append, FPS
+// compress when the buffer is full, and FPS beacon selection at eviction.
+//
+// BeaconKV pages: wzjinhao.cn explainer, section "怎么挑出这几个信标：一种叫FPS
+// 的采样算法" -- seed = the query with the lowest mean similarity to the others;
+// then repeatedly the query farthest from (least similar to) the chosen set;
+// similarity on pre-RoPE queries; each head keeps a bounded buffer that is
+// FPS-compressed to a smaller size whenever it fills up.
+//
+// One CTA (256 threads) per unit.  For a buffer of n items (each the G*d
+// pre-RoPE vector of one decode step):
+//   1. Gram matrix G = X X^T on the tensor core: TMA streams 64-column
+//      slices of X (128-byte swizzle) into shared memory and one thread
+//      issues tcgen05 MMAs; rows 0..127 and 128..255 land in TMEM columns
+//      [0, 256) and [256, 512) with fp32 accumulation.  The Gram stays in
+//      TMEM for the whole selection.
+//   2. Thread i owns item i (its TMEM lane): 1/||x_i|| from the diagonal,
+//      its mean cosine to the others from its TMEM row -> seed = argmin.
+//   3. Greedy: each step reads the new pick's Gram column (one TMEM column:
+//      every thread gets its own item's entry), updates its min distance
+//      1 - cos in a register and a block argmax (warp shuffles, then shared
+//      memory) picks the next item.
+//   4. Exactness guard: an fp32 decision is final only when the winner leads
+//      the runner-up by more than twice a bound on the fp32 error; otherwise
+//      every contender within that band is re-evaluated in fp64 from the
+//      bf16 inputs and the fp64 values decide (ties: lowest index), so the
+//      indices equal those of an fp64 evaluation.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bkv {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kStages = 3;
+constexpr int kMaxSel = 64;
+constexpr int kMaxCont = 64;  // contenders re-evaluated per round of a recheck
+// Bound on |fp32 cosine - exact cosine| for the tensor-core Gram (bf16
+// products are exact; fp32 accumulation over up to 2048 terms in blocks,
+// plus normalisation) with a safety factor; the seed's mean adds a
+// summation error over up to 256 terms.
+constexpr float kTauCos = 4e-5f;
+constexpr float kTauMean = 1e-4f;
+
+struct __align__(16) FpsShared {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t done;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t n_sel;
+  int32_t winner;
+  int32_t n_cont;
+  int32_t pad;
+  float inv[256];
+  int32_t sel[kMaxSel];
+  int32_t surv[kMaxSel];
+  int32_t cont[kMaxCont];
+  double cont_val[kMaxCont];
+  double norm64[256];
+  float red_v1[kWarps];
+  float red_v2[kWarps];
+  int32_t red_i1[kWarps];
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* abort) {
+  bool ok = *reinterpret_cast<volatile int32_t*>(abort) == 0 && wait_bar(bar, parity);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) *reinterpret_cast<volatile int32_t*>(abort) = 1;
+  return ok;
+}
+
+// (best value, its index, runner-up value) under the order "smaller value
+// first, then smaller index" (argmin; the argmax passes negated values).
+struct Top2 {
+  float v1;
+  int i1;
+  float v2;
+};
+__device__ __forceinline__ Top2 top2_merge(Top2 a, Top2 b) {
+  const bool a_first = a.v1 < b.v1 || (a.v1 == b.v1 && a.i1 < b.i1);
+  Top2 r;
+  if (a_first) {
+    r.v1 = a.v1;
+    r.i1 = a.i1;
+    r.v2 = fminf(a.v2, b.v1);
+  } else {
+    r.v1 = b.v1;
+    r.i1 = b.i1;
+    r.v2 = fminf(b.v2, a.v1);
+  }
+  return r;
+}
+// Block-wide Top2 (all threads call; result valid in every thread).
+__device__ Top2 block_top2(Top2 t, FpsShared* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Top2 o2;
+    o2.v1 = __shfl_xor_sync(0xffffffffu, t.v1, o);
+    o2.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
+    o2.v2 = __shfl_xor_sync(0xffffffffu, t.v2, o);
+    t = top2_merge(t, o2);
+  }
+  if (lane == 0) {
+    sh->red_v1[warp] = t.v1;
+    sh->red_i1[warp] = t.i1;
+    sh->red_v2[warp] = t.v2;
+  }
+  __syncthreads();
+  Top2 r{sh->red_v1[0], sh->red_i1[0], sh->red_v2[0]};
+  for (int w = 1; w < kWarps; ++w) r = top2_merge(r, Top2{sh->red_v1[w], sh->red_i1[w], sh->red_v2[w]});
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ double bf16d(uint16_t b) {
+  return static_cast<double>(bf16_bits_to_float(b));
+}
+
+// fp64 norm of item i (cached in shared memory; -1 = not yet computed).
+// Called by a whole warp.
+__device__ double item_norm64(const uint16_t* X, int D, int i, FpsShared* sh) {
+  double nv = sh->norm64[i];
+  if (nv >= 0.0) return nv;
+  const int lane = threadIdx.x & 31;
+  double ss = 0.0;
+  for (int k = lane; k < D; k += 32) {
+    const double v = bf16d(X[static_cast<size_t>(i) * D + k]);
+    ss = fma(v, v, ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  nv = sqrt(ss);
+  __syncwarp();
+  if (lane == 0) sh->norm64[i] = nv;
+  __syncwarp();
+  return nv;
+}
+
+// fp64 cosine of items a and b (whole warp).
+__device__ double cos64(const uint16_t* X, int D, int a, int b, FpsShared* sh) {
+  const double na = item_norm64(X, D, a, sh), nb = item_norm64(X, D, b, sh);
+  const int lane = threadIdx.x & 31;
+  double s = 0.0;
+  for (int k = lane; k < D; k += 32)
+    s = fma(bf16d(X[static_cast<size_t>(a) * D + k]), bf16d(X[static_cast<size_t>(b) * D + k]), s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (na == 0.0 || nb == 0.0) return 0.0;
+  return s / (na * nb);
+}
+
+// FPS of m items out of the first n rows of unit u's buffer.  Writes the
+// selection order to sh->sel and returns its length.  A CTA runs at most one
+// non-trivial selection per launch (after a compress the buffer holds M
+// items and the beacon pass takes all of them), so the mbarriers start from
+// phase 0 here.
+__device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
+                          uint8_t* stages, int stage_rows, int u, int n, int m) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (m <= 0) return 0;
+  if (n <= m) {
+    for (int i = tid; i < n; i += kThreads) sh->sel[i] = i;
+    __syncthreads();
+    return n;
+  }
+  const int D = p.D;
+  const uint16_t* X = p.buf + static_cast<size_t>(u) * p.C * D;
+  const int N = (n + 15) & ~15;
+  const int nbands = (n + 127) / 128;
+  const int nchunks = D / 64;
+  const uint32_t stage_bytes = static_cast<uint32_t>(stage_rows) * 128;
+  const uint32_t box_bytes = static_cast<uint32_t>(min(stage_rows, (p.C + 15) & ~15)) * 128;
+
+  if (warp == 0) tmem_alloc(&sh->tmem_base, 512);  // no relinquish: a CTA may select twice
+  for (int i = tid; i < 256; i += kThreads) sh->norm64[i] = -1.0;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sh->tmem_base;
+
+  // ---- Gram on the tensor core (thread 0 drives TMA and MMA)
+  if (tid == 0) {
+    const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(N));
+    bool ok = true;
+    const int pro = min(kStages, nchunks);
+    for (int c = 0; c < pro; ++c) {
+      mbar_arrive_expect_tx(&sh->full[c], box_bytes);
+      tma_load_3d(stages + c * stage_bytes, bmap, &sh->full[c], 64 * c, 0, u);
+    }
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int st = c % kStages;
+      if (!wait_bar(&sh->full[st], (c / kStages) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sbase = smem_u32(stages + st * stage_bytes);
+      for (int h = 0; h < nbands; ++h)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16(tbase + h * 256, sdesc_sw128(sbase + h * 16384 + kk * 32),
+                   sdesc_sw128(sbase + kk * 32), idesc, (c | kk) != 0);
+      mma_commit(&sh->empty[st]);
+      const int cn = c + kStages;
+      if (cn < nchunks) {
+        if (!wait_bar(&sh->empty[st], (c / kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&sh->full[st], box_bytes);
+        tma_load_3d(stages + st * stage_bytes, bmap, &sh->full[st], 64 * cn, 0, u);
+      }
+    }
+    mma_commit(&sh->done);
+    if (!ok) {
+      sh->abort_flag = 1;
+      record_error(p.ws, BKV_ETIMEOUT, kSiteFpsWait);
+    }
+  }
+  __syncthreads();
+  warp_wait(&sh->done, 0, &sh->abort_flag);
+  tc_fence_after();
+  __syncthreads();
+  const bool gram_ok = sh->abort_flag == 0;  // block-uniform
+
+  // item of this thread: band h = warp / 4, TMEM lane quarter = warp % 4
+  const int h = warp >> 2, q = warp & 3;
+  const int i = tid;  // = 128 h + 32 q + lane
+  const bool band_live = h < nbands;
+  const uint32_t trow = tbase + (static_cast<uint32_t>(q * 32) << 16) + h * 256;
+  float inv_i = 0.f;
+  if (band_live) {
+    uint32_t v[32];
+    tmem_ld32(trow + 128 * h + 32 * q, v);  // diagonal block of this warp
+    tmem_wait_ld();
+    float g = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      if (k == lane) g = __uint_as_float(v[k]);
+    inv_i = (i < n && g > 0.f) ? rsqrtf(g) : 0.f;
+  }
+  sh->inv[i] = inv_i;
+  __syncthreads();
+
+  // ---- seed: lowest mean cosine to the other items
+  float mean = INFINITY;
+  if (band_live) {
+    float acc = 0.f;
+    for (int c = 0; c < (N + 31) / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(trow + c * 32, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int j = c * 32 + k;  // columns past n were never written: skip them
+        if (j < n && j != i) acc = fmaf(__uint_as_float(v[k]), sh->inv[j], acc);
+      }
+    }
+    if (i < n) mean = acc * inv_i / static_cast<float>(n - 1);
+  }
+  Top2 t = block_top2(Top2{mean, i, INFINITY}, sh);
+  int seed = t.i1;
+  if (!(t.v2 - t.v1 > 2.f * kTauMean) && gram_ok) {
+    // near-tie: re-decide among the contenders in fp64
+    if (tid == 0) sh->n_cont = 0;
+    __syncthreads();
+    if (i < n && mean <= t.v1 + 2.f * kTauMean) {
+      const int slot = atomicAdd(&sh->n_cont, 1);
+      if (slot < kMaxCont) sh->cont[slot] = i;
+    }
+    __syncthreads();
+    const int nc = min(sh->n_cont, kMaxCont);
+    for (int c = warp; c < nc; c += kWarps) {
+      const int a = sh->cont[c];
+      double s = 0.0;
+      for (int j = 0; j < n; ++j)
+        if (j != a) s += cos64(X, D, a, j, sh);
+      if (lane == 0) sh->cont_val[c] = s / static_cast<double>(n - 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int best = -1;
+      double bv = 0.0;
+      for (int c = 0; c < nc; ++c) {
+        const int a = sh->cont[c];
+        const double v = sh->cont_val[c];
+        if (best < 0 || v < bv || (v == bv && a < best)) {
+          best = a;
+          bv = v;
+        }
+      }
+      sh->winner = best;
+    }
+    __syncthreads();
+    seed = sh->winner;
+  }
+
+  // ---- greedy farthest-point steps
+  if (tid == 0) sh->sel[0] = seed;
+  bool chosen = (i == seed);
+  float dist = 1.f;
+  auto update = [&](int k) {
+    // Gram column k: this thread's entry G[i][k] (band h holds rows 128h..)
+    float gk = 0.f;
+    if (band_live) {
+      uint32_t v;
+      tmem_ld1(trow + k, v);
+      tmem_wait_ld();
+      gk = __uint_as_float(v);
+    }
+    const float c = gk * inv_i * sh->inv[k];
+    dist = fminf(dist, 1.f - c);
+  };
+  update(seed);
+  for (int k = 1; k < m; ++k) {
+    const bool live = i < n && !chosen;
+    Top2 r = block_top2(Top2{live ? -dist : INFINITY, i, INFINITY}, sh);
+    int win = r.i1;
+    if (!(r.v2 - r.v1 > 2.f * kTauCos) && gram_ok) {
+      if (tid == 0) sh->n_cont = 0;
+      __syncthreads();
+      if (live && -dist <= r.v1 + 2.f * kTauCos) {
+        const int slot = atomicAdd(&sh->n_cont, 1);
+        if (slot < kMaxCont) sh->cont[slot] = i;
+      }
+      __syncthreads();
+      const int nc = min(sh->n_cont, kMaxCont);
+      for (int c = warp; c < nc; c += kWarps) {
+        const int a = sh->cont[c];
+        double dmin = 0.0;
+        for (int s = 0; s < k; ++s) {
+          const double dv = 1.0 - cos64(X, D, a, sh->sel[s], sh);
+          dmin = (s == 0) ? dv : fmin(dmin, dv);
+        }
+        if (lane == 0) sh->cont_val[c] = dmin;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int best = -1;
+        double bv = 0.0;
+        for (int c = 0; c < nc; ++c) {
+          const int a = sh->cont[c];
+          const double v = sh->cont_val[c];
+          if (best < 0 || v > bv || (v == bv && a < best)) {
+            best = a;
+            bv = v;
+          }
+        }
+        sh->winner = best;
+      }
+      __syncthreads();
+      win = sh->winner;
+    }
+    if (tid == 0) sh->sel[k] = win;
+    chosen = chosen || (i == win);
+    update(win);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, 512);
+  return m;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fps_update_kernel(const __grid_constant__ FpsParams p,
+                      const __grid_constant__ CUtensorMap bmap, int stage_rows) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // TMA destinations with the 128-byte swizzle need 1024-byte alignment
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+  FpsShared* sh = reinterpret_cast<FpsShared*>(stages + kStages * stage_rows * 128);
+  const int u = blockIdx.x, tid = threadIdx.x;
+  const int D = p.D;
+  uint16_t* buf = p.buf + static_cast<size_t>(u) * p.C * D;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], 1);
+    }
+    mbar_init(&sh->done, 1);
+    sh->abort_flag = 0;
+    fence_mbar_init();
+  }
+  int c = p.cnt[u];
+  const bool ok_state = c >= 0 && c < p.C;
+  if (!ok_state) {
+    if (tid == 0) record_error(p.ws, BKV_EDEVICE, kSiteFpsState);
+    c = 0;
+  }
+  // ---- 1. append the step's query to the ring and the buffer
+  if (p.q_new != nullptr && ok_state) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.q_new + static_cast<size_t>(u) * D);
+    uint4* ring = p.W > 0 ? reinterpret_cast<uint4*>(
+                                p.recent_q + (static_cast<size_t>(u) * p.W +
+                                              static_cast<size_t>(p.step % p.W)) * D)
+                          : nullptr;
+    uint4* dst = reinterpret_cast<uint4*>(buf + static_cast<size_t>(c) * D);
+    for (int k = tid; k < D / 8; k += kThreads) {
+      const uint4 v = src[k];
+      if (ring != nullptr) ring[k] = v;
+      dst[k] = v;
+    }
+    c += 1;
+  }
+  fence_proxy_async();  // generic writes to the buffer -> later TMA reads
+  __syncthreads();
+
+  // ---- 2. compress a full buffer to its FPS survivors, in slot order
+  if (ok_state && c == p.C) {
+    const int got = fps_select(p, &bmap, sh, stages, stage_rows, u, c, p.M);
+    if (tid == 0) {
+      for (int k = 0; k < got; ++k) sh->surv[k] = sh->sel[k];
+      for (int a = 1; a < got; ++a) {  // insertion sort, got <= 64
+        const int v = sh->surv[a];
+        int b = a - 1;
+        while (b >= 0 && sh->surv[b] > v) {
+          sh->surv[b + 1] = sh->surv[b];
+          --b;
+        }
+        sh->surv[b + 1] = v;
+      }
+    }
+    __syncthreads();
+    // row k <- row surv[k] (surv ascending, surv[k] >= k): batches read into
+    // shared memory first, then written
+    const int row_vec = D / 8;  // uint4 per row
+    const int batch = max(1, static_cast<int>((kStages * stage_rows * 128) / (D * 2)));
+    uint4* tmp = reinterpret_cast<uint4*>(stages);
+    for (int k0 = 0; k0 < got; k0 += batch) {
+      const int k1 = min(got, k0 + batch);
+      for (int e = tid; e < (k1 - k0) * row_vec; e += kThreads) {
+        const int k = k0 + e / row_vec, v = e % row_vec;
+        tmp[e] = reinterpret_cast<const uint4*>(buf + static_cast<size_t>(sh->surv[k]) * D)[v];
+      }
+      __syncthreads();
+      for (int e = tid; e < (k1 - k0) * row_vec; e += kThreads) {
+        const int k = k0 + e / row_vec, v = e % row_vec;
+        reinterpret_cast<uint4*>(buf + static_cast<size_t>(k) * D)[v] = tmp[e];
+      }
+      __syncthreads();
+    }
+    c = got;
+    fence_proxy_async();
+    __syncthreads();
+  }
+
+  // ---- 3. beacons: FPS over the current buffer (read-only)
+  if (p.want_beacons) {
+    const int got = ok_state ? fps_select(p, &bmap, sh, stages, stage_rows, u, c, p.M) : 0;
+    __syncthreads();
+    if (p.beacon_idx != nullptr)
+      for (int k = tid; k < p.M; k += kThreads)
+        p.beacon_idx[static_cast<size_t>(u) * p.M + k] = k < got ? sh->sel[k] : -1;
+    if (p.beacons != nullptr) {
+      const int row_vec = D / 8;
+      for (int e = tid; e < got * row_vec; e += kThreads) {
+        const int k = e / row_vec, v = e % row_vec;
+        reinterpret_cast<uint4*>(p.beacons + (static_cast<size_t>(u) * p.M + k) * D)[v] =
+            reinterpret_cast<const uint4*>(buf + static_cast<size_t>(sh->sel[k]) * D)[v];
+      }
+    }
+    if (p.n_beacons != nullptr && tid == 0) p.n_beacons[u] = got;
+  }
+  if (tid == 0 && ok_state) p.cnt[u] = c;
+}
+
+}  // namespace
+
+// Stage rows cover every row a 128-row MMA band reads (one band up to C =
+// 128, two bands beyond).
+int fps_stage_rows(int C) { return C <= 128 ? 128 : 256; }
+
+// At least 120 KB so that one CTA holds an SM (each takes all 512 TMEM columns).
+size_t fps_smem_bytes(int C) {
+  const size_t need =
+      1024 + static_cast<size_t>(kStages) * fps_stage_rows(C) * 128 + sizeof(FpsShared);
+  return need < 120 * 1024 ? 120 * 1024 : need;
+}
+
+cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, cudaStream_t st) {
+  const int rows = fps_stage_rows(p.C);
+  const size_t smem = fps_smem_bytes(p.C);
+  cudaError_t e = cudaFuncSetAttribute(fps_update_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  fps_update_kernel<<<p.U, kThreads, smem, st>>>(p, bufmap, rows);
+  return cudaGetLastError();
+}
+
+}  // namespace bkv

@@ -1,0 +1,72 @@
+// Launch interfaces of the eviction-step kernels (internal to libbkv).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace bkv {
+
+struct WsHeader;
+
+// ------------------------------------------------------------------ score
+struct ScoreParams {
+  const int32_t* L;
+  const int32_t* kpos;
+  const uint16_t* recent_q;
+  const uint16_t* beacons;
+  const int32_t* n_beacons;
+  const int32_t* cur_pos;
+  float* scores;
+  float2* part;  // [U][nsplit][nrows_part] (running max, sum of exp2), log2 units
+  WsHeader* ws;
+  int64_t step;
+  int32_t U, G, d, W, M, L_cap;
+  int32_t NQ;               // (W + M) * G scoring rows
+  int32_t NQ16;             // NQ rounded up to 16
+  int32_t nrows_part;       // NQ rounded up to 128 (pass-1 row blocks)
+  int32_t ngrp;             // pass-2 row groups of <= 256
+  int32_t nsplit;           // key-range splits per unit
+  int32_t tiles_per_split;  // 128-key tiles per split
+  int32_t agg, causal;
+  float qscale;             // log2(e) / sqrt(d)
+  float freq_hi[64];        // theta^(-2i/d) = freq_hi + freq_lo
+  float freq_lo[64];
+};
+
+cudaError_t launch_score(const ScoreParams& p, const CUtensorMap& kmap, cudaStream_t st);
+size_t score_smem_bytes(int d, int NQ16, int W);
+
+// --------------------------------------------------------- select+compact
+struct SelectParams {
+  const float* scores;
+  uint8_t* K;
+  uint8_t* V;
+  int32_t* kpos;
+  int32_t* L;
+  int32_t* kept;       // optional [U][B]
+  int32_t* unit_done;  // [U] counters in the workspace (start at 0)
+  WsHeader* ws;
+  int32_t U, L_cap, B, R, row_bytes;
+};
+
+cudaError_t launch_select_compact(const SelectParams& p, cudaStream_t st);
+
+// ---------------------------------------------------------------- FPS
+struct FpsParams {
+  const uint16_t* q_new;  // [U][D] or null
+  uint16_t* recent_q;     // [U][W][D]
+  uint16_t* buf;          // [U][C][D]
+  int32_t* cnt;
+  int32_t* beacon_idx;    // [U][M] or null
+  uint16_t* beacons;      // [U][M][D] or null
+  int32_t* n_beacons;     // [U] or null
+  WsHeader* ws;
+  int64_t step;
+  int32_t U, D, W, M, C;
+  int32_t want_beacons;
+};
+
+cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, cudaStream_t st);
+
+}  // namespace bkv

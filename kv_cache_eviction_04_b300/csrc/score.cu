@@ -1,0 +1,586 @@
+// Eviction scoring: per-key max (or mean) over (query, head) rows of the
+// softmax attention of the W recent queries and the M beacons.
+//
+// BeaconKV pages: wzjinhao.cn explainer, section "信标查询怎么用：位置对齐与打分
+// 策略" -- beacons are rotated to the current decode position, recent queries
+// keep the positions they were generated at, and a key's importance is the
+// maximum over queries (max beats mean); inkeast.github.io reading, section
+// 三, scoring with the union of recent and beacon queries.
+//
+// Two launches per call, both tcgen05 kernels fed by TMA:
+//   score_stats  (pass 1): rows on the 128 TMEM lanes, keys on the columns:
+//                D = Q * K^T; each thread owns one row and keeps a running
+//                max and sum of exp2 over its keys -> per-split (m, z).
+//   score_final  (pass 2): keys on the TMEM lanes, rows on the columns:
+//                D = K * Q^T; each thread owns one key, merges the splits'
+//                (m, z) into each row's log-sum-exp and takes the max (or
+//                mean) of the normalised probability over rows in registers.
+// Queries are rotated in fp32 (angles reduced in extended precision) and
+// carried as q = q_hi + q_lo, two bf16 terms; both terms run through the
+// tensor core into one fp32 accumulator, so the logits carry ~2^-17
+// relative query error instead of bf16's 2^-9.  Logits are kept in log2
+// units (log2(e)/sqrt(d) is folded into the queries).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bkv {
+namespace {
+
+constexpr int kThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kEpiThreads = 128;
+constexpr int kTileKeys = 128;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Every lane of the warp waits on `bar`; the verdict is warp-uniform.  Once
+// any wait of the CTA has timed out (`abort` set) later waits fail at once,
+// so every role drains its loop without blocking and all threads still meet
+// at the CTA's barriers.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* abort) {
+  bool ok = *reinterpret_cast<volatile int32_t*>(abort) == 0 && wait_bar(bar, parity);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) *reinterpret_cast<volatile int32_t*>(abort) = 1;
+  return ok;
+}
+
+// Reduce a position-times-frequency product to [-pi, pi] in fp32 with
+// extra precision: the product is split into a rounded part and its exact
+// error (fma), and 2*pi is subtracted in three pieces (Cody and Waite,
+// "Software Manual for the Elementary Functions", 1980).  Valid for
+// positions below 2^24 and frequencies <= 1.
+__device__ __forceinline__ float reduce_angle(float pos, float f_hi, float f_lo) {
+  const float ph = pos * f_hi;
+  const float pe = fmaf(pos, f_hi, -ph);
+  const float pl = pos * f_lo;
+  const float k = rintf(ph * 0.15915494309189535f);
+  // 2*pi = A + B + C, A with 8 significant bits so that k * A is exact
+  constexpr float A = 6.28125f;
+  constexpr float B = 1.9353071693331003e-03f;   // fp32(2*pi - A)
+  constexpr float Cc = 1.0253376273028358e-11f;  // fp32(2*pi - A - B)
+  float r = fmaf(-k, A, ph);
+  r = fmaf(-k, B, r);
+  r = fmaf(-k, Cc, r);
+  return r + (pe + pl);
+}
+
+// Row metadata: row r = item * G + g; items 0..W-1 are ring slots, the
+// rest beacons.  Returns the row's position, or INT32_MIN when the row is
+// empty (ring slot never written, beacon past n_beacons, padding).
+__device__ __forceinline__ int row_position(const ScoreParams& p, int u, int r, int nb,
+                                            int32_t cur) {
+  if (r >= p.NQ) return INT32_MIN;
+  const int item = r / p.G;
+  if (item < p.W) {
+    const int64_t age = ((p.step - item) % p.W + p.W) % p.W;
+    if (age > p.step) return INT32_MIN;
+    return cur - static_cast<int32_t>(age);
+  }
+  return (item - p.W < nb) ? cur : INT32_MIN;
+}
+
+// Build the rotated, scaled, hi/lo-split query operand for rows
+// [row0, row0 + nrows) in two K-major 128B-swizzled smem images.  Run by
+// `nthr` threads with ids tid in [0, nthr); ends with named barrier `bar`.
+template <int D>
+__device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, uint8_t* q_hi,
+                              uint8_t* q_lo, int32_t* row_pos, float2* cs, int tid, int nthr,
+                              int bar) {
+  constexpr int H = D / 2;
+  const int32_t cur = p.cur_pos[u];
+  const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
+  const int nage = max(p.W, 1);
+  // cos/sin of every (age, frequency); age 0 is the current position
+  for (int idx = tid; idx < nage * H; idx += nthr) {
+    const int age = idx / H, i = idx % H;
+    const float a = reduce_angle(static_cast<float>(cur - age), p.freq_hi[i], p.freq_lo[i]);
+    float s, c;
+    sincosf(a, &s, &c);
+    cs[idx] = make_float2(c, s);
+  }
+  for (int r = tid; r < nrows; r += nthr) row_pos[r] = row_position(p, u, row0 + r, nb, cur);
+  named_sync(bar, nthr);
+  // one thread per (row, pair of 8 consecutive rotary pairs)
+  constexpr int kGroups = H / 8;
+  for (int idx = tid; idx < nrows * kGroups; idx += nthr) {
+    const int r = idx / kGroups, grp = idx % kGroups;
+    const int rr = row0 + r;
+    const int32_t pos = row_pos[r];
+    uint16_t hi0[8], hi1[8], lo0[8], lo1[8];
+    if (pos == INT32_MIN) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) hi0[k] = hi1[k] = lo0[k] = lo1[k] = 0;
+    } else {
+      const int item = rr / p.G, g = rr % p.G;
+      const uint16_t* src;
+      if (item < p.W)
+        src = p.recent_q + ((static_cast<size_t>(u) * p.W + item) * p.G + g) * D;
+      else
+        src = p.beacons + ((static_cast<size_t>(u) * p.M + (item - p.W)) * p.G + g) * D;
+      const int age = cur - pos;
+      const uint4 va = *reinterpret_cast<const uint4*>(src + grp * 8);
+      const uint4 vb = *reinterpret_cast<const uint4*>(src + H + grp * 8);
+      const uint16_t* a16 = reinterpret_cast<const uint16_t*>(&va);
+      const uint16_t* b16 = reinterpret_cast<const uint16_t*>(&vb);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = grp * 8 + k;
+        const float2 csv = cs[age * H + i];
+        const float x0 = bf16_bits_to_float(a16[k]), x1 = bf16_bits_to_float(b16[k]);
+        const float y0 = (x0 * csv.x - x1 * csv.y) * p.qscale;
+        const float y1 = (x1 * csv.x + x0 * csv.y) * p.qscale;
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(y0 - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(y1 - __bfloat162float(h1));
+        hi0[k] = __bfloat16_as_ushort(h0);
+        hi1[k] = __bfloat16_as_ushort(h1);
+        lo0[k] = __bfloat16_as_ushort(l0);
+        lo1[k] = __bfloat16_as_ushort(l1);
+      }
+    }
+    // 8 consecutive elements = one 16-byte chunk of the swizzled image
+    const uint32_t o0 = sw128_offset(r, grp * 8, nrows);
+    const uint32_t o1 = sw128_offset(r, H + grp * 8, nrows);
+    *reinterpret_cast<uint4*>(q_hi + o0) = *reinterpret_cast<const uint4*>(hi0);
+    *reinterpret_cast<uint4*>(q_hi + o1) = *reinterpret_cast<const uint4*>(hi1);
+    *reinterpret_cast<uint4*>(q_lo + o0) = *reinterpret_cast<const uint4*>(lo0);
+    *reinterpret_cast<uint4*>(q_lo + o1) = *reinterpret_cast<const uint4*>(lo1);
+  }
+  fence_proxy_async_shared();  // generic smem writes -> visible to the tensor core
+  named_sync(bar, nthr);
+}
+
+struct __align__(8) Barriers {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t minpos;
+  int32_t pad;
+};
+
+// Key tile range of split `s` for unit u.
+__device__ __forceinline__ void split_tiles(const ScoreParams& p, int u, int s, int& t0, int& t1,
+                                            int& L) {
+  L = p.L[u];
+  if (L < 0 || L > p.L_cap) {
+    if (threadIdx.x == 0) record_error(p.ws, BKV_EDEVICE, kSiteScoreState);
+    L = 0;
+  }
+  const int nt = (L + kTileKeys - 1) / kTileKeys;
+  t0 = min(s * p.tiles_per_split, nt);
+  t1 = min(t0 + p.tiles_per_split, nt);
+}
+
+__device__ __forceinline__ void init_barriers(Barriers* bars, int ns) {
+  for (int i = 0; i < ns; ++i) {
+    mbar_init(&bars->full[i], 1);
+    mbar_init(&bars->empty[i], 1);
+  }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&bars->tfull[i], 1);
+    mbar_init(&bars->tempty[i], 4);  // one arrival per epilogue warp
+  }
+  bars->abort_flag = 0;
+  bars->minpos = INT32_MAX;
+  fence_mbar_init();
+}
+
+// TMA producer (one elected lane of warp 0): stream the split's key tiles.
+template <int D, int NS>
+__device__ void produce_tiles(const ScoreParams& p, const CUtensorMap* kmap, Barriers* bars,
+                              uint8_t* stages, int u, int t0, int ntl) {
+  constexpr uint32_t kStageBytes = kTileKeys * D * 2;
+  prefetch_tmap(kmap);
+  for (int i = 0; i < ntl; ++i) {
+    const int st = i % NS;
+    if (*reinterpret_cast<volatile int32_t*>(&bars->abort_flag) != 0 ||
+        !wait_bar(&bars->empty[st], ((i / NS) & 1) ^ 1)) {
+      bars->abort_flag = 1;
+      record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+      return;
+    }
+    mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
+    const int j0 = (t0 + i) * kTileKeys;
+#pragma unroll
+    for (int a = 0; a < D / 64; ++a)
+      tma_load_3d(stages + st * kStageBytes + a * 16384, kmap, &bars->full[st], 64 * a, j0, u);
+  }
+}
+
+// --------------------------------------------------------------- pass 1
+template <int D, int NS>
+__global__ void __launch_bounds__(kThreads, 1)
+    score_stats_kernel(const __grid_constant__ ScoreParams p,
+                       const __grid_constant__ CUtensorMap kmap) {
+  constexpr uint32_t kQBytes = 128 * D * 2;  // one 128-row operand image
+  constexpr uint32_t kStageBytes = kTileKeys * D * 2;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, kTileKeys);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* q_hi = smem;
+  uint8_t* q_lo = q_hi + kQBytes;
+  uint8_t* stages = q_lo + kQBytes;
+  Barriers* bars = reinterpret_cast<Barriers*>(stages + NS * kStageBytes);
+  int32_t* row_pos = reinterpret_cast<int32_t*>(bars + 1);  // [128]
+  int32_t* kp = row_pos + 128;                              // [128]
+  float2* cs = reinterpret_cast<float2*>(kp + 128);         // [max(W,1)][D/2]
+
+  const int s = blockIdx.x, rb = blockIdx.y, u = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int t0, t1, L;
+  split_tiles(p, u, s, t0, t1, L);
+  const int ntl = t1 - t0;
+
+  if (threadIdx.x == 0) init_barriers(bars, NS);
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 2 * kTileKeys);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+
+  if (warp == 0) {
+    if (elect_one()) produce_tiles<D, NS>(p, &kmap, bars, stages, u, t0, ntl);
+  } else {
+    build_queries<D>(p, u, rb * 128, 128, q_hi, q_lo, row_pos, cs, threadIdx.x - 32,
+                     kThreads - 32, 1);
+    if (warp == 1) {
+      // ---------------- MMA issuer: D[row][key] = sum_k Q[row][k] K[key][k]
+      for (int i = 0; i < ntl; ++i) {
+        const int st = i % NS, b = i & 1;
+        if (!warp_wait(&bars->full[st], (i / NS) & 1, &bars->abort_flag) ||
+            !warp_wait(&bars->tempty[b], ((i >> 1) & 1) ^ 1, &bars->abort_flag)) {
+          if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t dt = tbase + b * kTileKeys;
+          const uint32_t kbase = smem_u32(stages + st * kStageBytes);
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t qbase = smem_u32(part ? q_lo : q_hi);
+#pragma unroll
+            for (int a = 0; a < D / 64; ++a)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(dt, sdesc_sw128(qbase + a * 16384 + kk * 32),
+                         sdesc_sw128(kbase + a * 16384 + kk * 32), kIdesc,
+                         (part | a | kk) != 0);
+          }
+          mma_commit(&bars->empty[st]);
+          mma_commit(&bars->tfull[b]);
+        }
+        __syncwarp();
+      }
+    } else {
+      // ---------------- epilogue: thread = one row; running max / sum of exp2
+      const int q = warp & 3;
+      const int et = threadIdx.x - 64;  // 0..127
+      const int lrow = q * 32 + lane;   // TMEM lane = row within the block
+      const int32_t rpos = row_pos[lrow];
+      const int32_t lim = (p.causal || rpos == INT32_MIN) ? rpos : INT32_MAX - 1;
+      float m = -INFINITY, z = 0.f;
+      for (int i = 0; i < ntl; ++i) {
+        const int b = i & 1;
+        const int j = (t0 + i) * kTileKeys + et;
+        kp[et] = j < L ? p.kpos[static_cast<size_t>(u) * p.L_cap + j] : INT32_MAX;
+        named_sync(2, kEpiThreads);
+        if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < kTileKeys / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + (static_cast<uint32_t>(q * 32) << 16) + b * kTileKeys + c * 32, v);
+            tmem_wait_ld();
+            if (c == kTileKeys / 32 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->tempty[b]);
+            }
+            const int4* kp4 = reinterpret_cast<const int4*>(kp + c * 32);
+            float t[32];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int k4 = 0; k4 < 8; ++k4) {
+              const int4 kk = kp4[k4];
+              const int kv[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int k = k4 * 4 + e;
+                t[k] = (kv[e] <= lim) ? __uint_as_float(v[k]) : -INFINITY;
+                mx = fmaxf(mx, t[k]);
+              }
+            }
+            const float mn = fmaxf(m, mx);
+            if (mn != -INFINITY) {
+              float acc = (m == -INFINITY) ? 0.f : z * ex2(m - mn);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) acc += ex2(t[k] - mn);
+              z = acc;
+              m = mn;
+            }
+          }
+        } else if (lane == 0) {
+          record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+        }
+        named_sync(2, kEpiThreads);  // kp is rewritten by the next tile
+      }
+      const int row = rb * 128 + lrow;
+      p.part[(static_cast<size_t>(u) * p.nsplit + s) * p.nrows_part + row] = make_float2(m, z);
+      // several row groups combine through atomics in pass 2: start from 0
+      if (p.ngrp > 1 && rb == 0)
+        for (int jj = t0 * kTileKeys + et; jj < min(t1 * kTileKeys, L); jj += kEpiThreads)
+          p.scores[static_cast<size_t>(u) * p.L_cap + jj] = 0.f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 2 * kTileKeys);
+}
+
+// --------------------------------------------------------------- pass 2
+template <int D, int NS, int NMAX>
+__global__ void __launch_bounds__(kThreads, 1)
+    score_final_kernel(const __grid_constant__ ScoreParams p,
+                       const __grid_constant__ CUtensorMap kmap) {
+  constexpr uint32_t kStageBytes = kTileKeys * D * 2;
+  constexpr uint32_t kCols = NMAX <= 128 ? 256 : 512;  // two accumulator buffers
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int s = blockIdx.x, grp = blockIdx.y, u = blockIdx.z;
+  const int row0 = grp * 256;
+  const int N = min(256, p.NQ16 - row0);  // rows of this group, a multiple of 16
+  uint8_t* q_hi = smem;
+  uint8_t* q_lo = q_hi + NMAX * D * 2;
+  uint8_t* stages = q_lo + NMAX * D * 2;
+  Barriers* bars = reinterpret_cast<Barriers*>(stages + NS * kStageBytes);
+  int32_t* row_pos = reinterpret_cast<int32_t*>(bars + 1);  // [256]
+  float* lse = reinterpret_cast<float*>(row_pos + 256);      // [256]
+  float2* cs = reinterpret_cast<float2*>(lse + 256);         // [max(W,1)][D/2]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int t0, t1, L;
+  split_tiles(p, u, s, t0, t1, L);
+  const int ntl = t1 - t0;
+
+  if (threadIdx.x == 0) init_barriers(bars, NS);
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+
+  if (warp == 0) {
+    if (elect_one()) produce_tiles<D, NS>(p, &kmap, bars, stages, u, t0, ntl);
+  } else {
+    const int tid = threadIdx.x - 32, nthr = kThreads - 32;
+    build_queries<D>(p, u, row0, N, q_hi, q_lo, row_pos, cs, tid, nthr, 1);
+    // merge the per-split (max, sum) of each row into its log2-sum-exp
+    for (int r = tid; r < N; r += nthr) {
+      const int row = row0 + r;
+      float l = INFINITY;  // empty rows: every probability is 0
+      if (row_pos[r] != INT32_MIN) {
+        const float2* pr = p.part + static_cast<size_t>(u) * p.nsplit * p.nrows_part + row;
+        float mm = -INFINITY;
+        for (int k = 0; k < p.nsplit; ++k)
+          mm = fmaxf(mm, pr[static_cast<size_t>(k) * p.nrows_part].x);
+        float zz = 0.f;
+        if (mm != -INFINITY)
+          for (int k = 0; k < p.nsplit; ++k) {
+            const float2 mz = pr[static_cast<size_t>(k) * p.nrows_part];
+            if (mz.x != -INFINITY) zz += mz.y * ex2(mz.x - mm);
+          }
+        if (zz > 0.f) l = mm + lg2(zz);
+        atomicMin(&bars->minpos, row_pos[r]);
+        if (!p.causal) row_pos[r] = INT32_MAX;
+      }
+      lse[r] = l;
+    }
+    named_sync(1, nthr);
+    if (warp == 1) {
+      // ---------------- MMA issuer: D[key][row] = sum_k K[key][k] Q[row][k]
+      const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(N));
+      for (int i = 0; i < ntl; ++i) {
+        const int st = i % NS, b = i & 1;
+        if (!warp_wait(&bars->full[st], (i / NS) & 1, &bars->abort_flag) ||
+            !warp_wait(&bars->tempty[b], ((i >> 1) & 1) ^ 1, &bars->abort_flag)) {
+          if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t dt = tbase + b * (kCols / 2);
+          const uint32_t kbase = smem_u32(stages + st * kStageBytes);
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t qbase = smem_u32(part ? q_lo : q_hi);
+#pragma unroll
+            for (int a = 0; a < D / 64; ++a)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(dt, sdesc_sw128(kbase + a * 16384 + kk * 32),
+                         sdesc_sw128(qbase + a * (N * 128) + kk * 32), idesc,
+                         (part | a | kk) != 0);
+          }
+          mma_commit(&bars->empty[st]);
+          mma_commit(&bars->tfull[b]);
+        }
+        __syncwarp();
+      }
+    } else {
+      // ---------------- epilogue: thread = one key
+      const int q = warp & 3;
+      const int32_t minpos = bars->minpos;
+      const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
+      const int nrec = p.step + 1 < p.W ? static_cast<int>(p.step + 1) : p.W;
+      const float inv_rows = 1.f / static_cast<float>(max((nrec + nb) * p.G, 1));
+      const int nchunks = (N + 31) / 32;
+      for (int i = 0; i < ntl; ++i) {
+        const int b = i & 1;
+        const int j = (t0 + i) * kTileKeys + q * 32 + lane;
+        const int32_t kpj = j < L ? p.kpos[static_cast<size_t>(u) * p.L_cap + j] : INT32_MAX;
+        if (!warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
+          if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+          continue;
+        }
+        tc_fence_after();
+        const bool nomask = __all_sync(0xffffffffu, kpj <= minpos);
+        float best = -INFINITY, acc = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + (static_cast<uint32_t>(q * 32) << 16) + b * (kCols / 2) + c * 32, v);
+          tmem_wait_ld();
+          if (c == nchunks - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[b]);
+          }
+          const int nv = min(32, N - c * 32);
+          const float4* l4 = reinterpret_cast<const float4*>(lse + c * 32);
+          const int4* p4 = reinterpret_cast<const int4*>(row_pos + c * 32);
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4) {
+            if (k4 * 4 < nv) {
+              const float4 lv = l4[k4];
+              const int4 pv = p4[k4];
+              const float ll[4] = {lv.x, lv.y, lv.z, lv.w};
+              const int pp[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float x = __uint_as_float(v[k4 * 4 + e]) - ll[e];
+                if (!nomask && kpj > pp[e]) x = -INFINITY;
+                if (p.agg == BKV_AGG_MAX)
+                  best = fmaxf(best, x);
+                else
+                  acc += ex2(x);
+              }
+            }
+          }
+        }
+        if (j < L) {
+          float* dst = p.scores + static_cast<size_t>(u) * p.L_cap + j;
+          if (p.agg == BKV_AGG_MAX) {
+            const float sc = best == -INFINITY ? 0.f : ex2(best);
+            if (p.ngrp > 1)
+              atomicMax(reinterpret_cast<int*>(dst), __float_as_int(sc));
+            else
+              *dst = sc;
+          } else {
+            const float sc = acc * inv_rows;
+            if (p.ngrp > 1)
+              atomicAdd(dst, sc);
+            else
+              *dst = sc;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, kCols);
+}
+
+template <int D, int NS>
+size_t stats_smem(int W) {
+  return 1024 + 2 * 128 * D * 2 + NS * kTileKeys * D * 2 + sizeof(Barriers) + 128 * 4 + 128 * 4 +
+         static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
+}
+template <int D, int NS, int NMAX>
+size_t final_smem(int W) {
+  return 1024 + 2 * NMAX * D * 2 + NS * kTileKeys * D * 2 + sizeof(Barriers) + 256 * 4 +
+         256 * 4 + static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
+}
+
+template <typename Kern>
+cudaError_t launch(Kern kernel, dim3 grid, size_t smem, cudaStream_t st, const ScoreParams& p,
+                   const CUtensorMap& map) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads, smem, st>>>(p, map);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t score_smem_bytes(int d, int NQ16, int W) {
+  const bool small = NQ16 <= 128;
+  if (d == 128) {
+    const size_t a = stats_smem<128, 3>(W);
+    const size_t b = small ? final_smem<128, 3, 128>(W) : final_smem<128, 2, 256>(W);
+    return a > b ? a : b;
+  }
+  const size_t a = stats_smem<64, 4>(W);
+  const size_t b = small ? final_smem<64, 4, 128>(W) : final_smem<64, 4, 256>(W);
+  return a > b ? a : b;
+}
+
+cudaError_t launch_score(const ScoreParams& p, const CUtensorMap& kmap, cudaStream_t st) {
+  const dim3 g1(p.nsplit, p.nrows_part / 128, p.U);
+  const dim3 g2(p.nsplit, p.ngrp, p.U);
+  const bool small = p.NQ16 <= 128;
+  cudaError_t e;
+  if (p.d == 128) {
+    e = launch(score_stats_kernel<128, 3>, g1, stats_smem<128, 3>(p.W), st, p, kmap);
+    if (e != cudaSuccess) return e;
+    if (small)
+      return launch(score_final_kernel<128, 3, 128>, g2, final_smem<128, 3, 128>(p.W), st, p,
+                    kmap);
+    return launch(score_final_kernel<128, 2, 256>, g2, final_smem<128, 2, 256>(p.W), st, p,
+                  kmap);
+  }
+  e = launch(score_stats_kernel<64, 4>, g1, stats_smem<64, 4>(p.W), st, p, kmap);
+  if (e != cudaSuccess) return e;
+  if (small)
+    return launch(score_final_kernel<64, 4, 128>, g2, final_smem<64, 4, 128>(p.W), st, p, kmap);
+  return launch(score_final_kernel<64, 4, 256>, g2, final_smem<64, 4, 256>(p.W), st, p, kmap);
+}
+
+}  // namespace bkv

@@ -1,0 +1,323 @@
+"""GPU parity: every kernel of the eviction step against the CPU oracle, on
+seeded synthetic inputs, through the C ABI.
+
+Bars: FPS indices, kept lists (decided on the same fp32 scores) and the
+compacted cache bit-exact; scores within 1e-6 + 2e-3 |oracle|; kept sets
+equal to the oracle's own except at keys within 1e-4 relative of its
+B_KV-th score.
+"""
+import numpy as np
+import pytest
+
+from kv_cache_eviction_04_b300 import workload as wl
+from tests.conftest import gpu_available
+
+pytestmark = pytest.mark.gpu
+
+if gpu_available():
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import oracle
+    from kv_cache_eviction_04_b300 import bkv
+    from tests.gpu_util import (DeviceState, dev, host_u16, kept_sets_agree,
+                                score_tol_excess)
+
+
+def _unit(units, u):
+    return {k: (v[u] if getattr(v, "ndim", 0) else v) for k, v in units.items()}
+
+
+# ------------------------------------------------------------------ select
+
+
+def _select_case(rng, U, d, L_cap, B, R, Ls, tie_frac=0.3):
+    scores = rng.random((U, L_cap), dtype=np.float32)
+    for u in range(U):
+        if tie_frac:
+            m = rng.random(L_cap) < tie_frac
+            scores[u, m] = np.float32(0.25)
+    scores[0, :5] = -0.0
+    K = rng.integers(0, 2 ** 16, size=(U, L_cap, d), dtype=np.uint16)
+    V = rng.integers(0, 2 ** 16, size=(U, L_cap, d), dtype=np.uint16)
+    kpos = np.tile(np.arange(L_cap, dtype=np.int32), (U, 1)) * 3
+    return scores, K, V, kpos, np.array(Ls, dtype=np.int32)
+
+
+@pytest.mark.parametrize("d,L_cap,B,R", [(128, 2176, 2048, 16), (64, 512, 128, 16),
+                                         (128, 1000, 300, 0), (128, 700, 64, 64),
+                                         (64, 4224, 4096, 16), (128, 5000, 200, 7)])
+def test_select_compact_bit_exact(d, L_cap, B, R):
+    rng = np.random.default_rng(d + L_cap + B + R)
+    U = 9
+    Ls = [L_cap, B, B + 1, max(0, B - 5), 0, L_cap - 1, min(L_cap, B + 129), R, L_cap]
+    scores, K, V, kpos, L = _select_case(rng, U, d, L_cap, B, R, Ls)
+    dims = bkv.Dims.make(U, 1, d, 16, 16, 64, B, R, L_cap, 1e4)
+    ws = bkv.make_workspace(dims)
+    tK, tV, tp, tL, ts = dev(K), dev(V), dev(kpos), dev(L), dev(scores)
+    kept = torch.zeros((U, B), dtype=torch.int32, device="cuda")
+    bkv.select_compact(dims, ts, tK, tV, tp, tL, kept, ws)
+    assert bkv.get_status(ws) == 0
+    Kg, Vg, pg, Lg, kg = host_u16(tK), host_u16(tV), tp.cpu().numpy(), tL.cpu().numpy(), \
+        kept.cpu().numpy()
+    for u in range(U):
+        ref = oracle.select(scores[u].astype(np.float64), B, R, int(L[u]))
+        n = ref.size
+        assert Lg[u] == n
+        assert np.array_equal(kg[u, :n], ref)
+        assert np.all(kg[u, n:] == -1)
+        assert np.array_equal(Kg[u, :n], K[u][ref])
+        assert np.array_equal(Vg[u, :n], V[u][ref])
+        assert np.array_equal(pg[u, :n], kpos[u][ref])
+
+
+def test_select_compact_dense_eviction_and_repeat():
+    """Keep a small fraction of a long cache (most rows move far), twice in
+    a row on the same workspace."""
+    rng = np.random.default_rng(3)
+    U, d, L_cap, B, R = 5, 128, 8192, 512, 16
+    scores, K, V, kpos, L = _select_case(rng, U, d, L_cap, B, R, [L_cap] * U, tie_frac=0)
+    dims = bkv.Dims.make(U, 1, d, 16, 16, 64, B, R, L_cap, 1e4)
+    ws = bkv.make_workspace(dims)
+    tK, tV, tp, tL, ts = dev(K), dev(V), dev(kpos), dev(L), dev(scores)
+    bkv.select_compact(dims, ts, tK, tV, tp, tL, None, ws)
+    bkv.select_compact(dims, ts, tK, tV, tp, tL, None, ws)  # L <= B now: no-op
+    assert bkv.get_status(ws) == 0
+    Kg, Lg = host_u16(tK), tL.cpu().numpy()
+    for u in range(U):
+        ref = oracle.select(scores[u].astype(np.float64), B, R)
+        assert Lg[u] == B
+        assert np.array_equal(Kg[u, :B], K[u][ref])
+
+
+# ------------------------------------------------------------------- score
+
+
+def _score_check(cfg, units, ustate, agg="max", causal=True):
+    st = ustate
+    sg = st.scores.cpu().numpy().astype(np.float64)
+    worst = -1.0
+    for u in range(st.U):
+        un = _unit(units, u)
+        nb = int(st.nb[u])
+        beac = host_u16(st.beac[u])[:nb]
+        ref = oracle.score(un["K"], un["kpos"], host_u16(st.ring[u]), st.step, beac,
+                           int(un["cur_pos"]), cfg.theta, agg, causal, L=int(un["L"]))
+        worst = max(worst, score_tol_excess(sg[u, : int(un["L"])], ref))
+    assert worst <= 0, f"score parity: worst excess over tolerance {worst:.3g}"
+
+
+def _upload_oracle_beacons(st, units, cfg):
+    """Give the device state the oracle's beacons (isolates scoring)."""
+    for u in range(st.U):
+        un = _unit(units, u)
+        cb = oracle.ContinualBuffer.from_state(un["buf"], int(un["cnt"]), cfg.M)
+        idx, vec = cb.beacons()
+        st.nb[u] = len(idx)
+        if len(idx):
+            st.beac[u, : len(idx)] = dev(vec.reshape(len(idx), cfg.G, cfg.d))
+
+
+@pytest.mark.parametrize("cid,units_", [(1, 2), (2, 6), (3, 3)])
+def test_score_parity_configs(cid, units_):
+    cfg = wl.CONFIGS[cid]
+    units = wl.make_units(cfg, range(units_))
+    st = DeviceState(units, cfg)
+    _upload_oracle_beacons(st, units, cfg)
+    st.score()
+    assert st.status() == 0
+    _score_check(cfg, units, st)
+
+
+@pytest.mark.parametrize("M", wl.CONFIG4_M_SWEEP)
+def test_score_parity_beacon_sweep(M):
+    cfg = wl.config4(M)
+    units = wl.make_units(cfg, range(2))
+    st = DeviceState(units, cfg)
+    _upload_oracle_beacons(st, units, cfg)
+    st.score()
+    assert st.status() == 0
+    _score_check(cfg, units, st)
+
+
+def test_score_parity_long_cache():
+    cfg = wl.CONFIGS[5]
+    units = wl.make_units(cfg, range(1))
+    st = DeviceState(units, cfg.with_(C=256))  # scoring does not read the buffer
+    # the 32K workload's buffer holds C = 512 items; take beacons from its
+    # first 255 items (this build's FPS handles C <= 256)
+    for u in range(st.U):
+        un = _unit(units, u)
+        idx = oracle.fps(un["buf"][:255].reshape(255, -1), cfg.M)
+        st.nb[u] = len(idx)
+        st.beac[u, : len(idx)] = dev(un["buf"][idx])
+    st.score()
+    assert st.status() == 0
+    _score_check(cfg, units, st)
+
+
+@pytest.mark.parametrize("variant", ["mean", "noncausal", "no_beacons", "early_step",
+                                     "ragged", "tiny_L", "beacons_only", "d64_g1"])
+def test_score_edge_cases(variant):
+    cfg = wl.CONFIGS[2].with_(M=16)
+    agg, causal = "max", True
+    if variant == "d64_g1":
+        cfg = cfg.with_(d=64, G=1, theta=1e4)
+    units = wl.make_units(cfg, range(3))
+    L_cap = None
+    if variant == "ragged":
+        units["L"] = np.array([2176, 1999, 130], dtype=np.int32)
+    if variant == "tiny_L":
+        units["L"] = np.array([1, 17, 127], dtype=np.int32)
+        units["kpos"][:, :127] = np.arange(cfg.cur_pos - 126, cfg.cur_pos + 1)
+    if variant == "beacons_only":
+        cfg = cfg.with_(W=0)
+        units["ring"] = units["ring"][:, :0]
+    st = DeviceState(units, cfg, L_cap=L_cap, agg=bkv.AGG_MEAN if variant == "mean" else bkv.AGG_MAX,
+                     causal=0 if variant == "noncausal" else 1)
+    if variant == "mean":
+        agg = "mean"
+    if variant == "noncausal":
+        causal = False
+    if variant == "early_step":
+        st.step = 5  # only ring slots 0..5 were ever written
+    _upload_oracle_beacons(st, units, cfg)
+    if variant == "no_beacons":
+        st.nb.zero_()
+    st.score()
+    assert st.status() == 0
+    _score_check(cfg, units, st, agg, causal)
+
+
+# --------------------------------------------------------------------- FPS
+
+
+def test_fps_stream_replay_tiny():
+    """The tiny workload's 600-query trace through the continual buffer
+    (compress every 48 steps), beacons checked at every 100th step."""
+    cfg = wl.CONFIGS[1]
+    U = cfg.U
+    streams = [wl.make_unit(cfg, u, stream_len=600)["stream"] for u in range(U)]
+    D = cfg.G * cfg.d
+    dims = bkv.Dims.from_config(cfg)
+    ws = bkv.make_workspace(dims)
+    ring = torch.zeros((U, cfg.W, cfg.G, cfg.d), dtype=torch.int16, device="cuda")
+    buf = torch.zeros((U, cfg.C, cfg.G, cfg.d), dtype=torch.int16, device="cuda")
+    cnt = torch.zeros(U, dtype=torch.int32, device="cuda")
+    bidx = torch.zeros((U, cfg.M), dtype=torch.int32, device="cuda")
+    beac = torch.zeros((U, cfg.M, cfg.G, cfg.d), dtype=torch.int16, device="cuda")
+    nb = torch.zeros(U, dtype=torch.int32, device="cuda")
+    refs = [oracle.ContinualBuffer(cfg.C, cfg.M, D) for _ in range(U)]
+    for t in range(600):
+        q = dev(np.stack([s[t] for s in streams]))
+        want = (t % 100 == 99) or t == 599
+        bkv.fps_update(dims, q, t, ring, buf, cnt, want, bidx, beac, nb, ws)
+        for u in range(U):
+            refs[u].push(streams[u][t])
+        if want:
+            assert bkv.get_status(ws) == 0
+            for u in range(U):
+                c = int(refs[u].cnt[0])
+                assert int(cnt[u]) == c
+                assert np.array_equal(host_u16(buf[u]).reshape(cfg.C, D)[:c], refs[u].items)
+                idx, vec = refs[u].beacons()
+                assert int(nb[u]) == len(idx)
+                assert np.array_equal(bidx[u].cpu().numpy()[: len(idx)], idx)
+                assert np.array_equal(host_u16(beac[u]).reshape(cfg.M, D)[: len(idx)], vec)
+    assert refs[0].compressions >= 10
+    ring_ref = np.stack([s[600 - cfg.W:] for s in streams])  # steps 584..599
+    slots = [(584 + k) % cfg.W for k in range(cfg.W)]
+    assert np.array_equal(host_u16(ring)[:, slots], ring_ref)
+
+
+@pytest.mark.parametrize("cfgname", ["c2", "c4m1", "c4m4", "c4m16", "c4m32", "c4m64"])
+def test_fps_compress_and_select_parity(cfgname):
+    cfg = wl.CONFIGS[2] if cfgname == "c2" else wl.config4(int(cfgname[3:]))
+    units = wl.make_units(cfg, range(4))
+    D = cfg.G * cfg.d
+    # (a) beacons of a C - 1 item buffer, no append
+    st = DeviceState(units, cfg)
+    st.fps(with_append=False, want_beacons=True)
+    assert st.status() == 0
+    for u in range(st.U):
+        un = _unit(units, u)
+        idx = oracle.fps(un["buf"][: cfg.C - 1].reshape(cfg.C - 1, D), cfg.M)
+        assert np.array_equal(st.bidx[u].cpu().numpy()[: len(idx)], idx), u
+        assert int(st.nb[u]) == len(idx)
+    # (b) the append fills the buffer: compress, then beacons of the M survivors
+    st = DeviceState(units, cfg)
+    st.fps(with_append=True, want_beacons=True)
+    assert st.status() == 0
+    for u in range(st.U):
+        un = _unit(units, u)
+        cb = oracle.ContinualBuffer.from_state(un["buf"], int(un["cnt"]), cfg.M)
+        assert cb.push(un["q_new"])
+        assert int(st.cnt[u]) == cfg.M
+        assert np.array_equal(host_u16(st.buf[u]).reshape(cfg.C, D)[: cfg.M], cb.items)
+        idx, _ = cb.beacons()
+        assert np.array_equal(st.bidx[u].cpu().numpy(), idx)
+
+
+def test_fps_exact_ties_and_zero_vectors():
+    """Duplicated items and a zero vector: decisions on exact ties must pick
+    the lowest index, as the fp64 definition does."""
+    cfg = wl.CONFIGS[2]
+    units = wl.make_units(cfg, range(3))
+    D = cfg.G * cfg.d
+    buf = units["buf"].reshape(3, cfg.C, D)
+    buf[0, 10:20] = buf[0, 0:10]          # duplicates
+    buf[1, 7] = 0                          # zero vector
+    buf[1, 100:140] = buf[1, 60:100]
+    base = buf[2, 0].copy()                # many near-parallel items
+    for i in range(1, cfg.C):
+        buf[2, i] = base if i % 3 == 0 else buf[2, i]
+    units["buf"] = buf.reshape(units["buf"].shape)
+    st = DeviceState(units, cfg)
+    st.fps(with_append=False, want_beacons=True)
+    assert st.status() == 0
+    for u in range(3):
+        idx = oracle.fps(units["buf"][u][: cfg.C - 1].reshape(cfg.C - 1, D), cfg.M)
+        assert np.array_equal(st.bidx[u].cpu().numpy(), idx), u
+
+
+# ------------------------------------------------------------ whole round
+
+
+def _round_parity(cfg, units, st):
+    st.fps()
+    st.score()
+    sg = st.scores.cpu().numpy().astype(np.float64)
+    st.select_compact()
+    assert st.status() == 0
+    worst = -1.0
+    for u in range(st.U):
+        un = _unit(units, u)
+        ref = oracle.round_unit(un, cfg.W, cfg.M, cfg.B_KV, cfg.Rw, cfg.theta)
+        assert np.array_equal(st.bidx[u].cpu().numpy()[: len(ref["beacon_idx"])],
+                              ref["beacon_idx"])
+        L0 = int(un["L"])
+        worst = max(worst, score_tol_excess(sg[u, :L0], ref["scores"]))
+        kept = st.kept[u].cpu().numpy()
+        n = min(L0, cfg.B_KV)
+        assert np.array_equal(kept[:n], oracle.select(sg[u, :L0], cfg.B_KV, cfg.Rw))
+        assert kept_sets_agree(kept[:n], ref["scores"], cfg.B_KV, cfg.Rw, L0)
+        assert np.array_equal(host_u16(st.K[u])[:n], un["K"][kept[:n]])
+        assert np.array_equal(host_u16(st.V[u])[:n], un["V"][kept[:n]])
+        assert np.array_equal(st.kpos[u].cpu().numpy()[:n], un["kpos"][kept[:n]])
+        assert int(st.L[u]) == n
+    assert worst <= 0, f"score parity: worst excess {worst:.3g}"
+
+
+def test_round_parity_tiny():
+    cfg = wl.CONFIGS[1]
+    units = wl.make_units(cfg, range(cfg.U))
+    _round_parity(cfg, units, DeviceState(units, cfg))
+
+
+def test_round_parity_qwen3_4b_one_layer_full():
+    """The benchmark workload at full size (112 units, one launch each),
+    every unit checked."""
+    cfg = wl.CONFIGS[2]
+    units = wl.make_units(cfg, range(cfg.U))
+    _round_parity(cfg, units, DeviceState(units, cfg))
