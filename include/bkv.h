@@ -80,7 +80,7 @@ enum { BKV_AGG_MAX = 0, BKV_AGG_MEAN = 1 };
  *                  0: every row sees every key
  *   rope_theta     rotary base (rotate-half pairs (i, i + d/2),
  *                  frequency theta^(-2i/d))
- * Limits: (W + M) * G <= 512 scoring rows; positions < 2^24.
+ * Limits: (W + M) * G <= 1024 scoring rows; positions < 2^24.
  */
 typedef struct bkv_dims {
   int32_t U, G, d, W, M, C, B_KV, R;

@@ -33,7 +33,7 @@ int validate(const bkv_dims* d) {
   if (d->causal_recent != 0 && d->causal_recent != 1) return BKV_EINVAL;
   if (d->reserved != 0) return BKV_EINVAL;
   if (!(d->rope_theta > 1.0) || !std::isfinite(d->rope_theta)) return BKV_EINVAL;
-  if (d->W + d->M < 1 || (d->W + d->M) * d->G > 512) return BKV_EINVAL;
+  if (d->W + d->M < 1 || (d->W + d->M) * d->G > 1024) return BKV_EINVAL;
   if (static_cast<int64_t>(d->U) * d->L_cap * d->d >= (int64_t(1) << 40)) return BKV_EINVAL;
   if (d->C > 256) return BKV_EUNSUPPORTED;
   return BKV_OK;

@@ -35,7 +35,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kStages = 3;
 constexpr int kMaxSel = 64;
-constexpr int kMaxCont = 64;  // contenders re-evaluated per round of a recheck
 // Bound on |fp32 cosine - exact cosine| for the tensor-core Gram (bf16
 // products are exact; fp32 accumulation over up to 2048 terms in blocks,
 // plus normalisation) with a safety factor; the seed's mean adds a
@@ -51,13 +50,13 @@ struct __align__(16) FpsShared {
   int32_t abort_flag;
   int32_t n_sel;
   int32_t winner;
-  int32_t n_cont;
   int32_t pad;
   float inv[256];
   int32_t sel[kMaxSel];
   int32_t surv[kMaxSel];
-  int32_t cont[kMaxCont];
-  double cont_val[kMaxCont];
+  int32_t wcount[kWarps];
+  int32_t cont[256];      // contenders of a recheck, ascending item index
+  double cont_val[256];
   double norm64[256];
   float red_v1[kWarps];
   float red_v2[kWarps];
@@ -113,6 +112,25 @@ __device__ Top2 block_top2(Top2 t, FpsShared* sh) {
   for (int w = 1; w < kWarps; ++w) r = top2_merge(r, Top2{sh->red_v1[w], sh->red_i1[w], sh->red_v2[w]});
   __syncthreads();
   return r;
+}
+
+// Ordered list of the items whose flag is set (thread i = item i): writes
+// them to sh->cont in ascending index order and returns how many there are.
+// Every thread calls; no cap, so a recheck always sees every contender.
+__device__ int collect_contenders(bool flag, FpsShared* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t b = __ballot_sync(0xffffffffu, flag);
+  if (lane == 0) sh->wcount[warp] = __popc(b);
+  __syncthreads();
+  int off = 0, total = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    const int c = sh->wcount[w];
+    off += w < warp ? c : 0;
+    total += c;
+  }
+  if (flag) sh->cont[off + __popc(b & ((1u << lane) - 1u))] = threadIdx.x;
+  __syncthreads();
+  return total;
 }
 
 __device__ __forceinline__ double bf16d(uint16_t b) {
@@ -264,31 +282,25 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   Top2 t = block_top2(Top2{mean, i, INFINITY}, sh);
   int seed = t.i1;
   if (!(t.v2 - t.v1 > 2.f * kTauMean) && gram_ok) {
-    // near-tie: re-decide among the contenders in fp64
-    if (tid == 0) sh->n_cont = 0;
-    __syncthreads();
-    if (i < n && mean <= t.v1 + 2.f * kTauMean) {
-      const int slot = atomicAdd(&sh->n_cont, 1);
-      if (slot < kMaxCont) sh->cont[slot] = i;
-    }
-    __syncthreads();
-    const int nc = min(sh->n_cont, kMaxCont);
+    // near-tie: re-decide among the contenders in fp64.  The sum runs over
+    // every item in slot order and then drops the item's own term, so two
+    // identical items get bit-identical sums and the lowest slot wins.
+    const int nc = collect_contenders(i < n && mean <= t.v1 + 2.f * kTauMean, sh);
     for (int c = warp; c < nc; c += kWarps) {
       const int a = sh->cont[c];
       double s = 0.0;
-      for (int j = 0; j < n; ++j)
-        if (j != a) s += cos64(X, D, a, j, sh);
+      for (int j = 0; j < n; ++j) s += cos64(X, D, a, j, sh);
+      s -= cos64(X, D, a, a, sh);
       if (lane == 0) sh->cont_val[c] = s / static_cast<double>(n - 1);
     }
     __syncthreads();
     if (tid == 0) {
       int best = -1;
       double bv = 0.0;
-      for (int c = 0; c < nc; ++c) {
-        const int a = sh->cont[c];
+      for (int c = 0; c < nc; ++c) {  // ascending index: strict < keeps the lowest
         const double v = sh->cont_val[c];
-        if (best < 0 || v < bv || (v == bv && a < best)) {
-          best = a;
+        if (best < 0 || v < bv) {
+          best = sh->cont[c];
           bv = v;
         }
       }
@@ -301,7 +313,8 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   // ---- greedy farthest-point steps
   if (tid == 0) sh->sel[0] = seed;
   bool chosen = (i == seed);
-  float dist = 1.f;
+  // 1 - cos lies in [0, 2]: start above it so the seed's column sets it
+  float dist = INFINITY;
   auto update = [&](int k) {
     // Gram column k: this thread's entry G[i][k] (band h holds rows 128h..)
     float gk = 0.f;
@@ -320,14 +333,7 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
     Top2 r = block_top2(Top2{live ? -dist : INFINITY, i, INFINITY}, sh);
     int win = r.i1;
     if (!(r.v2 - r.v1 > 2.f * kTauCos) && gram_ok) {
-      if (tid == 0) sh->n_cont = 0;
-      __syncthreads();
-      if (live && -dist <= r.v1 + 2.f * kTauCos) {
-        const int slot = atomicAdd(&sh->n_cont, 1);
-        if (slot < kMaxCont) sh->cont[slot] = i;
-      }
-      __syncthreads();
-      const int nc = min(sh->n_cont, kMaxCont);
+      const int nc = collect_contenders(live && -dist <= r.v1 + 2.f * kTauCos, sh);
       for (int c = warp; c < nc; c += kWarps) {
         const int a = sh->cont[c];
         double dmin = 0.0;
@@ -341,11 +347,10 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
       if (tid == 0) {
         int best = -1;
         double bv = 0.0;
-        for (int c = 0; c < nc; ++c) {
-          const int a = sh->cont[c];
+        for (int c = 0; c < nc; ++c) {  // ascending index: strict > keeps the lowest
           const double v = sh->cont_val[c];
-          if (best < 0 || v > bv || (v == bv && a < best)) {
-            best = a;
+          if (best < 0 || v > bv) {
+            best = sh->cont[c];
             bv = v;
           }
         }

@@ -98,13 +98,16 @@ int ora_fps(const uint16_t* X, int n, int D, int m, int32_t* sel, double* radius
     return n;
   }
   std::vector<double> S = cosine_matrix(X, n, D);
-  // seed: lowest mean similarity to the other items (ties -> lowest index)
+  // seed: lowest mean similarity to the other items (ties -> lowest index).
+  // The sum over the others is the whole row, summed in slot order, minus
+  // the item's own term: two identical items then get the same value bit
+  // for bit, so an exact tie is decided by the index, not by rounding.
   int seed = 0;
   double seed_val = std::numeric_limits<double>::infinity();
   for (int i = 0; i < n; ++i) {
     double sum = 0.0;
-    for (int j = 0; j < n; ++j)
-      if (j != i) sum += S[static_cast<size_t>(i) * n + j];
+    for (int j = 0; j < n; ++j) sum += S[static_cast<size_t>(i) * n + j];
+    sum -= S[static_cast<size_t>(i) * n + i];
     double mean = sum / static_cast<double>(n - 1);
     if (mean < seed_val) {
       seed_val = mean;

@@ -50,7 +50,7 @@ def _dims(**kw):
     dict(U=0), dict(G=0), dict(G=17), dict(d=96), dict(W=-1), dict(W=65), dict(M=65),
     dict(M=256, C=256), dict(C=1, M=0), dict(B_KV=0), dict(B_KV=20000, L_cap=20000),
     dict(R=-1), dict(R=4096, B_KV=2048), dict(L_cap=100), dict(rope_theta=0.5),
-    dict(rope_theta=float("inf")), dict(W=0, M=0), dict(W=64, M=64, G=5), dict(agg=3),
+    dict(rope_theta=float("inf")), dict(W=0, M=0), dict(W=64, M=64, G=9), dict(agg=3),
     dict(causal_recent=2),
 ])
 def test_bad_dims_rejected(bad):

@@ -294,8 +294,17 @@ def _round_parity(cfg, units, st):
     for u in range(st.U):
         un = _unit(units, u)
         ref = oracle.round_unit(un, cfg.W, cfg.M, cfg.B_KV, cfg.Rw, cfg.theta)
-        assert np.array_equal(st.bidx[u].cpu().numpy()[: len(ref["beacon_idx"])],
-                              ref["beacon_idx"])
+        nbr = len(ref["beacon_idx"])
+        assert np.array_equal(st.bidx[u].cpu().numpy()[:nbr], ref["beacon_idx"]), u
+        # after a compress the beacon slots are trivially 0..M-1: the buffer
+        # contents and the beacon vectors are what show the survivors
+        D = cfg.G * cfg.d
+        c = ref["cnt"]
+        assert int(st.cnt[u]) == c
+        assert np.array_equal(host_u16(st.buf[u]).reshape(cfg.C, D)[:c],
+                              ref["buf"].reshape(-1, D)[:c]), u
+        assert np.array_equal(host_u16(st.beac[u]).reshape(-1, D)[:nbr],
+                              ref["buf"].reshape(-1, D)[ref["beacon_idx"]]), u
         L0 = int(un["L"])
         worst = max(worst, score_tol_excess(sg[u, :L0], ref["scores"]))
         kept = st.kept[u].cpu().numpy()
