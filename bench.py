@@ -1,10 +1,9 @@
 """Benchmark of the BeaconKV eviction step on B300.
 
-One step = one pass of the whole hot path over one batch of units: the
-decode step's query append to the continual FPS buffer (which fills it, so
-the FPS compress runs), the beacon selection, eviction scoring, top-B_KV
-selection and in-place K/V compaction -- the calls bkv_fps_update, bkv_score
-and bkv_select_compact of libbkv.  The workload is the Qwen3-4B-shaped
+One step = one eviction round over every unit: FPS beacon selection over
+the continual buffer (C - 1 items), eviction scoring, top-B_KV selection and
+in-place K/V compaction -- the calls bkv_fps_update (no append),
+bkv_score and bkv_select_compact of libbkv.  The workload is the Qwen3-4B-shaped
 one-layer round: 14 sequences x 8 KV heads (GQA 4), d = 128, cache length
 2176 -> B_KV 2048, W = 16 recent queries, M = 16 beacons, buffer C = 256.
 
@@ -61,6 +60,15 @@ def cfg_of(cid):
     return wl.CONFIGS[cid]
 
 
+def round_units(cfg, units_idx, seed=wl.SEED):
+    """Units in the state of an eviction round: the current step's query is
+    already in the recent ring (at cur_pos); the FPS buffer holds C - 1
+    earlier queries."""
+    units = wl.make_units(cfg, units_idx, seed=seed)
+    units["ring"][:, int(units["step"]) % cfg.W] = units["q_new"]
+    return units
+
+
 def workload_desc(cfg, world):
     return {
         "workload": f"{cfg.name}: {cfg.layers} layer(s) x {cfg.batch} seq x {cfg.kv_heads} KV "
@@ -69,7 +77,7 @@ def workload_desc(cfg, world):
         "units_per_gpu": cfg.U, "global_units": cfg.U * world,
         "parallelism": f"units sharded over {world} GPU(s)",
         "l2": "flushed (256 MiB write) and state restored before every timed step",
-        "step": "fps_update(append+compress+beacons) + score + select_compact",
+        "step": "fps_update(beacon select over C-1 items) + score + select_compact",
     }
 
 
@@ -81,7 +89,7 @@ def oracle_round_time(cfg, units, n):
     t0 = time.perf_counter()
     for u in range(n):
         un = {k: (v[u] if getattr(v, "ndim", 0) else v) for k, v in units.items()}
-        oracle.round_unit(un, cfg.W, cfg.M, cfg.B_KV, cfg.Rw, cfg.theta)
+        oracle.round_unit(un, cfg.W, cfg.M, cfg.B_KV, cfg.Rw, cfg.theta, append=False)
     return time.perf_counter() - t0
 
 
@@ -91,7 +99,7 @@ def run_reference(args, rank, world):
         return
     cfg = cfg_of(args.config)
     n = 8
-    units = wl.make_units(cfg, range(n))
+    units = round_units(cfg, range(n))
     oracle_round_time(cfg, units, 1)  # builds / loads the oracle
     for _ in range(args.warmup):
         oracle_round_time(cfg, units, 1)
@@ -188,12 +196,12 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", local)
     cfg = cfg_of(args.config)
     U = cfg.U
-    units = wl.make_units(cfg, range(U), seed=wl.SEED + rank)
+    units = round_units(cfg, range(U), seed=wl.SEED + rank)
     t = lambda a: torch.from_numpy(  # noqa: E731
         np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).to(dev)
     pristine = {k: t(units[k]) for k in ("K", "V", "kpos", "L", "ring", "buf", "cnt")}
     work = {k: v.clone() for k, v in pristine.items()}
-    q_new, cur = t(units["q_new"]), t(units["cur_pos"])
+    cur = t(units["cur_pos"])
     step = int(units["step"])
     M, G, d, B = cfg.M, cfg.G, cfg.d, cfg.B_KV
     bidx = torch.zeros((U, M), dtype=torch.int32, device=dev)
@@ -216,7 +224,7 @@ def run_ours(args, rank, world):
     def one_step(timed):
         restore()
         ev[0].record(stream)
-        bkv.fps_update(dims, q_new, step, work["ring"], work["buf"], work["cnt"], True, bidx,
+        bkv.fps_update(dims, None, step, work["ring"], work["buf"], work["cnt"], True, bidx,
                        beac, nb, ws, stream)
         ev[1].record(stream)
         bkv.score(dims, work["K"], work["L"], work["kpos"], work["ring"], step, beac, nb, cur,
@@ -263,19 +271,16 @@ def run_ours(args, rank, world):
 
     # ---------------- end to end through host buffers (pinned)
     host = {k: v.cpu().pin_memory() for k, v in pristine.items()}
-    host_q, host_cur = q_new.cpu().pin_memory(), cur.cpu().pin_memory()
+    host_cur = cur.cpu().pin_memory()
     out_host = {
         "K": torch.empty((U, B, d), dtype=torch.int16).pin_memory(),
         "V": torch.empty((U, B, d), dtype=torch.int16).pin_memory(),
         "kpos": torch.empty((U, B), dtype=torch.int32).pin_memory(),
         "L": torch.empty(U, dtype=torch.int32).pin_memory(),
         "kept": torch.empty((U, B), dtype=torch.int32).pin_memory(),
-        "buf": torch.empty_like(host["buf"]).pin_memory(),
-        "cnt": torch.empty(U, dtype=torch.int32).pin_memory(),
-        "ring": torch.empty_like(host["ring"]).pin_memory(),
+        "beacons": torch.empty((U, M, G, d), dtype=torch.int16).pin_memory(),
     }
-    h2d = sum(v.numel() * v.element_size() for v in host.values()) + \
-        host_q.numel() * 2 + host_cur.numel() * 4
+    h2d = sum(v.numel() * v.element_size() for v in host.values()) + host_cur.numel() * 4
     d2h = sum(v.numel() * v.element_size() for v in out_host.values())
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -284,9 +289,8 @@ def run_ours(args, rank, world):
         e0.record(stream)
         for k, v in host.items():
             work[k].copy_(v, non_blocking=True)
-        q_new.copy_(host_q, non_blocking=True)
         cur.copy_(host_cur, non_blocking=True)
-        bkv.fps_update(dims, q_new, step, work["ring"], work["buf"], work["cnt"], True, bidx,
+        bkv.fps_update(dims, None, step, work["ring"], work["buf"], work["cnt"], True, bidx,
                        beac, nb, ws, stream)
         bkv.score(dims, work["K"], work["L"], work["kpos"], work["ring"], step, beac, nb, cur,
                   scores, ws, stream)
@@ -297,9 +301,7 @@ def run_ours(args, rank, world):
         out_host["kpos"].copy_(work["kpos"][:, :B], non_blocking=True)
         out_host["L"].copy_(work["L"], non_blocking=True)
         out_host["kept"].copy_(kept, non_blocking=True)
-        out_host["buf"].copy_(work["buf"], non_blocking=True)
-        out_host["cnt"].copy_(work["cnt"], non_blocking=True)
-        out_host["ring"].copy_(work["ring"], non_blocking=True)
+        out_host["beacons"].copy_(beac, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         return e0.elapsed_time(e1)
@@ -319,7 +321,7 @@ def run_ours(args, rank, world):
     Lr = cfg.L
     alg = {
         # bytes each kernel must move (reads + writes) per launch
-        "fps_update": U * (cfg.C * cfg.D * 2 + 3 * cfg.D * 2 + 2 * cfg.M * cfg.D * 2 + 8),
+        "fps_update": U * ((cfg.C - 1) * cfg.D * 2 + cfg.M * cfg.D * 2 + cfg.M * 4 + 8),
         "score": U * (Lr * d * 2 + Lr * 4 + Lr * 4 + (cfg.W + M) * cfg.D * 2),
         "select_compact": U * Lr * 4 * 2 + U * B * 4 + n_moved * (2 * 2 * d * 2 + 8),
     }
@@ -347,7 +349,7 @@ def run_ours(args, rank, world):
     }
     if not args.no_cpu_baseline and world == 1:
         n = U
-        units_cpu = wl.make_units(cfg, range(n), seed=wl.SEED)
+        units_cpu = round_units(cfg, range(n), seed=wl.SEED)
         secs = oracle_round_time(cfg, units_cpu, n)
         line["cpu_baseline"] = {"value": 1.0 / (secs / n * U), "unit": UNIT, "cores": 1,
                                 "kind": "oracle",

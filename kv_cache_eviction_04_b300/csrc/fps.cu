@@ -22,9 +22,11 @@
 //      memory) picks the next item.
 //   4. Exactness guard: an fp32 decision is final only when the winner leads
 //      the runner-up by more than twice a bound on the fp32 error; otherwise
-//      every contender within that band is re-evaluated in fp64 from the
-//      bf16 inputs and the fp64 values decide (ties: lowest index), so the
-//      indices equal those of an fp64 evaluation.
+//      every contender within that band is re-evaluated from the bf16 inputs
+//      with exact products and error-free (TwoSum) sums, ~2^-44 accurate,
+//      and those values decide (ties: lowest index).  The indices then equal
+//      those of an fp64 evaluation except where two candidates' exact values
+//      differ by less than ~1e-12; identical items tie exactly.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -57,7 +59,9 @@ struct __align__(16) FpsShared {
   int32_t wcount[kWarps];
   int32_t cont[256];      // contenders of a recheck, ascending item index
   double cont_val[256];
-  double norm64[256];
+  double rn64[256];       // fp64 1/||x_i|| of the rechecks (negative: not yet)
+  double red64[kWarps];
+  double pair64[kThreads];  // 1 - cos of (contender, chosen) pairs
   float red_v1[kWarps];
   float red_v2[kWarps];
   int32_t red_i1[kWarps];
@@ -133,41 +137,74 @@ __device__ int collect_contenders(bool flag, FpsShared* sh) {
   return total;
 }
 
-__device__ __forceinline__ double bf16d(uint16_t b) {
-  return static_cast<double>(bf16_bits_to_float(b));
+// ---- exact-product dot products for the near-tie rechecks.
+// B300 runs fp64 at a small fraction of its fp32 rate, so the rechecks
+// work on the fp32 pipes: a product of two bf16 values is exact in fp32
+// (8-bit significands), and the sum is carried as an unevaluated pair
+// hi + lo with Knuth's TwoSum (Knuth, TAOCP vol. 2, 4.2.2), which keeps the
+// rounding error of every addition.  The pair is ~2^-44 accurate relative
+// to the sum of |terms|; only then is it widened to fp64.  The result is a
+// deterministic function of the two rows, symmetric in them, so identical
+// items get identical values and exact ties stay exact.
+struct FF {
+  float hi, lo;
+};
+__device__ __forceinline__ void ff_add(FF& acc, float p) {
+  const float s = acc.hi + p;
+  const float bb = s - acc.hi;
+  const float e = (acc.hi - (s - bb)) + (p - bb);
+  acc.hi = s;
+  acc.lo += e;
 }
-
-// fp64 norm of item i (cached in shared memory; -1 = not yet computed).
-// Called by a whole warp.
-__device__ double item_norm64(const uint16_t* X, int D, int i, FpsShared* sh) {
-  double nv = sh->norm64[i];
-  if (nv >= 0.0) return nv;
-  const int lane = threadIdx.x & 31;
-  double ss = 0.0;
-  for (int k = lane; k < D; k += 32) {
-    const double v = bf16d(X[static_cast<size_t>(i) * D + k]);
-    ss = fma(v, v, ss);
+// Dot product of rows a and b of X (D bf16 each, 16-byte aligned rows),
+// by one thread.
+__device__ double dot_rows(const uint16_t* X, int D, int a, int b) {
+  const uint4* ra = reinterpret_cast<const uint4*>(X + static_cast<size_t>(a) * D);
+  const uint4* rb = reinterpret_cast<const uint4*>(X + static_cast<size_t>(b) * D);
+  FF acc{0.f, 0.f};
+  for (int v = 0; v < D / 8; ++v) {
+    const uint4 va = ra[v], vb = rb[v];
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      ff_add(acc, __uint_as_float(wa[h] << 16) * __uint_as_float(wb[h] << 16));
+      ff_add(acc, __uint_as_float(wa[h] & 0xFFFF0000u) * __uint_as_float(wb[h] & 0xFFFF0000u));
+    }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  nv = sqrt(ss);
-  __syncwarp();
-  if (lane == 0) sh->norm64[i] = nv;
-  __syncwarp();
-  return nv;
+  return static_cast<double>(acc.hi) + static_cast<double>(acc.lo);
 }
 
-// fp64 cosine of items a and b (whole warp).
-__device__ double cos64(const uint16_t* X, int D, int a, int b, FpsShared* sh) {
-  const double na = item_norm64(X, D, a, sh), nb = item_norm64(X, D, b, sh);
-  const int lane = threadIdx.x & 31;
-  double s = 0.0;
-  for (int k = lane; k < D; k += 32)
-    s = fma(bf16d(X[static_cast<size_t>(a) * D + k]), bf16d(X[static_cast<size_t>(b) * D + k]), s);
+// 1/||x_i|| in fp64 (0 for a zero vector: cosine 0 with everything),
+// cached in shared memory (negative = not computed yet).  One thread.
+__device__ double inv_norm64(const uint16_t* X, int D, int i, FpsShared* sh) {
+  double r = sh->rn64[i];
+  if (r >= 0.0) return r;
+  const double n2 = dot_rows(X, D, i, i);
+  r = n2 > 0.0 ? 1.0 / sqrt(n2) : 0.0;
+  sh->rn64[i] = r;
+  return r;
+}
+
+// Cosine of items a and b from the exact-product dot product; one thread.
+// (g * r_a) * r_b: identical rows give identical values.
+__device__ __forceinline__ double cos_rows(const uint16_t* X, int D, int a, int b,
+                                           FpsShared* sh) {
+  const double ra = inv_norm64(X, D, a, sh), rb = inv_norm64(X, D, b, sh);
+  return (dot_rows(X, D, a, b) * ra) * rb;
+}
+
+// Block-wide fp64 sum of one value per thread, in a fixed order (warp
+// butterflies, then the warps in order); the result reaches every thread.
+__device__ double block_sum64(double v, FpsShared* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (na == 0.0 || nb == 0.0) return 0.0;
-  return s / (na * nb);
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) sh->red64[warp] = v;
+  __syncthreads();
+  double t = sh->red64[0];
+  for (int w = 1; w < kWarps; ++w) t += sh->red64[w];
+  __syncthreads();
+  return t;
 }
 
 // FPS of m items out of the first n rows of unit u's buffer.  Writes the
@@ -193,7 +230,7 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   const uint32_t box_bytes = static_cast<uint32_t>(min(stage_rows, (p.C + 15) & ~15)) * 128;
 
   if (warp == 0) tmem_alloc(&sh->tmem_base, 512);  // no relinquish: a CTA may select twice
-  for (int i = tid; i < 256; i += kThreads) sh->norm64[i] = -1.0;
+  for (int i = tid; i < 256; i += kThreads) sh->rn64[i] = -1.0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -282,16 +319,22 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   Top2 t = block_top2(Top2{mean, i, INFINITY}, sh);
   int seed = t.i1;
   if (!(t.v2 - t.v1 > 2.f * kTauMean) && gram_ok) {
-    // near-tie: re-decide among the contenders in fp64.  The sum runs over
-    // every item in slot order and then drops the item's own term, so two
-    // identical items get bit-identical sums and the lowest slot wins.
+    // near-tie: re-decide among the contenders with exact-product cosines.
+    // The sum runs over every item in a fixed order and then drops the
+    // item's own term, so two identical items get bit-identical sums and
+    // the lowest slot wins.
     const int nc = collect_contenders(i < n && mean <= t.v1 + 2.f * kTauMean, sh);
-    for (int c = warp; c < nc; c += kWarps) {
+    // every thread first fills its own item's 1/||x|| (no two threads
+    // write the same entry)
+    if (i < n) inv_norm64(X, D, i, sh);
+    __syncthreads();
+    for (int c = 0; c < nc; ++c) {
       const int a = sh->cont[c];
-      double s = 0.0;
-      for (int j = 0; j < n; ++j) s += cos64(X, D, a, j, sh);
-      s -= cos64(X, D, a, a, sh);
-      if (lane == 0) sh->cont_val[c] = s / static_cast<double>(n - 1);
+      // thread j: cos(a, j); the sum runs over every item in a fixed order
+      const double cj = i < n ? cos_rows(X, D, a, i, sh) : 0.0;
+      const double caa = cos_rows(X, D, a, a, sh);
+      const double tot = block_sum64(cj, sh) - caa;
+      if (tid == 0) sh->cont_val[c] = tot / static_cast<double>(n - 1);
     }
     __syncthreads();
     if (tid == 0) {
@@ -334,16 +377,25 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
     int win = r.i1;
     if (!(r.v2 - r.v1 > 2.f * kTauCos) && gram_ok) {
       const int nc = collect_contenders(live && -dist <= r.v1 + 2.f * kTauCos, sh);
-      for (int c = warp; c < nc; c += kWarps) {
-        const int a = sh->cont[c];
-        double dmin = 0.0;
-        for (int s = 0; s < k; ++s) {
-          const double dv = 1.0 - cos64(X, D, a, sh->sel[s], sh);
-          dmin = (s == 0) ? dv : fmin(dmin, dv);
-        }
-        if (lane == 0) sh->cont_val[c] = dmin;
-      }
+      // 1/||x|| of contenders and chosen items, each entry by one thread
+      if (live && -dist <= r.v1 + 2.f * kTauCos) inv_norm64(X, D, i, sh);
+      if (chosen) inv_norm64(X, D, i, sh);
       __syncthreads();
+      // one thread per (contender, chosen item) pair, in rounds of at most
+      // kThreads pairs; then the min over the chosen items per contender
+      const int per = max(1, kThreads / k);
+      for (int c0 = 0; c0 < nc; c0 += per) {
+        const int cn = min(per, nc - c0);
+        if (tid < cn * k)
+          sh->pair64[tid] = 1.0 - cos_rows(X, D, sh->cont[c0 + tid / k], sh->sel[tid % k], sh);
+        __syncthreads();
+        if (tid < cn) {
+          double dmin = sh->pair64[tid * k];
+          for (int s2 = 1; s2 < k; ++s2) dmin = fmin(dmin, sh->pair64[tid * k + s2]);
+          sh->cont_val[c0 + tid] = dmin;
+        }
+        __syncthreads();
+      }
       if (tid == 0) {
         int best = -1;
         double bv = 0.0;

@@ -188,17 +188,19 @@ def compact(rows, kept):
 
 
 def round_unit(unit: dict, W: int, M: int, B: int, R: int, theta: float,
-               agg: str = "max", causal: bool = True):
-    """One full eviction round of one unit, as the benchmark step runs it:
-    append the new query (compressing a full buffer), take beacons, score,
-    select and compact.  ``unit`` is one unit of ``workload.make_unit``.
-    Returns dict(beacon_idx, scores, kept, K, V, kpos, buf, cnt)."""
+               agg: str = "max", causal: bool = True, append: bool = True):
+    """One full eviction round of one unit: (if ``append``) append the new
+    query to the ring and the buffer, compressing a full buffer; take the
+    beacons, score, select and compact.  ``unit`` is one unit of
+    ``workload.make_unit``.  Returns dict(beacon_idx, scores, kept, K, V,
+    kpos, buf, cnt)."""
     G, d = unit["ring"].shape[1], unit["ring"].shape[2]
     ring = unit["ring"].copy()
     step = int(unit["step"])
-    ring[step % W] = unit["q_new"]
     cb = ContinualBuffer.from_state(unit["buf"], int(unit["cnt"]), M)
-    cb.push(unit["q_new"])
+    if append:
+        ring[step % W] = unit["q_new"]
+        cb.push(unit["q_new"])
     bidx, bvec = cb.beacons()
     sc = score(unit["K"], unit["kpos"], ring, step, bvec.reshape(-1, G, d),
                int(unit["cur_pos"]), theta, agg, causal, L=int(unit["L"]))

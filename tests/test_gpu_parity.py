@@ -284,8 +284,8 @@ def test_fps_exact_ties_and_zero_vectors():
 # ------------------------------------------------------------ whole round
 
 
-def _round_parity(cfg, units, st):
-    st.fps()
+def _round_parity(cfg, units, st, append=True):
+    st.fps(with_append=append)
     st.score()
     sg = st.scores.cpu().numpy().astype(np.float64)
     st.select_compact()
@@ -293,7 +293,7 @@ def _round_parity(cfg, units, st):
     worst = -1.0
     for u in range(st.U):
         un = _unit(units, u)
-        ref = oracle.round_unit(un, cfg.W, cfg.M, cfg.B_KV, cfg.Rw, cfg.theta)
+        ref = oracle.round_unit(un, cfg.W, cfg.M, cfg.B_KV, cfg.Rw, cfg.theta, append=append)
         nbr = len(ref["beacon_idx"])
         assert np.array_equal(st.bidx[u].cpu().numpy()[:nbr], ref["beacon_idx"]), u
         # after a compress the beacon slots are trivially 0..M-1: the buffer
@@ -330,3 +330,13 @@ def test_round_parity_qwen3_4b_one_layer_full():
     cfg = wl.CONFIGS[2]
     units = wl.make_units(cfg, range(cfg.U))
     _round_parity(cfg, units, DeviceState(units, cfg))
+
+
+def test_round_parity_bench_round_full():
+    """The benchmark's round at full size: the current query already in the
+    ring, beacons by FPS over the C - 1 buffered items (no append, no
+    compress), then score, select and compact; every unit checked."""
+    cfg = wl.CONFIGS[2]
+    units = wl.make_units(cfg, range(cfg.U))
+    units["ring"][:, int(units["step"]) % cfg.W] = units["q_new"]
+    _round_parity(cfg, units, DeviceState(units, cfg), append=False)
