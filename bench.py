@@ -21,7 +21,6 @@ import argparse
 import hashlib
 import json
 import os
-import subprocess
 import sys
 import threading
 import time
@@ -122,62 +121,125 @@ def run_reference(args, rank, world):
 
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples SM clock, power and clock-event reasons of one GPU every
+    10 ms from a thread (NVML, read-only queries), so that even a short
+    timed region gets samples.  Falls back to an nvidia-smi loop."""
 
-    def __init__(self, index):
-        self.index, self.rows, self.proc = index, [], None
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"))
+
+    def __init__(self, torch_device):
+        self.dev, self.rows, self.stop_ev = torch_device, [], threading.Event()
+        self.nv, self.h, self.max_mhz, self.th, self.err = None, None, None, None, None
+
+    def _handle(self, nv):
+        import torch
+        try:
+            pr = torch.cuda.get_device_properties(self.dev)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+            return nv.nvmlDeviceGetHandleByPciBusId(bus)
+        except Exception:
+            return nv.nvmlDeviceGetHandleByIndex(self.dev.index or 0)
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.th = threading.Thread(target=self._read, daemon=True)
-            self.th.start()
-        except OSError:
-            self.proc = None
+            import pynvml as nv
+            nv.nvmlInit()
+            self.nv, self.h = nv, self._handle(nv)
+            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
+            self.th = threading.Thread(target=self._loop, daemon=True)
+        except Exception as e:  # no NVML: poll nvidia-smi instead
+            self.nv, self.err = None, f"{type(e).__name__}: {e}"[:120]
+            self.th = threading.Thread(target=self._smi_loop, daemon=True)
+        self.th.start()
+        t0 = time.time()
+        while not self.rows and time.time() - t0 < 3.0:  # sampler running before timing
+            time.sleep(0.005)
+        self.rows.clear()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.rows.append([x.strip() for x in line.split(",")])
+    def _smi_loop(self):
+        import subprocess
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        idx = str(self.dev.index or 0)
+        try:
+            proc = subprocess.Popen(["nvidia-smi", "-i", idx, f"--query-gpu={q}",
+                                     "--format=csv,noheader,nounits", "-lms", "20"],
+                                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        for line in proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 7 and f[0].isdigit():
+                bits = sum(1 << k for k in range(4) if f[3 + k] == "Active")
+                self.max_mhz = float(f[1]) if f[1].replace(".", "").isdigit() else None
+                pw = float(f[2]) if f[2].replace(".", "").isdigit() else 0.0
+                self.rows.append((float(f[0]), bits, pw))
+            if self.stop_ev.is_set():
+                break
+        proc.terminate()
+
+    def _loop(self):
+        nv = self.nv
+        while not self.stop_ev.is_set():
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                pw = nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
+                self.rows.append((sm, rs, pw))
+            except Exception:
+                pass
+            self.stop_ev.wait(0.01)
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        rows = [r for r in self.rows if len(r) >= 8]
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[k] for r in rows for k in range(4) if r[4 + k] == "Active"})
-        return {"sm_mhz": float(np.median(sm)) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+        self.stop_ev.set()
+        self.th.join(timeout=3)
+        src = "nvml" if self.nv is not None else f"nvidia-smi (nvml: {self.err})"
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no samples"],
+                    "source": src}
+        if self.nv is not None:
+            masks = [getattr(self.nv, attr, 0) for _, attr in self.REASONS]
+        else:
+            masks = [1 << k for k in range(4)]
+        reasons = sorted({name for _, rs, _ in self.rows
+                          for (name, _), m in zip(self.REASONS, masks) if rs & m})
+        return {"sm_mhz": float(np.median([r[0] for r in self.rows])),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.rows),
+                "power_w_max": float(max(r[2] for r in self.rows)), "source": src}
 
 
 # ------------------------------------------------------------------ ours
 
 
 def traffic_for(kernel_file, kernel):
-    """ncu DRAM bytes per launch recorded for this kernel's current source."""
-    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    """ncu DRAM bytes (read + write) per call recorded in
+    profiles/ncu_traffic.txt for this kernel's current source, else None.
+    Line format: <call> <sha256[:16] of its .cu file> <bytes per call> <workload>."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
-        return None
-    rec = json.load(open(p)).get(kernel)
-    if not rec:
         return None
     src = os.path.join(ROOT, "kv_cache_eviction_04_b300", "csrc", kernel_file)
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return rec.get("bytes_per_launch") if rec.get("source_sha") == h else None
+    for line in open(p):
+        f = line.split()
+        if len(f) >= 3 and not line.startswith("#") and f[0] == kernel and f[1] == h:
+            return float(f[2])
+    return None
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's elapsed time (every rank gets it)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def run_ours(args, rank, world):
@@ -247,7 +309,7 @@ def run_ours(args, rank, world):
     kp = kept.cpu().numpy()
     n_moved = int((kp != np.arange(B)[None, :]).sum())
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -263,11 +325,7 @@ def run_ours(args, rank, world):
         raise RuntimeError(f"device status {status} during the timed steps")
     per = np.array(per)  # ms [steps][kernel]
     total_ms = float(per.sum())
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
 
     # ---------------- end to end through host buffers (pinned)
     host = {k: v.cpu().pin_memory() for k, v in pristine.items()}
@@ -313,21 +371,27 @@ def run_ours(args, rank, world):
 
     if rank != 0:
         return
-    # ---------------- roofline of the dominant kernel
+    # ---------------- rooflines (algorithmic bytes / CUDA-event time per call)
     hbm, tfl, src = peaks()
     names = ["fps_update", "score", "select_compact"]
     mean_ms = per.mean(axis=0)
     dom = int(np.argmax(mean_ms))
-    Lr = cfg.L
+    Lr, D = cfg.L, cfg.D
     alg = {
-        # bytes each kernel must move (reads + writes) per launch
-        "fps_update": U * ((cfg.C - 1) * cfg.D * 2 + cfg.M * cfg.D * 2 + cfg.M * 4 + 8),
-        "score": U * (Lr * d * 2 + Lr * 4 + Lr * 4 + (cfg.W + M) * cfg.D * 2),
-        "select_compact": U * Lr * 4 * 2 + U * B * 4 + n_moved * (2 * 2 * d * 2 + 8),
+        # bytes each call must move (reads + writes), all units of one round
+        "fps_update": U * ((cfg.C - 1) * D * 2 + M * D * 2 + M * 4 + 8),
+        "score": U * (Lr * d * 2 + Lr * 4 + Lr * 4 + (cfg.W + M) * D * 2),
+        "select_compact": U * (Lr * 4 + B * 4) + n_moved * (2 * 2 * d * 2 + 2 * 4),
     }
-    achieved = alg[names[dom]] / (mean_ms[dom] * 1e-3) / 1e9
-    kfile = {"fps_update": "fps.cu", "score": "score.cu",
-             "select_compact": "select_compact.cu"}[names[dom]]
+    kfile = {"fps_update": "fps.cu", "score": "score.cu", "select_compact": "select_compact.cu"}
+    launches = {"fps_update": 1, "score": 2, "select_compact": 1}
+    roofs = {}
+    for k, n in enumerate(names):
+        ach = alg[n] / (mean_ms[k] * 1e-3) / 1e9
+        roofs[n] = {"kernel": n, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                    "frac": ach / hbm, "peak_source": src, "ms": float(mean_ms[k]),
+                    "launches_per_call": launches[n], "traffic": traffic_for(kfile[n], n),
+                    "algorithmic_bytes_per_launch": alg[n]}
     kv_bytes = U * (Lr * d * 2 + 2 * Lr * d * 2)  # K scored + K and V compacted (logical)
     rounds = world * args.steps / (total_ms * 1e-3)
     line = {
@@ -338,10 +402,8 @@ def run_ours(args, rank, world):
         "config": workload_desc(cfg, world),
         "kv_gbs": world * kv_bytes * args.steps / (total_ms * 1e-3) / 1e9,
         "kernel_ms": {n: float(m) for n, m in zip(names, mean_ms)},
-        "roofline": {"kernel": names[dom], "bound": "hbm", "achieved": achieved, "peak": hbm,
-                     "unit": "GB/s", "frac": achieved / hbm, "peak_source": src,
-                     "traffic": traffic_for(kfile, names[dom]),
-                     "algorithmic_bytes_per_launch": alg[names[dom]]},
+        "roofline": roofs[names[dom]],
+        "rooflines": roofs,
         "clocks": clk,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
