@@ -183,6 +183,42 @@ int bkv_select_compact(const bkv_dims* dims, const float* scores, void* K, void*
  */
 int bkv_get_status(void* workspace, bkv_stream_t stream, int32_t* device_status);
 
+/*
+ * bkv_score without a caller-provided workspace.  (The BeaconKV paper has
+ * no counterpart: this is a deployment variant of bkv_score.)
+ *
+ * For callers that cannot allocate device memory themselves: plugins
+ * hosted by a framework that owns every device allocation and offers no
+ * allocation hook, or loops where cudaMalloc's implicit device-wide
+ * synchronisation is not acceptable.  The call allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine); its scratch is a
+ * fixed array of BKV_NOALLOC_SCRATCH_BYTES bytes in the library's own
+ * device memory, which every GPU that loads the library holds until the
+ * process exits.
+ *
+ * Arguments and results are those of bkv_score, except:
+ *   device_status  optional device pointer to one int32; when the call's
+ *                  kernels finish it holds BKV_OK or the BKV_ETIMEOUT /
+ *                  BKV_EDEVICE they recorded (NULL: not reported)
+ * Returns BKV_EUNSUPPORTED, before enqueuing anything, when the shape needs
+ * more scratch than the array holds: 256 + U * nsplit * ceil(NQ/128)*128 * 8
+ * bytes, nsplit being the key-range splits the launch uses (about
+ * U * ceil(NQ/128) * ceil(L_cap/128) / 592 tiles per split, at least 2).
+ * For example 112 units of 128 rows and L_cap 2176 need 0.6 MB.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress) and caches it; make that first call before
+ * any stream capture.  Every call on a device shares the one array, so
+ * calls whose kernels overlap on the GPU (different streams without an
+ * ordering between them) race: order them.  Each call clears the status
+ * word it uses before its kernels run.
+ */
+#define BKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+int bkv_score_noalloc(const bkv_dims* dims, const void* K, const int32_t* L,
+                      const int32_t* kpos, const void* recent_q, int64_t step,
+                      const void* beacons, const int32_t* n_beacons, const int32_t* cur_pos,
+                      float* scores, int32_t* device_status, bkv_stream_t stream);
+
 /* Static description of a return code. */
 const char* bkv_strerror(int code);
 

@@ -51,15 +51,20 @@ _lib.bkv_workspace_init.argtypes = [_vp, ctypes.c_size_t, _vp]
 _lib.bkv_fps_update.argtypes = [_dp, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]
 _lib.bkv_score.argtypes = [_dp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.bkv_select_compact.argtypes = [_dp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+_lib.bkv_score_noalloc.argtypes = [_dp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.bkv_get_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
 _lib.bkv_strerror.argtypes = [ctypes.c_int]
 _lib.bkv_strerror.restype = ctypes.c_char_p
 for _f in ("bkv_workspace_size", "bkv_workspace_init", "bkv_fps_update", "bkv_score",
-           "bkv_select_compact", "bkv_get_status", "bkv_version"):
+           "bkv_select_compact", "bkv_get_status", "bkv_version", "bkv_score_noalloc"):
     getattr(_lib, _f).restype = ctypes.c_int
 
 EXPORTS = ("bkv_workspace_size", "bkv_workspace_init", "bkv_fps_update", "bkv_score",
-           "bkv_select_compact", "bkv_get_status", "bkv_strerror", "bkv_version")
+           "bkv_select_compact", "bkv_get_status", "bkv_strerror", "bkv_version",
+           "bkv_score_noalloc")
+
+# Bytes of the library's fixed scratch behind bkv_score_noalloc.
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def strerror(code: int) -> str:
@@ -119,6 +124,16 @@ def score(dims: Dims, K, L, kpos, recent_q, step, beacons, n_beacons, cur_pos, s
     _check(_lib.bkv_score(ctypes.byref(dims), _ptr(K), _ptr(L), _ptr(kpos), _ptr(recent_q),
                           int(step), _ptr(beacons), _ptr(n_beacons), _ptr(cur_pos),
                           _ptr(scores), _ptr(workspace), _stream(stream)), "bkv_score")
+
+
+def score_noalloc(dims: Dims, K, L, kpos, recent_q, step, beacons, n_beacons, cur_pos, scores,
+                  device_status=None, stream=None):
+    """bkv_score with the library's fixed scratch instead of a workspace, for
+    callers that cannot allocate device memory (see bkv_score_noalloc)."""
+    _check(_lib.bkv_score_noalloc(ctypes.byref(dims), _ptr(K), _ptr(L), _ptr(kpos),
+                                  _ptr(recent_q), int(step), _ptr(beacons), _ptr(n_beacons),
+                                  _ptr(cur_pos), _ptr(scores), _ptr(device_status),
+                                  _stream(stream)), "bkv_score_noalloc")
 
 
 def select_compact(dims: Dims, scores, K, V, kpos, L, kept=None, workspace=None, stream=None):

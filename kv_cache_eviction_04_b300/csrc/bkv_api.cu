@@ -122,6 +122,36 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? BKV_OK : BKV_ECUDA; }
 
 }  // namespace
 
+// Scratch of bkv_score_noalloc: a status header (as in a workspace) and the
+// per-split (max, sum) partials of the scoring passes.  Lives in the
+// library's device memory on every GPU that loads it, until process exit.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[BKV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 256;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device.  In host code the array's name is only a host-side stand-in.
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+    return BKV_ECUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return BKV_ECUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return BKV_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int bkv_version(void) { return 1; }
@@ -269,6 +299,75 @@ int bkv_select_compact(const bkv_dims* dims, const float* scores, void* K, void*
   p.R = dims->R;
   p.row_bytes = dims->d * 2;
   return cuda_rc(bkv::launch_select_compact(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bkv_score_noalloc(const bkv_dims* dims, const void* K, const int32_t* L,
+                      const int32_t* kpos, const void* recent_q, int64_t step,
+                      const void* beacons, const int32_t* n_beacons, const int32_t* cur_pos,
+                      float* scores, int32_t* device_status, bkv_stream_t stream) {
+  int v = validate(dims);
+  if (v != BKV_OK) return v;
+  if (K == nullptr || L == nullptr || kpos == nullptr || cur_pos == nullptr ||
+      scores == nullptr || step < 0)
+    return BKV_EINVAL;
+  if (dims->W > 0 && recent_q == nullptr) return BKV_EINVAL;
+  if (dims->M > 0 && (beacons == nullptr || n_beacons == nullptr)) return BKV_EINVAL;
+  if (!aligned16(K) || (recent_q && !aligned16(recent_q)) || (beacons && !aligned16(beacons)))
+    return BKV_EINVAL;
+  const ScoreShape s = score_shape(dims);
+  if (bkv::score_smem_bytes(dims->d, s.NQ16, dims->W) > static_cast<size_t>(kMaxSmem))
+    return BKV_EUNSUPPORTED;
+  const size_t need = bkv::kWsHeaderBytes +
+                      static_cast<size_t>(dims->U) * s.nsplit * s.nrows_part * sizeof(float2);
+  if (need > static_cast<size_t>(BKV_NOALLOC_SCRATCH_BYTES)) return BKV_EUNSUPPORTED;
+  void* base = nullptr;
+  v = noalloc_scratch(&base);
+  if (v != BKV_OK) return v;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the previous call's status must not leak into this one
+  if (cudaMemsetAsync(base, 0, bkv::kWsHeaderBytes, st) != cudaSuccess) return BKV_ECUDA;
+  bkv::ScoreParams p{};
+  p.L = L;
+  p.kpos = kpos;
+  p.recent_q = static_cast<const uint16_t*>(recent_q);
+  p.beacons = static_cast<const uint16_t*>(beacons);
+  p.n_beacons = n_beacons;
+  p.cur_pos = cur_pos;
+  p.scores = scores;
+  p.part = reinterpret_cast<float2*>(static_cast<uint8_t*>(base) + bkv::kWsHeaderBytes);
+  p.ws = static_cast<WsHeader*>(base);
+  p.step = step;
+  p.U = dims->U;
+  p.G = dims->G;
+  p.d = dims->d;
+  p.W = dims->W;
+  p.M = dims->M;
+  p.L_cap = dims->L_cap;
+  p.NQ = s.NQ;
+  p.NQ16 = s.NQ16;
+  p.nrows_part = s.nrows_part;
+  p.ngrp = s.ngrp;
+  p.nsplit = s.nsplit;
+  p.tiles_per_split = s.tiles_per_split;
+  p.agg = dims->agg;
+  p.causal = dims->causal_recent;
+  p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dims->d)));
+  for (int i = 0; i < dims->d / 2; ++i) {
+    const double f = std::pow(dims->rope_theta, -2.0 * i / static_cast<double>(dims->d));
+    p.freq_hi[i] = static_cast<float>(f);
+    p.freq_lo[i] = static_cast<float>(f - static_cast<double>(p.freq_hi[i]));
+  }
+  CUtensorMap map;
+  v = make_map(&map, K, static_cast<uint64_t>(dims->d), static_cast<uint64_t>(dims->L_cap),
+               static_cast<uint64_t>(dims->U), 128);
+  if (v != BKV_OK) return v;
+  v = cuda_rc(bkv::launch_score(p, map, st));
+  if (v != BKV_OK) return v;
+  if (device_status != nullptr &&
+      cudaMemcpyAsync(device_status, base, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) !=
+          cudaSuccess)
+    return BKV_ECUDA;
+  return BKV_OK;
 }
 
 int bkv_get_status(void* workspace, bkv_stream_t stream, int32_t* device_status) {
