@@ -121,8 +121,10 @@ int bkv_workspace_init(void* workspace, size_t bytes, bkv_stream_t stream);
  * survivors stay in slot order in buf[0..M), cnt = M; (3) if want_beacons:
  * FPS picks min(M, cnt) of the cnt items (read-only; all of them, in slot
  * order, when cnt <= M).  Beacon and survivor indices match an fp64
- * evaluation exactly: near-ties of the fp32 tensor-core pass are re-decided
- * in fp64.  Requires a workspace of bkv_workspace_size(dims) bytes.
+ * evaluation: near-ties of the fp32 tensor-core pass are re-decided from the
+ * bf16 inputs with exact products and error-free sums (~2^-44 relative), and
+ * identical items tie exactly (lowest slot).  Requires a workspace of
+ * bkv_workspace_size(dims) bytes.
  */
 int bkv_fps_update(const bkv_dims* dims, const void* q_new, int64_t step, void* recent_q,
                    void* buf, int32_t* cnt, int32_t want_beacons, int32_t* beacon_idx,
@@ -202,9 +204,11 @@ int bkv_get_status(void* workspace, bkv_stream_t stream, int32_t* device_status)
  *                  BKV_EDEVICE they recorded (NULL: not reported)
  * Returns BKV_EUNSUPPORTED, before enqueuing anything, when the shape needs
  * more scratch than the array holds: 256 + U * nsplit * ceil(NQ/128)*128 * 8
- * bytes, nsplit being the key-range splits the launch uses (about
- * U * ceil(NQ/128) * ceil(L_cap/128) / 592 tiles per split, at least 2).
- * For example 112 units of 128 rows and L_cap 2176 need 0.6 MB.
+ * bytes (NQ = (W + M) * G scoring rows).  nsplit, the key-range splits of
+ * the launch, is 1 when one CTA scores a whole unit (NQ <= 256 and either
+ * 2 U >= the SM count or L_cap <= 3072); otherwise the splits take about
+ * U * ceil(NQ/128) * ceil(L_cap/128) / (4 * SMs) key tiles each, at least 2.
+ * For example 112 units of 128 rows need 0.11 MB.
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress) and caches it; make that first call before

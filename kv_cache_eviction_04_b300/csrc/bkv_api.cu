@@ -10,7 +10,8 @@
 #include "kernels.h"
 
 namespace bkv {
-size_t select_smem_bytes(int B, int row_bytes);
+size_t select_smem_bytes(int B, int nbufs);
+int select_ring_buffers(int B, int L_cap, bool many_units);
 size_t fps_smem_bytes(int C);
 }  // namespace bkv
 
@@ -52,6 +53,7 @@ int sm_count() {
 
 struct ScoreShape {
   int NQ, NQ16, nrows_part, ngrp, ntiles, tiles_per_split, nsplit;
+  bool fused;
 };
 
 ScoreShape score_shape(const bkv_dims* d) {
@@ -61,6 +63,15 @@ ScoreShape score_shape(const bkv_dims* d) {
   s.nrows_part = (s.NQ + 127) / 128 * 128;
   s.ngrp = (s.NQ16 + 255) / 256;
   s.ntiles = (d->L_cap + 127) / 128;
+  // One CTA per unit runs both passes when the rows fit one CTA and there
+  // are enough units to fill the GPU (or the caches are short); otherwise the
+  // keys of a unit are split over CTAs and the passes are two launches.
+  s.fused = s.NQ16 <= 256 && (2 * d->U >= sm_count() || s.ntiles <= 24);
+  if (s.fused) {
+    s.tiles_per_split = s.ntiles > 0 ? s.ntiles : 1;
+    s.nsplit = 1;
+    return s;
+  }
   // about four CTAs per SM in the first pass, at least two tiles each
   const int64_t work = static_cast<int64_t>(d->U) * (s.nrows_part / 128) * s.ntiles;
   const int64_t target = 4ll * sm_count();
@@ -75,16 +86,22 @@ ScoreShape score_shape(const bkv_dims* d) {
 }
 
 struct WsLayout {
-  size_t unit_done, part, total;
+  size_t part, total;
 };
 
 WsLayout ws_layout(const bkv_dims* d) {
   WsLayout w{};
   const ScoreShape s = score_shape(d);
-  w.unit_done = bkv::kWsHeaderBytes;
-  w.part = w.unit_done + ((static_cast<size_t>(d->U) * 4 + 255) & ~static_cast<size_t>(255));
+  w.part = bkv::kWsHeaderBytes;
   w.total = w.part + static_cast<size_t>(d->U) * s.nsplit * s.nrows_part * sizeof(float2);
   return w;
+}
+
+// CTAs per unit of the select + compact kernel: one CTA per SM in all, as
+// one cluster of at most 8 (the portable cluster size) per unit.
+int select_cluster_size(int U) {
+  const int c = sm_count() / (U > 0 ? U : 1);
+  return c < 1 ? 1 : (c > 8 ? 8 : c);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -231,7 +248,7 @@ int bkv_score(const bkv_dims* dims, const void* K, const int32_t* L, const int32
   if (!aligned16(K) || (recent_q && !aligned16(recent_q)) || (beacons && !aligned16(beacons)))
     return BKV_EINVAL;
   const ScoreShape s = score_shape(dims);
-  if (bkv::score_smem_bytes(dims->d, s.NQ16, dims->W) > static_cast<size_t>(kMaxSmem))
+  if (bkv::score_smem_bytes(dims->d, s.NQ16, dims->W, s.fused) > static_cast<size_t>(kMaxSmem))
     return BKV_EUNSUPPORTED;
   const WsLayout w = ws_layout(dims);
   bkv::ScoreParams p{};
@@ -257,6 +274,7 @@ int bkv_score(const bkv_dims* dims, const void* K, const int32_t* L, const int32
   p.ngrp = s.ngrp;
   p.nsplit = s.nsplit;
   p.tiles_per_split = s.tiles_per_split;
+  p.fused = s.fused ? 1 : 0;
   p.agg = dims->agg;
   p.causal = dims->causal_recent;
   p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dims->d)));
@@ -281,9 +299,9 @@ int bkv_select_compact(const bkv_dims* dims, const float* scores, void* K, void*
       workspace == nullptr)
     return BKV_EINVAL;
   if (!aligned16(K) || !aligned16(V)) return BKV_EINVAL;
-  if (bkv::select_smem_bytes(dims->B_KV, dims->d * 2) > static_cast<size_t>(kMaxSmem))
+  const int nbufs = bkv::select_ring_buffers(dims->B_KV, dims->L_cap, dims->U >= 2 * sm_count());
+  if (nbufs < 3 || bkv::select_smem_bytes(dims->B_KV, nbufs) > static_cast<size_t>(kMaxSmem))
     return BKV_EUNSUPPORTED;
-  const WsLayout w = ws_layout(dims);
   bkv::SelectParams p{};
   p.scores = scores;
   p.K = static_cast<uint8_t*>(K);
@@ -291,13 +309,14 @@ int bkv_select_compact(const bkv_dims* dims, const float* scores, void* K, void*
   p.kpos = kpos;
   p.L = L;
   p.kept = kept;
-  p.unit_done = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + w.unit_done);
   p.ws = static_cast<WsHeader*>(workspace);
   p.U = dims->U;
   p.L_cap = dims->L_cap;
   p.B = dims->B_KV;
   p.R = dims->R;
   p.row_bytes = dims->d * 2;
+  p.ncl = select_cluster_size(dims->U);
+  p.nbufs = nbufs;
   return cuda_rc(bkv::launch_select_compact(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -315,7 +334,7 @@ int bkv_score_noalloc(const bkv_dims* dims, const void* K, const int32_t* L,
   if (!aligned16(K) || (recent_q && !aligned16(recent_q)) || (beacons && !aligned16(beacons)))
     return BKV_EINVAL;
   const ScoreShape s = score_shape(dims);
-  if (bkv::score_smem_bytes(dims->d, s.NQ16, dims->W) > static_cast<size_t>(kMaxSmem))
+  if (bkv::score_smem_bytes(dims->d, s.NQ16, dims->W, s.fused) > static_cast<size_t>(kMaxSmem))
     return BKV_EUNSUPPORTED;
   const size_t need = bkv::kWsHeaderBytes +
                       static_cast<size_t>(dims->U) * s.nsplit * s.nrows_part * sizeof(float2);
@@ -349,6 +368,7 @@ int bkv_score_noalloc(const bkv_dims* dims, const void* K, const int32_t* L,
   p.ngrp = s.ngrp;
   p.nsplit = s.nsplit;
   p.tiles_per_split = s.tiles_per_split;
+  p.fused = s.fused ? 1 : 0;
   p.agg = dims->agg;
   p.causal = dims->causal_recent;
   p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dims->d)));

@@ -14,8 +14,10 @@
 //      issues tcgen05 MMAs; rows 0..127 and 128..255 land in TMEM columns
 //      [0, 256) and [256, 512) with fp32 accumulation.  The Gram stays in
 //      TMEM for the whole selection.
-//   2. Thread i owns item i (its TMEM lane): 1/||x_i|| from the diagonal,
-//      its mean cosine to the others from its TMEM row -> seed = argmin.
+//      While a chunk is staged, thread i also accumulates the exact squared
+//      norm of item i from it (exact bf16 products, TwoSum sums).
+//   2. Thread i owns item i (its TMEM lane): its mean cosine to the others
+//      from its TMEM row (error-free sum) -> seed = argmin.
 //   3. Greedy: each step reads the new pick's Gram column (one TMEM column:
 //      every thread gets its own item's entry), updates its min distance
 //      1 - cos in a register and a block argmax (warp shuffles, then shared
@@ -38,11 +40,14 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kStages = 3;
 constexpr int kMaxSel = 64;
 // Bound on |fp32 cosine - exact cosine| for the tensor-core Gram (bf16
-// products are exact; fp32 accumulation over up to 2048 terms in blocks,
-// plus normalisation) with a safety factor; the seed's mean adds a
-// summation error over up to 256 terms.
+// products are exact; fp32 accumulation over up to 2048 terms in blocks of
+// 16, plus the normalisation by exact norms) with a safety factor.  The
+// seed's mean sums its terms error-free, so its bound is the same plus the
+// final rounding.
 constexpr float kTauCos = 4e-5f;
-constexpr float kTauMean = 1e-4f;
+constexpr float kTauMean = 4.1e-5f;
+constexpr int kCg = 8;           // contenders per pass of the seed recheck
+constexpr int kMaxPairs = 256;   // near-minimum (contender, chosen) pairs per greedy recheck
 
 struct __align__(16) FpsShared {
   uint64_t full[kStages];
@@ -52,19 +57,22 @@ struct __align__(16) FpsShared {
   int32_t abort_flag;
   int32_t n_sel;
   int32_t winner;
-  int32_t pad;
-  float inv[256];
+  int32_t npairs;
+  float inv[256];         // fp32 1/||x_i|| (from the exact norm)
   int32_t sel[kMaxSel];
   int32_t surv[kMaxSel];
   int32_t wcount[kWarps];
   int32_t cont[256];      // contenders of a recheck, ascending item index
   double cont_val[256];
-  double rn64[256];       // fp64 1/||x_i|| of the rechecks (negative: not yet)
+  double rn64[256];       // fp64 1/||x_i|| from the exact squared norm
   double red64[kWarps];
-  double pair64[kThreads];  // 1 - cos of (contender, chosen) pairs
-  float red_v1[kWarps];
-  float red_v2[kWarps];
-  int32_t red_i1[kWarps];
+  double self64[kCg];     // cos(a, a) of the seed-recheck contenders
+  double pair64[kMaxPairs];
+  int16_t pair_a[kMaxPairs];  // item of a pair's contender
+  int16_t pair_s[kMaxPairs];  // its chosen item
+  float red_v1[2][kWarps];
+  float red_v2[2][kWarps];
+  int32_t red_i1[2][kWarps];
 };
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* abort) {
@@ -95,8 +103,11 @@ __device__ __forceinline__ Top2 top2_merge(Top2 a, Top2 b) {
   }
   return r;
 }
-// Block-wide Top2 (all threads call; result valid in every thread).
-__device__ Top2 block_top2(Top2 t, FpsShared* sh) {
+// Block-wide Top2 (all threads call; result valid in every thread).  One
+// barrier: consecutive calls alternate between two reduction buffers
+// (`par` = call count & 1), so a call never overwrites what a thread of the
+// previous call may still read.
+__device__ Top2 block_top2(Top2 t, FpsShared* sh, int par) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -107,14 +118,14 @@ __device__ Top2 block_top2(Top2 t, FpsShared* sh) {
     t = top2_merge(t, o2);
   }
   if (lane == 0) {
-    sh->red_v1[warp] = t.v1;
-    sh->red_i1[warp] = t.i1;
-    sh->red_v2[warp] = t.v2;
+    sh->red_v1[par][warp] = t.v1;
+    sh->red_i1[par][warp] = t.i1;
+    sh->red_v2[par][warp] = t.v2;
   }
   __syncthreads();
-  Top2 r{sh->red_v1[0], sh->red_i1[0], sh->red_v2[0]};
-  for (int w = 1; w < kWarps; ++w) r = top2_merge(r, Top2{sh->red_v1[w], sh->red_i1[w], sh->red_v2[w]});
-  __syncthreads();
+  Top2 r{sh->red_v1[par][0], sh->red_i1[par][0], sh->red_v2[par][0]};
+  for (int w = 1; w < kWarps; ++w)
+    r = top2_merge(r, Top2{sh->red_v1[par][w], sh->red_i1[par][w], sh->red_v2[par][w]});
   return r;
 }
 
@@ -156,41 +167,39 @@ __device__ __forceinline__ void ff_add(FF& acc, float p) {
   acc.hi = s;
   acc.lo += e;
 }
-// Dot product of rows a and b of X (D bf16 each, 16-byte aligned rows),
-// by one thread.
-__device__ double dot_rows(const uint16_t* X, int D, int a, int b) {
+__device__ __forceinline__ void ff_add_products(FF& acc, uint4 a, uint4 b) {
+  const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    ff_add(acc, __uint_as_float(wa[h] << 16) * __uint_as_float(wb[h] << 16));
+    ff_add(acc, __uint_as_float(wa[h] & 0xFFFF0000u) * __uint_as_float(wb[h] & 0xFFFF0000u));
+  }
+}
+__device__ __forceinline__ FF ff_merge(FF a, FF b) {
+  FF r{a.hi, a.lo + b.lo};
+  ff_add(r, b.hi);
+  return r;
+}
+__device__ __forceinline__ double ff_value(FF a) {
+  return static_cast<double>(a.hi) + static_cast<double>(a.lo);
+}
+
+// Exact-product dot product of rows a and b of X by one warp: lane l takes
+// the 16-byte pieces l, l + 32, ...; the partial pairs are merged by an
+// xor butterfly (TwoSum is exact in either operand order, so every lane ends
+// with the same value, and the result is symmetric in a and b).
+__device__ double warp_dot_rows(const uint16_t* X, int D, int a, int b) {
+  const int lane = threadIdx.x & 31;
   const uint4* ra = reinterpret_cast<const uint4*>(X + static_cast<size_t>(a) * D);
   const uint4* rb = reinterpret_cast<const uint4*>(X + static_cast<size_t>(b) * D);
   FF acc{0.f, 0.f};
-  for (int v = 0; v < D / 8; ++v) {
-    const uint4 va = ra[v], vb = rb[v];
-    const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+  for (int v = lane; v < D / 8; v += 32) ff_add_products(acc, ra[v], rb[v]);
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      ff_add(acc, __uint_as_float(wa[h] << 16) * __uint_as_float(wb[h] << 16));
-      ff_add(acc, __uint_as_float(wa[h] & 0xFFFF0000u) * __uint_as_float(wb[h] & 0xFFFF0000u));
-    }
+  for (int o = 16; o > 0; o >>= 1) {
+    FF other{__shfl_xor_sync(0xffffffffu, acc.hi, o), __shfl_xor_sync(0xffffffffu, acc.lo, o)};
+    acc = ff_merge(acc, other);
   }
-  return static_cast<double>(acc.hi) + static_cast<double>(acc.lo);
-}
-
-// 1/||x_i|| in fp64 (0 for a zero vector: cosine 0 with everything),
-// cached in shared memory (negative = not computed yet).  One thread.
-__device__ double inv_norm64(const uint16_t* X, int D, int i, FpsShared* sh) {
-  double r = sh->rn64[i];
-  if (r >= 0.0) return r;
-  const double n2 = dot_rows(X, D, i, i);
-  r = n2 > 0.0 ? 1.0 / sqrt(n2) : 0.0;
-  sh->rn64[i] = r;
-  return r;
-}
-
-// Cosine of items a and b from the exact-product dot product; one thread.
-// (g * r_a) * r_b: identical rows give identical values.
-__device__ __forceinline__ double cos_rows(const uint16_t* X, int D, int a, int b,
-                                           FpsShared* sh) {
-  const double ra = inv_norm64(X, D, a, sh), rb = inv_norm64(X, D, b, sh);
-  return (dot_rows(X, D, a, b) * ra) * rb;
+  return ff_value(acc);
 }
 
 // Block-wide fp64 sum of one value per thread, in a fixed order (warp
@@ -230,50 +239,64 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   const uint32_t box_bytes = static_cast<uint32_t>(min(stage_rows, (p.C + 15) & ~15)) * 128;
 
   if (warp == 0) tmem_alloc(&sh->tmem_base, 512);  // no relinquish: a CTA may select twice
-  for (int i = tid; i < 256; i += kThreads) sh->rn64[i] = -1.0;
+  if (tid == 0) sh->npairs = 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sh->tmem_base;
+  const int i = tid;  // this thread's item
 
-  // ---- Gram on the tensor core (thread 0 drives TMA and MMA)
-  if (tid == 0) {
-    const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(N));
-    bool ok = true;
-    const int pro = min(kStages, nchunks);
-    for (int c = 0; c < pro; ++c) {
+  // ---- Gram on the tensor core (thread 0 issues TMA and MMA).  Meanwhile
+  // every thread accumulates the exact squared norm of its own item from
+  // the staged 64-column chunks (rows of 128 bytes, whose 16-byte pieces are
+  // swizzled by row & 7).  A stage is refilled once the MMAs and all eight
+  // warps are done with it.
+  FF n2{0.f, 0.f};
+  const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(N));
+  if (tid == 0)
+    for (int c = 0; c < min(kStages, nchunks); ++c) {
       mbar_arrive_expect_tx(&sh->full[c], box_bytes);
       tma_load_3d(stages + c * stage_bytes, bmap, &sh->full[c], 64 * c, 0, u);
     }
-    for (int c = 0; c < nchunks && ok; ++c) {
-      const int st = c % kStages;
-      if (!wait_bar(&sh->full[st], (c / kStages) & 1)) {
-        ok = false;
-        break;
-      }
+  bool ok = true;
+  for (int c = 0; c < nchunks; ++c) {
+    const int st = c % kStages;
+    ok = __all_sync(0xffffffffu, ok && wait_bar(&sh->full[st], (c / kStages) & 1));
+    if (!ok) break;
+    const uint8_t* sb = stages + st * stage_bytes;
+    if (tid == 0) {
       tc_fence_after();
-      const uint32_t sbase = smem_u32(stages + st * stage_bytes);
+      const uint32_t sbase = smem_u32(sb);
       for (int h = 0; h < nbands; ++h)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_bf16(tbase + h * 256, sdesc_sw128(sbase + h * 16384 + kk * 32),
                    sdesc_sw128(sbase + kk * 32), idesc, (c | kk) != 0);
       mma_commit(&sh->empty[st]);
-      const int cn = c + kStages;
-      if (cn < nchunks) {
-        if (!wait_bar(&sh->empty[st], (c / kStages) & 1)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&sh->full[st], box_bytes);
-        tma_load_3d(stages + st * stage_bytes, bmap, &sh->full[st], 64 * cn, 0, u);
+    }
+    if (i < n) {
+      const uint8_t* row = sb + i * 128;
+#pragma unroll
+      for (int lc = 0; lc < 8; ++lc) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + ((lc ^ (i & 7)) << 4));
+        ff_add_products(n2, v, v);
       }
     }
-    mma_commit(&sh->done);
-    if (!ok) {
-      sh->abort_flag = 1;
-      record_error(p.ws, BKV_ETIMEOUT, kSiteFpsWait);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh->empty[st]);
+    if (tid == 0 && c + kStages < nchunks) {
+      if (!wait_bar(&sh->empty[st], (c / kStages) & 1)) {
+        ok = false;
+      } else {
+        mbar_arrive_expect_tx(&sh->full[st], box_bytes);
+        tma_load_3d(stages + st * stage_bytes, bmap, &sh->full[st], 64 * (c + kStages), 0, u);
+      }
     }
+  }
+  if (tid == 0) mma_commit(&sh->done);
+  if (!ok) {
+    sh->abort_flag = 1;
+    if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteFpsWait);
   }
   __syncthreads();
   warp_wait(&sh->done, 0, &sh->abort_flag);
@@ -283,27 +306,23 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
 
   // item of this thread: band h = warp / 4, TMEM lane quarter = warp % 4
   const int h = warp >> 2, q = warp & 3;
-  const int i = tid;  // = 128 h + 32 q + lane
   const bool band_live = h < nbands;
   const uint32_t trow = tbase + (static_cast<uint32_t>(q * 32) << 16) + h * 256;
-  float inv_i = 0.f;
-  if (band_live) {
-    uint32_t v[32];
-    tmem_ld32(trow + 128 * h + 32 * q, v);  // diagonal block of this warp
-    tmem_wait_ld();
-    float g = 0.f;
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-      if (k == lane) g = __uint_as_float(v[k]);
-    inv_i = (i < n && g > 0.f) ? rsqrtf(g) : 0.f;
+  {
+    const double nn = ff_value(n2);
+    const double r = (i < n && nn > 0.0) ? 1.0 / sqrt(nn) : 0.0;
+    sh->rn64[i] = r;
+    sh->inv[i] = static_cast<float>(r);
   }
-  sh->inv[i] = inv_i;
   __syncthreads();
+  const float inv_i = sh->inv[i];
+  int tb = 0;  // block_top2 calls so far
 
-  // ---- seed: lowest mean cosine to the other items
+  // ---- seed: lowest mean cosine to the other items (error-free sum of the
+  // fp32 cosines, so the mean's error is that of one cosine)
   float mean = INFINITY;
   if (band_live) {
-    float acc = 0.f;
+    FF acc{0.f, 0.f};
     for (int c = 0; c < (N + 31) / 32; ++c) {
       uint32_t v[32];
       tmem_ld32(trow + c * 32, v);
@@ -311,32 +330,50 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const int j = c * 32 + k;  // columns past n were never written: skip them
-        if (j < n && j != i) acc = fmaf(__uint_as_float(v[k]), sh->inv[j], acc);
+        if (j < n && j != i) ff_add(acc, __uint_as_float(v[k]) * sh->inv[j]);
       }
     }
-    if (i < n) mean = acc * inv_i / static_cast<float>(n - 1);
+    if (i < n) mean = (acc.hi + acc.lo) * inv_i / static_cast<float>(n - 1);
   }
-  Top2 t = block_top2(Top2{mean, i, INFINITY}, sh);
+  Top2 t = block_top2(Top2{mean, i, INFINITY}, sh, tb++ & 1);
   int seed = t.i1;
   if (!(t.v2 - t.v1 > 2.f * kTauMean) && gram_ok) {
-    // near-tie: re-decide among the contenders with exact-product cosines.
-    // The sum runs over every item in a fixed order and then drops the
-    // item's own term, so two identical items get bit-identical sums and
-    // the lowest slot wins.
+    // Near-tie: re-decide among the contenders with exact-product cosines.
+    // Thread j reads its own row once per group of up to kCg contenders
+    // (staged in shared memory) and forms cos(a, j) for each; the sum over
+    // j runs in a fixed order and then drops the item's own term, so two
+    // identical items get bit-identical sums and the lowest slot wins.
     const int nc = collect_contenders(i < n && mean <= t.v1 + 2.f * kTauMean, sh);
-    // every thread first fills its own item's 1/||x|| (no two threads
-    // write the same entry)
-    if (i < n) inv_norm64(X, D, i, sh);
-    __syncthreads();
-    for (int c = 0; c < nc; ++c) {
-      const int a = sh->cont[c];
-      // thread j: cos(a, j); the sum runs over every item in a fixed order
-      const double cj = i < n ? cos_rows(X, D, a, i, sh) : 0.0;
-      const double caa = cos_rows(X, D, a, a, sh);
-      const double tot = block_sum64(cj, sh) - caa;
-      if (tid == 0) sh->cont_val[c] = tot / static_cast<double>(n - 1);
+    const int nv = D / 8;  // 16-byte pieces per row
+    uint4* crow = reinterpret_cast<uint4*>(stages);  // the Gram's stages are free now
+    const uint4* xr = reinterpret_cast<const uint4*>(X);
+    for (int c0 = 0; c0 < nc; c0 += kCg) {
+      const int cg = min(kCg, nc - c0);
+      for (int e = tid; e < cg * nv; e += kThreads)
+        crow[e] = xr[static_cast<size_t>(sh->cont[c0 + e / nv]) * nv + e % nv];
+      __syncthreads();
+      FF acc[kCg];
+#pragma unroll
+      for (int g = 0; g < kCg; ++g) acc[g] = FF{0.f, 0.f};
+      if (i < n) {
+        const uint4* mine = xr + static_cast<size_t>(i) * nv;
+#pragma unroll 4
+        for (int v = 0; v < nv; ++v) {
+          const uint4 xi = mine[v];
+#pragma unroll
+          for (int g = 0; g < kCg; ++g)
+            if (g < cg) ff_add_products(acc[g], crow[g * nv + v], xi);
+        }
+      }
+      for (int g = 0; g < cg; ++g) {
+        const int a = sh->cont[c0 + g];
+        const double cj = i < n ? (ff_value(acc[g]) * sh->rn64[a]) * sh->rn64[i] : 0.0;
+        if (i == a) sh->self64[g] = cj;
+        const double tot = block_sum64(cj, sh);  // contains barriers: self64 is set
+        if (tid == 0) sh->cont_val[c0 + g] = (tot - sh->self64[g]) / static_cast<double>(n - 1);
+      }
+      __syncthreads();  // crow is rewritten by the next group
     }
-    __syncthreads();
     if (tid == 0) {
       int best = -1;
       double bv = 0.0;
@@ -358,8 +395,7 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   bool chosen = (i == seed);
   // 1 - cos lies in [0, 2]: start above it so the seed's column sets it
   float dist = INFINITY;
-  auto update = [&](int k) {
-    // Gram column k: this thread's entry G[i][k] (band h holds rows 128h..)
+  auto gram = [&](int k) {  // this thread's fp32 cosine to item k (warp-collective)
     float gk = 0.f;
     if (band_live) {
       uint32_t v;
@@ -367,36 +403,60 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
       tmem_wait_ld();
       gk = __uint_as_float(v);
     }
-    const float c = gk * inv_i * sh->inv[k];
-    dist = fminf(dist, 1.f - c);
+    return gk * inv_i * sh->inv[k];
   };
-  update(seed);
+  dist = fminf(dist, 1.f - gram(seed));
   for (int k = 1; k < m; ++k) {
     const bool live = i < n && !chosen;
-    Top2 r = block_top2(Top2{live ? -dist : INFINITY, i, INFINITY}, sh);
+    Top2 r = block_top2(Top2{live ? -dist : INFINITY, i, INFINITY}, sh, tb++ & 1);
     int win = r.i1;
     if (!(r.v2 - r.v1 > 2.f * kTauCos) && gram_ok) {
-      const int nc = collect_contenders(live && -dist <= r.v1 + 2.f * kTauCos, sh);
-      // 1/||x|| of contenders and chosen items, each entry by one thread
-      if (live && -dist <= r.v1 + 2.f * kTauCos) inv_norm64(X, D, i, sh);
-      if (chosen) inv_norm64(X, D, i, sh);
+      const bool cont = live && -dist <= r.v1 + 2.f * kTauCos;
+      const int nc = collect_contenders(cont, sh);
+      // A contender's exact distance is the min over the chosen items; only
+      // those whose fp32 distance is within 2 tau of its fp32 min can attain
+      // it, so only those pairs are re-evaluated.
+      for (int s2 = 0; s2 < k; ++s2) {
+        const float dv = 1.f - gram(sh->sel[s2]);
+        if (cont && dv <= dist + 2.f * kTauCos) {
+          const int slot = atomicAdd(&sh->npairs, 1);
+          if (slot < kMaxPairs) {
+            sh->pair_a[slot] = static_cast<int16_t>(i);
+            sh->pair_s[slot] = static_cast<int16_t>(sh->sel[s2]);
+          }
+        }
+      }
       __syncthreads();
-      // one thread per (contender, chosen item) pair, in rounds of at most
-      // kThreads pairs; then the min over the chosen items per contender
-      const int per = max(1, kThreads / k);
-      for (int c0 = 0; c0 < nc; c0 += per) {
-        const int cn = min(per, nc - c0);
-        if (tid < cn * k)
-          sh->pair64[tid] = 1.0 - cos_rows(X, D, sh->cont[c0 + tid / k], sh->sel[tid % k], sh);
-        __syncthreads();
-        if (tid < cn) {
-          double dmin = sh->pair64[tid * k];
-          for (int s2 = 1; s2 < k; ++s2) dmin = fmin(dmin, sh->pair64[tid * k + s2]);
-          sh->cont_val[c0 + tid] = dmin;
+      const int np = sh->npairs;
+      if (np <= kMaxPairs) {
+        for (int pr = warp; pr < np; pr += kWarps) {
+          const int a = sh->pair_a[pr], b = sh->pair_s[pr];
+          const double cv = (warp_dot_rows(X, D, a, b) * sh->rn64[a]) * sh->rn64[b];
+          if (lane == 0) sh->pair64[pr] = 1.0 - cv;
         }
         __syncthreads();
+        for (int c = tid; c < nc; c += kThreads) {
+          const int a = sh->cont[c];
+          double dmin = INFINITY;
+          for (int pr = 0; pr < np; ++pr)
+            if (sh->pair_a[pr] == a) dmin = fmin(dmin, sh->pair64[pr]);
+          sh->cont_val[c] = dmin;
+        }
+      } else {
+        // too many near-minimum pairs: every (contender, chosen) pair
+        for (int c = warp; c < nc; c += kWarps) {
+          const int a = sh->cont[c];
+          double dmin = INFINITY;
+          for (int s2 = 0; s2 < k; ++s2) {
+            const int b = sh->sel[s2];
+            dmin = fmin(dmin, 1.0 - (warp_dot_rows(X, D, a, b) * sh->rn64[a]) * sh->rn64[b]);
+          }
+          if (lane == 0) sh->cont_val[c] = dmin;
+        }
       }
+      __syncthreads();
       if (tid == 0) {
+        sh->npairs = 0;
         int best = -1;
         double bv = 0.0;
         for (int c = 0; c < nc; ++c) {  // ascending index: strict > keeps the lowest
@@ -413,7 +473,7 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
     }
     if (tid == 0) sh->sel[k] = win;
     chosen = chosen || (i == win);
-    update(win);
+    dist = fminf(dist, 1.f - gram(win));
   }
   tc_fence_before();
   __syncthreads();
@@ -437,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sh->full[s], 1);
-      mbar_init(&sh->empty[s], 1);
+      mbar_init(&sh->empty[s], kWarps + 1);  // every warp read it + the MMAs ran
     }
     mbar_init(&sh->done, 1);
     sh->abort_flag = 0;

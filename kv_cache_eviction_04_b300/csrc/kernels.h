@@ -29,13 +29,14 @@ struct ScoreParams {
   int32_t nsplit;           // key-range splits per unit
   int32_t tiles_per_split;  // 128-key tiles per split
   int32_t agg, causal;
+  int32_t fused;            // 1: one CTA per unit runs both passes (NQ16 <= 256)
   float qscale;             // log2(e) / sqrt(d)
   float freq_hi[64];        // theta^(-2i/d) = freq_hi + freq_lo
   float freq_lo[64];
 };
 
 cudaError_t launch_score(const ScoreParams& p, const CUtensorMap& kmap, cudaStream_t st);
-size_t score_smem_bytes(int d, int NQ16, int W);
+size_t score_smem_bytes(int d, int NQ16, int W, bool fused);
 
 // --------------------------------------------------------- select+compact
 struct SelectParams {
@@ -44,10 +45,11 @@ struct SelectParams {
   uint8_t* V;
   int32_t* kpos;
   int32_t* L;
-  int32_t* kept;       // optional [U][B]
-  int32_t* unit_done;  // [U] counters in the workspace (start at 0)
+  int32_t* kept;  // optional [U][B]
   WsHeader* ws;
   int32_t U, L_cap, B, R, row_bytes;
+  int32_t ncl;    // CTAs (one cluster) per unit, 1..8
+  int32_t nbufs;  // wave buffers of 32 KB in the ring, 3..8
 };
 
 cudaError_t launch_select_compact(const SelectParams& p, cudaStream_t st);

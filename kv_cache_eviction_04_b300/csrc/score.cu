@@ -527,6 +527,268 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tbase, kCols);
 }
 
+// --------------------------------------------------------------- fused
+// Both passes in one CTA per unit, for up to 256 scoring rows: the queries
+// are rotated once, pass 1 runs over every key tile of the unit, each row's
+// log2-sum-exp is formed locally (no partials, no second launch), and pass 2
+// streams the same tiles again through TMA (a unit's keys are then usually
+// still in L2).  NR = 128-row blocks of the query image (1 or 2).
+template <int D, int NS, int NR>
+__global__ void __launch_bounds__(kThreads, 1)
+    score_fused_kernel(const __grid_constant__ ScoreParams p,
+                       const __grid_constant__ CUtensorMap kmap) {
+  constexpr int kRows = NR * 128;
+  constexpr uint32_t kQBytes = kRows * D * 2;  // one query image (hi or lo)
+  constexpr uint32_t kStageBytes = kTileKeys * D * 2;
+  constexpr uint32_t kBufCols = NR == 1 ? 128 : 256;  // TMEM columns per accumulator
+  constexpr uint32_t kCols = 2 * kBufCols;
+  constexpr uint32_t kIdesc1 = idesc_bf16_f32(128, kTileKeys);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* q_hi = smem;
+  uint8_t* q_lo = q_hi + kQBytes;
+  uint8_t* stages = q_lo + kQBytes;
+  Barriers* bars = reinterpret_cast<Barriers*>(stages + NS * kStageBytes);
+  int32_t* row_pos = reinterpret_cast<int32_t*>(bars + 1);  // [kRows]
+  float* lse = reinterpret_cast<float*>(row_pos + kRows);    // [kRows]
+  int32_t* kp = reinterpret_cast<int32_t*>(lse + kRows);      // [128] current pass-1 tile
+  float2* cs = reinterpret_cast<float2*>(kp + 128);           // [max(W,1)][D/2]
+
+  const int u = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int t0, t1, L;
+  split_tiles(p, u, 0, t0, t1, L);  // tiles_per_split covers the whole cache here
+  const int nt = t1 - t0;
+
+  if (threadIdx.x == 0) init_barriers(bars, NS);
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+
+  if (warp == 0) {
+    if (elect_one()) {
+      // ---------------- TMA producer: every tile twice (pass 1, then pass 2)
+      prefetch_tmap(&kmap);
+      for (int i = 0; i < 2 * nt; ++i) {
+        const int st = i % NS;
+        if (*reinterpret_cast<volatile int32_t*>(&bars->abort_flag) != 0 ||
+            !wait_bar(&bars->empty[st], ((i / NS) & 1) ^ 1)) {
+          bars->abort_flag = 1;
+          record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+          break;
+        }
+        mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
+        const int j0 = (i % nt) * kTileKeys;
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(stages + st * kStageBytes + a * 16384, &kmap, &bars->full[st], 64 * a, j0,
+                      u);
+      }
+    }
+  } else {
+    build_queries<D>(p, u, 0, kRows, q_hi, q_lo, row_pos, cs, threadIdx.x - 32, kThreads - 32,
+                     1);
+    if (warp == 1) {
+      // ---------------- MMA issuer
+      const uint32_t idesc2 = idesc_bf16_f32(128, static_cast<uint32_t>(p.NQ16));
+      for (int i = 0; i < 2 * nt; ++i) {
+        const int st = i % NS, b = i & 1;
+        if (!warp_wait(&bars->full[st], (i / NS) & 1, &bars->abort_flag) ||
+            !warp_wait(&bars->tempty[b], ((i >> 1) & 1) ^ 1, &bars->abort_flag)) {
+          if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t dt = tbase + b * kBufCols;
+          const uint32_t kbase = smem_u32(stages + st * kStageBytes);
+          if (i < nt) {
+            // pass 1: D[row][key] = Q[row] . K[key], one M = 128 block per row block
+#pragma unroll
+            for (int blk = 0; blk < NR; ++blk)
+#pragma unroll
+              for (int part = 0; part < 2; ++part) {
+                const uint32_t qbase = smem_u32(part ? q_lo : q_hi) + blk * 128 * 128;
+#pragma unroll
+                for (int a = 0; a < D / 64; ++a)
+#pragma unroll
+                  for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(dt + blk * 128, sdesc_sw128(qbase + a * (kRows * 128) + kk * 32),
+                             sdesc_sw128(kbase + a * 16384 + kk * 32), kIdesc1,
+                             (part | a | kk) != 0);
+              }
+          } else {
+            // pass 2: D[key][row] = K[key] . Q[row], N = NQ16 rows
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              const uint32_t qbase = smem_u32(part ? q_lo : q_hi);
+#pragma unroll
+              for (int a = 0; a < D / 64; ++a)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_bf16(dt, sdesc_sw128(kbase + a * 16384 + kk * 32),
+                           sdesc_sw128(qbase + a * (kRows * 128) + kk * 32), idesc2,
+                           (part | a | kk) != 0);
+            }
+          }
+          mma_commit(&bars->empty[st]);
+          mma_commit(&bars->tfull[b]);
+        }
+        __syncwarp();
+      }
+    } else {
+      // ---------------- epilogue (warps 2..5; TMEM lane quarter q)
+      const int q = warp & 3;
+      const int et = threadIdx.x - 64;  // 0..127
+      float m[NR], z[NR];
+      int32_t lim[NR];
+#pragma unroll
+      for (int blk = 0; blk < NR; ++blk) {
+        const int32_t rp = row_pos[blk * 128 + q * 32 + lane];
+        lim[blk] = (p.causal || rp == INT32_MIN) ? rp : INT32_MAX - 1;
+        m[blk] = -INFINITY;
+        z[blk] = 0.f;
+      }
+      // pass 1: thread = row; running max and sum of exp2 over the keys
+      for (int i = 0; i < nt; ++i) {
+        const int b = i & 1;
+        const int j = i * kTileKeys + et;
+        kp[et] = j < L ? p.kpos[static_cast<size_t>(u) * p.L_cap + j] : INT32_MAX;
+        named_sync(2, kEpiThreads);
+        if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
+          tc_fence_after();
+#pragma unroll
+          for (int blk = 0; blk < NR; ++blk) {
+#pragma unroll 1
+            for (int c = 0; c < kTileKeys / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tbase + (static_cast<uint32_t>(q * 32) << 16) + b * kBufCols +
+                            blk * 128 + c * 32,
+                        v);
+              tmem_wait_ld();
+              if (blk == NR - 1 && c == kTileKeys / 32 - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->tempty[b]);
+              }
+              const int4* kp4 = reinterpret_cast<const int4*>(kp + c * 32);
+              float t[32];
+              float mx = -INFINITY;
+#pragma unroll
+              for (int k4 = 0; k4 < 8; ++k4) {
+                const int4 kk = kp4[k4];
+                const int kv[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int k = k4 * 4 + e;
+                  t[k] = (kv[e] <= lim[blk]) ? __uint_as_float(v[k]) : -INFINITY;
+                  mx = fmaxf(mx, t[k]);
+                }
+              }
+              const float mn = fmaxf(m[blk], mx);
+              if (mn != -INFINITY) {
+                float acc = (m[blk] == -INFINITY) ? 0.f : z[blk] * ex2(m[blk] - mn);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) acc += ex2(t[k] - mn);
+                z[blk] = acc;
+                m[blk] = mn;
+              }
+            }
+          }
+        } else if (lane == 0) {
+          record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+        }
+        named_sync(2, kEpiThreads);  // kp is rewritten by the next tile
+      }
+      // each row's log2-sum-exp (empty rows: every probability is 0)
+#pragma unroll
+      for (int blk = 0; blk < NR; ++blk) {
+        const int r = blk * 128 + q * 32 + lane;
+        const int32_t rp = row_pos[r];
+        float l = INFINITY;
+        if (rp != INT32_MIN) {
+          if (z[blk] > 0.f) l = m[blk] + lg2(z[blk]);
+          atomicMin(&bars->minpos, rp);
+          if (!p.causal) row_pos[r] = INT32_MAX;
+        }
+        lse[r] = l;
+      }
+      named_sync(2, kEpiThreads);
+      // pass 2: thread = key; max (or mean) over rows of exp2(s - lse)
+      const int32_t minpos = bars->minpos;
+      const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
+      const int nrec = p.step + 1 < p.W ? static_cast<int>(p.step + 1) : p.W;
+      const float inv_rows = 1.f / static_cast<float>(max((nrec + nb) * p.G, 1));
+      const int N = p.NQ16;
+      const int nchunks = (N + 31) / 32;
+      for (int i = nt; i < 2 * nt; ++i) {
+        const int b = i & 1;
+        const int j = (i - nt) * kTileKeys + q * 32 + lane;
+        const int32_t kpj = j < L ? p.kpos[static_cast<size_t>(u) * p.L_cap + j] : INT32_MAX;
+        if (!warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
+          if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+          continue;
+        }
+        tc_fence_after();
+        const bool nomask = __all_sync(0xffffffffu, kpj <= minpos);
+        float best = -INFINITY, acc = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + (static_cast<uint32_t>(q * 32) << 16) + b * kBufCols + c * 32, v);
+          tmem_wait_ld();
+          if (c == nchunks - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->tempty[b]);
+          }
+          const int nv = min(32, N - c * 32);
+          const float4* l4 = reinterpret_cast<const float4*>(lse + c * 32);
+          const int4* p4 = reinterpret_cast<const int4*>(row_pos + c * 32);
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4) {
+            if (k4 * 4 < nv) {
+              const float4 lv = l4[k4];
+              const int4 pv = p4[k4];
+              const float ll[4] = {lv.x, lv.y, lv.z, lv.w};
+              const int pp[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float x = __uint_as_float(v[k4 * 4 + e]) - ll[e];
+                if (!nomask && kpj > pp[e]) x = -INFINITY;
+                if (p.agg == BKV_AGG_MAX)
+                  best = fmaxf(best, x);
+                else
+                  acc += ex2(x);
+              }
+            }
+          }
+        }
+        if (j < L)
+          p.scores[static_cast<size_t>(u) * p.L_cap + j] =
+              p.agg == BKV_AGG_MAX ? (best == -INFINITY ? 0.f : ex2(best)) : acc * inv_rows;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, kCols);
+}
+
+template <int D, int NS, int NR>
+size_t fused_smem(int W) {
+  return 1024 + 2 * static_cast<size_t>(NR) * 128 * D * 2 + NS * kTileKeys * D * 2 +
+         sizeof(Barriers) + NR * 128 * 8 + 128 * 4 +
+         static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
+}
+
 template <int D, int NS>
 size_t stats_smem(int W) {
   return 1024 + 2 * 128 * D * 2 + NS * kTileKeys * D * 2 + sizeof(Barriers) + 128 * 4 + 128 * 4 +
@@ -550,7 +812,12 @@ cudaError_t launch(Kern kernel, dim3 grid, size_t smem, cudaStream_t st, const S
 
 }  // namespace
 
-size_t score_smem_bytes(int d, int NQ16, int W) {
+size_t score_smem_bytes(int d, int NQ16, int W, bool fused) {
+  if (fused) {
+    const bool one = NQ16 <= 128;
+    if (d == 128) return one ? fused_smem<128, 3, 1>(W) : fused_smem<128, 2, 2>(W);
+    return one ? fused_smem<64, 4, 1>(W) : fused_smem<64, 4, 2>(W);
+  }
   const bool small = NQ16 <= 128;
   if (d == 128) {
     const size_t a = stats_smem<128, 3>(W);
@@ -563,6 +830,17 @@ size_t score_smem_bytes(int d, int NQ16, int W) {
 }
 
 cudaError_t launch_score(const ScoreParams& p, const CUtensorMap& kmap, cudaStream_t st) {
+  if (p.fused) {
+    const dim3 g(p.U);
+    const bool one = p.NQ16 <= 128;
+    if (p.d == 128)
+      return one ? launch(score_fused_kernel<128, 3, 1>, g, fused_smem<128, 3, 1>(p.W), st, p,
+                          kmap)
+                 : launch(score_fused_kernel<128, 2, 2>, g, fused_smem<128, 2, 2>(p.W), st, p,
+                          kmap);
+    return one ? launch(score_fused_kernel<64, 4, 1>, g, fused_smem<64, 4, 1>(p.W), st, p, kmap)
+               : launch(score_fused_kernel<64, 4, 2>, g, fused_smem<64, 4, 2>(p.W), st, p, kmap);
+  }
   const dim3 g1(p.nsplit, p.nrows_part / 128, p.U);
   const dim3 g2(p.nsplit, p.ngrp, p.U);
   const bool small = p.NQ16 <= 128;

@@ -5,23 +5,27 @@
 // "用信标 query 预判" (only the highest-scoring entries survive while a recent
 // sliding window is always kept).
 //
-// One CTA per (unit, tensor): part 0 compacts K (plus kpos, the kept list
-// and the new length), part 1 compacts V.  Each CTA selects on its own (the
-// scores of a unit are a few KB, far less than its K or V rows):
-//   * radix select, 8 bits per pass from the top, on an order-preserving
-//     integer image of the fp32 scores: a 256-bin shared-memory histogram
-//     with warp-aggregated increments (match.any ballots), then a block
-//     scan finds the bin holding the k-th largest;
+// One thread-block cluster of `ncl` CTAs per unit.  Every CTA selects on its
+// own (the scores of a unit are a few KB, far less than its K and V rows).
+// The unit's scores are read once, as order-preserving integer keys, into
+// shared memory (it reuses the copy ring, which is idle until then); longer
+// caches than the ring holds read the keys from global memory instead.
+//   * radix select, 8 bits per pass from the top, on the keys: a 256-bin
+//     shared-memory histogram
+//     with warp-aggregated increments (match.any), then a block scan finds
+//     the bin holding the k-th largest;
 //   * the ascending kept list by block prefix sums (equal scores: the lower
-//     slots first);
-//   * compaction: row i <- row kept[i] with kept[i] >= i.  Destination rows
-//     are processed in ascending chunks by one warp: TMA bulk copies bring a
-//     chunk's source rows into a shared-memory ring (one 16-byte-aligned
-//     row per lane) and one bulk store writes the chunk's contiguous
-//     destination rows back.  Sources of a later chunk lie at or above its
-//     own first row, so they are never overwritten by earlier chunks' stores,
-//     and a chunk is stored only after every earlier chunk's loads have
-//     landed: in-place compaction needs no second buffer.
+//     slots first).
+// Compaction (row i <- row kept[i], kept[i] >= i) runs in waves over the
+// rows that move, [first, n_kept): wave w covers ncl consecutive slices of
+// RS rows, one per CTA.  Each CTA brings its slice's source rows of K and V
+// into a shared-memory ring with TMA bulk copies (one row per thread), the
+// cluster meets at a hardware barrier once every CTA's loads of the wave have
+// landed, and only then is each slice stored back (two bulk stores of
+// contiguous rows).  Sources of a wave lie at or above its first row, so
+// stores of earlier waves never touch them, and a wave's stores wait for all
+// of its loads: in-place compaction needs no second buffer and no spin-wait
+// between CTAs.  Loads run two waves ahead of the stores.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,8 +34,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunkRows = 32;  // rows per chunk: one per lane of the copy warp
-constexpr int kStages = 8;
+constexpr int kMaxBufs = 8;             // ring of wave buffers (count set by the host)
+constexpr uint32_t kBufBytes = 32768;   // one wave of one CTA: RS rows of K and of V
 
 __device__ __forceinline__ uint32_t order_key(float s) {
   uint32_t u = __float_as_uint(s);
@@ -56,7 +60,7 @@ __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot) {
 }
 
 struct __align__(16) Smem {
-  uint64_t full[kStages];
+  uint64_t full[kMaxBufs];
   int32_t hist[256];
   int32_t warp_tot[kWarps];
   uint32_t prefix;
@@ -65,202 +69,273 @@ struct __align__(16) Smem {
   int32_t pad;
 };
 
+// Layout: Smem | kept list [B] | new kpos of this CTA's rows [B + 128] | ring.
+// (A CTA's kpos entries are indexed wave * RS + row; the last wave may run
+// up to RS - 1 <= 127 entries past its rows.)
+__host__ __device__ constexpr size_t kept_offset() { return (sizeof(Smem) + 15) & ~size_t(15); }
+__host__ __device__ inline size_t kpn_offset(int B) {
+  return kept_offset() + static_cast<size_t>(B) * 4;
+}
+__host__ __device__ inline size_t bufs_offset(int B) {
+  return (kpn_offset(B) + (static_cast<size_t>(B) + 128) * 4 + 1023) & ~static_cast<size_t>(1023);
+}
+
+// Select the kept slots of unit u into kept_s[0, n_kept); returns n_kept.
+// keys_s: the unit's order keys in shared memory, or null (read scores).
+__device__ int select_kept(const SelectParams& p, const float* sc, const uint32_t* keys_s,
+                           int L, int32_t* kept_s, Smem* sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int n_kept = L <= p.B ? L : p.B;
+  if (L <= p.B) {
+    for (int i = tid; i < n_kept; i += kThreads) kept_s[i] = i;
+    __syncthreads();
+    return n_kept;
+  }
+  auto key_at = [&](int j) { return keys_s != nullptr ? keys_s[j] : order_key(sc[j]); };
+  // ---------------- radix select of the (B - R)-th largest candidate
+  const int ncand = L - p.R;
+  const int k = p.B - p.R;
+  uint32_t prefix = 0;
+  int krem = k;
+  if (k > 0) {
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
+      sm->hist[tid] = 0;
+      __syncthreads();
+      for (int j0 = 0; j0 < ncand; j0 += kThreads) {
+        const int j = j0 + tid;
+        const bool in = j < ncand;
+        const uint32_t key = in ? key_at(j) : 0u;
+        const bool hit = in && (key & hmask) == prefix;
+        const uint32_t bin = (key >> shift) & 255u;
+        const uint32_t active = __ballot_sync(0xffffffffu, hit);
+        if (hit) {
+          const uint32_t same = __match_any_sync(active, bin);
+          if ((__ffs(same) - 1) == lane) atomicAdd(&sm->hist[bin], __popc(same));
+        }
+      }
+      __syncthreads();
+      // bins from the top: thread t holds bin 255 - t
+      const int h = sm->hist[255 - tid];
+      const int incl = block_incl_scan(h, sm->warp_tot);
+      if (incl >= krem && incl - h < krem) {
+        sm->prefix = prefix | (static_cast<uint32_t>(255 - tid) << shift);
+        sm->krem = krem - (incl - h);
+      }
+      __syncthreads();
+      prefix = sm->prefix;
+      krem = sm->krem;
+    }
+  } else {
+    prefix = 0xFFFFFFFFu;  // keep no candidate: only the window
+    krem = 0;
+  }
+  const uint32_t T = prefix;
+  const int need_eq = krem;  // candidates equal to T kept, lowest slots first
+  // ---------------- ascending kept list: contiguous segment per thread
+  const int seg = (L + kThreads - 1) / kThreads;
+  const int j0 = min(tid * seg, L), j1 = min(j0 + seg, L);
+  int eq_local = 0;
+  for (int j = j0; j < j1 && j < ncand; ++j) eq_local += key_at(j) == T;
+  const int eq_before = block_incl_scan(eq_local, sm->warp_tot) - eq_local;
+  int kept_local = 0;
+  {
+    int e = eq_before;
+    for (int j = j0; j < j1; ++j) {
+      bool keep = j >= ncand;
+      if (!keep) {
+        const uint32_t key = key_at(j);
+        keep = key > T || (key == T && e++ < need_eq);
+      }
+      kept_local += keep;
+    }
+  }
+  int pos = block_incl_scan(kept_local, sm->warp_tot) - kept_local;
+  {
+    int e = eq_before;
+    for (int j = j0; j < j1; ++j) {
+      bool keep = j >= ncand;
+      if (!keep) {
+        const uint32_t key = key_at(j);
+        keep = key > T || (key == T && e++ < need_eq);
+      }
+      if (keep) kept_s[pos++] = j;
+    }
+  }
+  __syncthreads();
+  return n_kept;
+}
+
 __global__ void __launch_bounds__(kThreads)
     select_compact_kernel(const __grid_constant__ SelectParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem* sm = reinterpret_cast<Smem*>(smem_raw);
-  int32_t* kept_s = reinterpret_cast<int32_t*>(smem_raw + sizeof(Smem));
-  uint8_t* stages =
-      smem_raw + ((sizeof(Smem) + static_cast<size_t>(p.B) * 4 + 1023) & ~static_cast<size_t>(1023));
-  const int u = blockIdx.x >> 1, part = blockIdx.x & 1;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t* kept_s = reinterpret_cast<int32_t*>(smem_raw + kept_offset());
+  int32_t* kpn = reinterpret_cast<int32_t*>(smem_raw + kpn_offset(p.B));
+  uint8_t* bufs = smem_raw + bufs_offset(p.B);
+  const int nbufs = p.nbufs;
+  const int ncl = static_cast<int>(cluster_nctarank());
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int u = blockIdx.x / ncl;
+  const int tid = threadIdx.x;
   const float* sc = p.scores + static_cast<size_t>(u) * p.L_cap;
 
   int L = p.L[u];
   const bool valid = L >= 0 && L <= p.L_cap;
   if (!valid) {
-    if (tid == 0) record_error(p.ws, BKV_EDEVICE, kSiteSelectState);
+    if (tid == 0 && rank == 0) record_error(p.ws, BKV_EDEVICE, kSiteSelectState);
     L = 0;
   }
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) mbar_init(&sm->full[i], 1);
+    for (int i = 0; i < nbufs; ++i) mbar_init(&sm->full[i], 1);
     fence_mbar_init();
+    sm->first = 0x7fffffff;
   }
-  const int n_kept = L <= p.B ? L : p.B;
-
-  if (L <= p.B) {
-    for (int i = tid; i < n_kept; i += kThreads) kept_s[i] = i;
-  } else {
-    // ---------------- radix select of the (B - R)-th largest candidate
-    const int ncand = L - p.R;
-    const int k = p.B - p.R;
-    uint32_t prefix = 0;
-    int krem = k;
-    if (k > 0) {
-      for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (shift + 8));
-        sm->hist[tid] = 0;
-        __syncthreads();
-        for (int j0 = 0; j0 < ncand; j0 += kThreads) {
-          const int j = j0 + tid;
-          const bool in = j < ncand;
-          const uint32_t key = in ? order_key(sc[j]) : 0u;
-          const bool hit = in && (key & hmask) == prefix;
-          const uint32_t bin = (key >> shift) & 255u;
-          const uint32_t active = __ballot_sync(0xffffffffu, hit);
-          if (hit) {
-            const uint32_t same = __match_any_sync(active, bin);
-            if ((__ffs(same) - 1) == lane) atomicAdd(&sm->hist[bin], __popc(same));
-          }
-        }
-        __syncthreads();
-        // bins from the top: thread t holds bin 255 - t
-        const int h = sm->hist[255 - tid];
-        const int incl = block_incl_scan(h, sm->warp_tot);
-        if (incl >= krem && incl - h < krem) {
-          sm->prefix = prefix | (static_cast<uint32_t>(255 - tid) << shift);
-          sm->krem = krem - (incl - h);
-        }
-        __syncthreads();
-        prefix = sm->prefix;
-        krem = sm->krem;
-      }
-    } else {
-      prefix = 0xFFFFFFFFu;  // keep no candidate: only the window
-      krem = 0;
-    }
-    const uint32_t T = prefix;
-    const int need_eq = krem;  // candidates equal to T kept, lowest slots first
-    // ---------------- ascending kept list: contiguous segment per thread
-    const int seg = (L + kThreads - 1) / kThreads;
-    const int j0 = min(tid * seg, L), j1 = min(j0 + seg, L);
-    int eq_local = 0;
-    for (int j = j0; j < j1 && j < ncand; ++j) eq_local += order_key(sc[j]) == T;
-    int eq_before = block_incl_scan(eq_local, sm->warp_tot) - eq_local;
-    int kept_local = 0;
-    {
-      int e = eq_before;
-      for (int j = j0; j < j1; ++j) {
-        bool keep = j >= ncand;
-        if (!keep) {
-          const uint32_t key = order_key(sc[j]);
-          keep = key > T || (key == T && e++ < need_eq);
-        }
-        kept_local += keep;
-      }
-    }
-    int pos = block_incl_scan(kept_local, sm->warp_tot) - kept_local;
-    {
-      int e = eq_before;
-      for (int j = j0; j < j1; ++j) {
-        bool keep = j >= ncand;
-        if (!keep) {
-          const uint32_t key = order_key(sc[j]);
-          keep = key > T || (key == T && e++ < need_eq);
-        }
-        if (keep) kept_s[pos++] = j;
-      }
-    }
+  // the unit's keys, staged in the (still idle) copy ring when they fit
+  uint32_t* keys_s = nullptr;
+  if (L > p.B && static_cast<size_t>(L) * 4 <= static_cast<size_t>(nbufs) * kBufBytes) {
+    keys_s = reinterpret_cast<uint32_t*>(bufs);
+#pragma unroll 8
+    for (int j = tid; j < L; j += kThreads) keys_s[j] = order_key(sc[j]);
   }
-  if (tid == 0) sm->first = n_kept;
   __syncthreads();
+  const int n_kept = select_kept(p, sc, keys_s, L, kept_s, sm);
   // first destination row whose source differs (kept[i] == i before it)
   for (int i = tid; i < n_kept; i += kThreads)
     if (kept_s[i] != i) atomicMin(&sm->first, i);
   __syncthreads();
-  const int first = sm->first;
+  const int first = min(sm->first, n_kept);
 
-  if (part == 0) {
-    if (p.kept != nullptr)
-      for (int i = tid; i < p.B; i += kThreads)
-        p.kept[static_cast<size_t>(u) * p.B + i] = i < n_kept ? kept_s[i] : -1;
-    // kpos: gather everything first, then write (all reads precede writes)
-    int32_t* kp = p.kpos + static_cast<size_t>(u) * p.L_cap;
-    int32_t* tmp = reinterpret_cast<int32_t*>(stages);
-    for (int i = first + tid; i < n_kept; i += kThreads) tmp[i - first] = kp[kept_s[i]];
-    __syncthreads();
-    for (int i = first + tid; i < n_kept; i += kThreads) kp[i] = tmp[i - first];
-    __syncthreads();
+  if (rank == 0 && p.kept != nullptr)
+    for (int i = tid; i < p.B; i += kThreads)
+      p.kept[static_cast<size_t>(u) * p.B + i] = i < n_kept ? kept_s[i] : -1;
+
+  // ---------------- compaction in cluster-wide waves
+  const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
+  const int RS = static_cast<int>(kBufBytes / (2 * rb));  // rows per CTA per wave
+  const size_t ubase = static_cast<size_t>(u) * p.L_cap;
+  uint8_t* Kb = p.K + ubase * rb;
+  uint8_t* Vb = p.V + ubase * rb;
+  int32_t* kp = p.kpos + ubase;
+  const int nmove = n_kept - first;
+  const int per_wave = ncl * RS;
+  const int nw = nmove > 0 ? (nmove + per_wave - 1) / per_wave : 0;
+
+  auto slice = [&](int w, int& r0, int& cnt) {
+    r0 = first + (w * ncl + rank) * RS;
+    cnt = max(0, min(RS, n_kept - r0));
+  };
+  // New kpos of every row this CTA writes, gathered before the first wave's
+  // barrier (no CTA writes kpos before it); entry w * RS + t = wave w, row t.
+  for (int e = tid; e < nw * RS; e += kThreads) {
+    int r0, cnt;
+    slice(e / RS, r0, cnt);
+    if (e % RS < cnt) kpn[e] = kp[kept_s[r0 + e % RS]];
   }
-
-  // ---------------- compaction of this part's rows (one warp)
-  if (warp == 0 && first < n_kept) {
-    const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
-    uint8_t* base = (part == 0 ? p.K : p.V) + static_cast<size_t>(u) * p.L_cap * rb;
-    const int nrows = n_kept - first;
-    const int nchunks = (nrows + kChunkRows - 1) / kChunkRows;
-    const uint32_t stage_bytes = kChunkRows * rb;
-    auto issue = [&](int c) {
-      const int st = c % kStages;
-      const int r0 = first + c * kChunkRows;
-      const int cnt = min(kChunkRows, n_kept - r0);
-      if (lane == 0) mbar_arrive_expect_tx(&sm->full[st], cnt * rb);
-      __syncwarp();
-      if (lane < cnt)
-        bulk_load(stages + st * stage_bytes + lane * rb,
-                  base + static_cast<size_t>(kept_s[r0 + lane]) * rb, rb, &sm->full[st]);
-    };
-    const int pro = min(kStages, nchunks);
-    for (int c = 0; c < pro; ++c) issue(c);
-    bool ok = true;
-    int waited = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      const int st = c % kStages;
-      ok = __all_sync(0xffffffffu, wait_bar(&sm->full[st], (c / kStages) & 1));
-      if (!ok) break;
-      waited = c + 1;
-      const int r0 = first + c * kChunkRows;
-      const int cnt = min(kChunkRows, n_kept - r0);
-      if (lane == 0) {
-        bulk_store(base + static_cast<size_t>(r0) * rb, stages + st * stage_bytes, cnt * rb);
+  __syncthreads();  // the keys in the ring are dead from here on
+  // thread t < RS loads K row t of the slice, thread 128 + t loads V row t
+  auto issue = [&](int w) {
+    int r0, cnt;
+    slice(w, r0, cnt);
+    uint8_t* buf = bufs + (w % nbufs) * kBufBytes;
+    if (tid == 0) mbar_arrive_expect_tx(&sm->full[w % nbufs], 2u * cnt * rb);
+    __syncthreads();
+    const int t = tid & 127;
+    if (t < cnt) {
+      const size_t src = static_cast<size_t>(kept_s[r0 + t]) * rb;
+      if (tid < 128)
+        bulk_load(buf + t * rb, Kb + src, rb, &sm->full[w % nbufs]);
+      else
+        bulk_load(buf + (RS + t) * rb, Vb + src, rb, &sm->full[w % nbufs]);
+    }
+  };
+  // Waves w + 1 .. w + kAhead are loading while wave w is stored.  Wave
+  // w + kAhead reuses the buffer of wave w + kAhead - nbufs = w - 2, whose
+  // store is the older of the two outstanding ones (waves w - 2 and w - 1).
+  const int kAhead = nbufs - 2;
+  for (int w = 0; w < kAhead && w < nw; ++w) issue(w);
+  bool ok = true;
+  int waited = 0;
+  for (int w = 0; w < nw; ++w) {
+    const int wn = w + kAhead;
+    if (ok && wn < nw) {
+      if (tid == 0) bulk_wait_read<1>();  // all stores but wave w - 1's have read smem
+      issue(wn);
+    }
+    if (ok) {
+      ok = wait_bar(&sm->full[w % nbufs], (w / nbufs) & 1);
+      ok = __syncthreads_and(ok);
+      if (ok) waited = w + 1;
+    }
+    int r0, cnt;
+    slice(w, r0, cnt);
+    // Every CTA's sources of wave w are in its shared memory (the loads have
+    // completed), so only execution order matters here; a one-CTA cluster
+    // needs nothing beyond the __syncthreads_and above.
+    if (ncl > 1) cluster_sync_relaxed();
+    if (ok && cnt > 0) {
+      if (tid == 0) {
+        const uint8_t* buf = bufs + (w % nbufs) * kBufBytes;
+        bulk_store(Kb + static_cast<size_t>(r0) * rb, buf, cnt * rb);
+        bulk_store(Vb + static_cast<size_t>(r0) * rb, buf + RS * rb, cnt * rb);
         bulk_commit();
       }
-      // refill the stage of chunk c - 1 once its store has read the stage
-      const int cn = c - 1 + kStages;
-      if (c >= 1 && cn < nchunks) {
-        if (lane == 0) bulk_wait_read<1>();
-        __syncwarp();
-        issue(cn);
-      }
-    }
-    if (!ok) {
-      if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteSelectWait);
-      // let copies already in flight land before the CTA exits (bounded)
-      const int issued = min(nchunks, max(pro, waited - 1 + kStages));
-      for (int c = waited; c < issued; ++c) wait_bar(&sm->full[c % kStages], (c / kStages) & 1);
-    }
-    if (lane == 0) bulk_wait<0>();
-  }
-  __syncthreads();
-  // the second CTA of the unit to finish publishes the new length: both
-  // CTAs have read L by then
-  if (tid == 0) {
-    __threadfence();
-    const int old = atomicAdd(&p.unit_done[u], 1);
-    if (old == 1) {
-      if (valid) p.L[u] = n_kept;
-      p.unit_done[u] = 0;
+      if (tid < cnt) kp[r0 + tid] = kpn[w * RS + tid];
     }
   }
+  if (!ok) {
+    if (tid == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteSelectWait);
+    // let copies already in flight land before the CTA exits (bounded)
+    const int issued = min(nw, waited + kAhead + 1);  // waves 0 .. waited + kAhead
+    for (int w = waited; w < issued; ++w) wait_bar(&sm->full[w % nbufs], (w / nbufs) & 1);
+  }
+  if (tid == 0) bulk_wait<0>();
+  cluster_sync();  // every CTA of the unit has read L and finished its copies
+  if (rank == 0 && tid == 0 && valid) p.L[u] = n_kept;
 }
 
 }  // namespace
 
-size_t select_smem_bytes(int B, int row_bytes) {
-  const size_t ring = static_cast<size_t>(kStages) * kChunkRows * row_bytes;
-  const size_t kpos_tmp = static_cast<size_t>(B) * 4;  // reuses the ring before the copy
-  return ((sizeof(Smem) + static_cast<size_t>(B) * 4 + 1023) & ~static_cast<size_t>(1023)) +
-         (ring > kpos_tmp ? ring : kpos_tmp);
+// Wave buffers of the ring: as many as fit (at most 8) when there are few
+// units, each CTA then streaming with a deep pipeline; with many units, just
+// enough to stage a unit's keys (at least 3), so that two CTAs share an SM
+// and one copies while the other selects.  0 if not even 3 fit.
+int select_ring_buffers(int B, int L_cap, bool many_units) {
+  const size_t off = bufs_offset(B);
+  if (off + 3 * static_cast<size_t>(kBufBytes) > 232448) return 0;
+  int n = static_cast<int>((232448 - off) / kBufBytes);
+  if (n > kMaxBufs) n = kMaxBufs;
+  if (!many_units) return n;
+  const size_t stage = (static_cast<size_t>(L_cap) * 4 + kBufBytes - 1) / kBufBytes;
+  const int want = stage < 3 ? 3 : static_cast<int>(stage);
+  return want < n ? want : n;
+}
+
+size_t select_smem_bytes(int B, int nbufs) {
+  return bufs_offset(B) + static_cast<size_t>(nbufs) * kBufBytes;
 }
 
 cudaError_t launch_select_compact(const SelectParams& p, cudaStream_t st) {
-  const size_t smem = select_smem_bytes(p.B, p.row_bytes);
+  const size_t smem = select_smem_bytes(p.B, p.nbufs);
   cudaError_t e = cudaFuncSetAttribute(select_compact_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  select_compact_kernel<<<2 * p.U, kThreads, smem, st>>>(p);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.U * p.ncl));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.ncl);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, select_compact_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
