@@ -4,6 +4,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "../../include/bkv.h"
 #include "ptx.cuh"
@@ -61,6 +64,24 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t e, uint32_
   const uint32_t atom = e >> 6, ce = e & 63u;
   const uint32_t chunk = (ce >> 3) ^ (r & 7u);
   return atom * rows * 128u + r * 128u + (chunk << 4) + ((ce & 7u) << 1);
+}
+
+// Host: raise a kernel's dynamic shared-memory limit to `bytes` once per
+// (kernel, device) instead of on every call (the attribute is sticky).
+inline cudaError_t set_smem_once(const void* fn, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(fn, dev);
+  const auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(bytes));
+  if (e == cudaSuccess) done[key] = bytes;
+  return e;
 }
 
 }  // namespace bkv

@@ -37,7 +37,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStages = 3;
+constexpr int kStages = 6;  // Gram chunk stages (8 chunks at D = 512: two refills)
 constexpr int kMaxSel = 64;
 // Bound on |fp32 cosine - exact cosine| for the tensor-core Gram (bf16
 // products are exact; fp32 accumulation over up to 2048 terms in blocks of
@@ -46,7 +46,6 @@ constexpr int kMaxSel = 64;
 // final rounding.
 constexpr float kTauCos = 4e-5f;
 constexpr float kTauMean = 4.1e-5f;
-constexpr int kCg = 8;           // contenders per pass of the seed recheck
 constexpr int kMaxPairs = 256;   // near-minimum (contender, chosen) pairs per greedy recheck
 
 struct __align__(16) FpsShared {
@@ -65,8 +64,8 @@ struct __align__(16) FpsShared {
   int32_t cont[256];      // contenders of a recheck, ascending item index
   double cont_val[256];
   double rn64[256];       // fp64 1/||x_i|| from the exact squared norm
-  double red64[kWarps];
-  double self64[kCg];     // cos(a, a) of the seed-recheck contenders
+  double n2_64[256];      // exact squared norm ||x_i||^2
+  float rh[256], rl[256];  // 1/||x_i|| as an unevaluated float pair
   double pair64[kMaxPairs];
   int16_t pair_a[kMaxPairs];  // item of a pair's contender
   int16_t pair_s[kMaxPairs];  // its chosen item
@@ -175,6 +174,14 @@ __device__ __forceinline__ void ff_add_products(FF& acc, uint4 a, uint4 b) {
     ff_add(acc, __uint_as_float(wa[h] & 0xFFFF0000u) * __uint_as_float(wb[h] & 0xFFFF0000u));
   }
 }
+// acc += x * (rh + rl) for a bf16 value x: x * rh is split exactly into
+// p + e (TwoProd by fma), x * rl is small enough to add rounded.
+__device__ __forceinline__ void ff_add_scaled(FF& acc, float x, float rh, float rl) {
+  const float p = x * rh;
+  const float e = fmaf(x, rh, -p);
+  ff_add(acc, p);
+  acc.lo += fmaf(x, rl, e);
+}
 __device__ __forceinline__ FF ff_merge(FF a, FF b) {
   FF r{a.hi, a.lo + b.lo};
   ff_add(r, b.hi);
@@ -200,20 +207,6 @@ __device__ double warp_dot_rows(const uint16_t* X, int D, int a, int b) {
     acc = ff_merge(acc, other);
   }
   return ff_value(acc);
-}
-
-// Block-wide fp64 sum of one value per thread, in a fixed order (warp
-// butterflies, then the warps in order); the result reaches every thread.
-__device__ double block_sum64(double v, FpsShared* sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) sh->red64[warp] = v;
-  __syncthreads();
-  double t = sh->red64[0];
-  for (int w = 1; w < kWarps; ++w) t += sh->red64[w];
-  __syncthreads();
-  return t;
 }
 
 // FPS of m items out of the first n rows of unit u's buffer.  Writes the
@@ -309,9 +302,13 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   const bool band_live = h < nbands;
   const uint32_t trow = tbase + (static_cast<uint32_t>(q * 32) << 16) + h * 256;
   {
-    const double nn = ff_value(n2);
-    const double r = (i < n && nn > 0.0) ? 1.0 / sqrt(nn) : 0.0;
+    const double nn = i < n ? ff_value(n2) : 0.0;
+    const double r = nn > 0.0 ? 1.0 / sqrt(nn) : 0.0;
     sh->rn64[i] = r;
+    sh->n2_64[i] = nn;
+    const float rhi = static_cast<float>(r);
+    sh->rh[i] = rhi;
+    sh->rl[i] = static_cast<float>(r - static_cast<double>(rhi));
     sh->inv[i] = static_cast<float>(r);
   }
   __syncthreads();
@@ -338,42 +335,70 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   Top2 t = block_top2(Top2{mean, i, INFINITY}, sh, tb++ & 1);
   int seed = t.i1;
   if (!(t.v2 - t.v1 > 2.f * kTauMean) && gram_ok) {
-    // Near-tie: re-decide among the contenders with exact-product cosines.
-    // Thread j reads its own row once per group of up to kCg contenders
-    // (staged in shared memory) and forms cos(a, j) for each; the sum over
-    // j runs in a fixed order and then drops the item's own term, so two
-    // identical items get bit-identical sums and the lowest slot wins.
+    // Near-tie: re-decide among the contenders with exact-product sums.
+    // sum_j cos(a, j) = r_a * (x_a . T) with T = sum_j r_j x_j, so T is built
+    // once (slot order, float-float, exact bf16 x fp32 products by TwoProd)
+    // and each contender needs one dot product with it; the item's own term
+    // (n2_a r_a) r_a is then removed.  Two identical items get bit-identical
+    // values, so the lowest slot wins an exact tie.
     const int nc = collect_contenders(i < n && mean <= t.v1 + 2.f * kTauMean, sh);
-    const int nv = D / 8;  // 16-byte pieces per row
-    uint4* crow = reinterpret_cast<uint4*>(stages);  // the Gram's stages are free now
-    const uint4* xr = reinterpret_cast<const uint4*>(X);
-    for (int c0 = 0; c0 < nc; c0 += kCg) {
-      const int cg = min(kCg, nc - c0);
-      for (int e = tid; e < cg * nv; e += kThreads)
-        crow[e] = xr[static_cast<size_t>(sh->cont[c0 + e / nv]) * nv + e % nv];
-      __syncthreads();
-      FF acc[kCg];
+    // T in two steps, in a fixed order: thread (group g, octet o) sums items
+    // [g * per, (g + 1) * per) over columns 8o .. 8o + 7 (16-byte loads, many
+    // in flight), then the groups' partial sums are merged in group order.
+    const int noct = D / 8;
+    const int ngrp = max(1, kThreads / noct);
+    const int per = (n + ngrp - 1) / ngrp;
+    FF* Tp = reinterpret_cast<FF*>(stages);  // [ngrp][D] partials (the Gram's stages are free)
+    FF* T = Tp + static_cast<size_t>(ngrp) * D;
+    for (int w = tid; w < ngrp * noct; w += kThreads) {
+      const int g = w / noct, o = w % noct;
+      FF acc[8];
 #pragma unroll
-      for (int g = 0; g < kCg; ++g) acc[g] = FF{0.f, 0.f};
-      if (i < n) {
-        const uint4* mine = xr + static_cast<size_t>(i) * nv;
-#pragma unroll 4
-        for (int v = 0; v < nv; ++v) {
-          const uint4 xi = mine[v];
+      for (int e = 0; e < 8; ++e) acc[e] = FF{0.f, 0.f};
+      const int j0 = g * per, j1 = min(n, j0 + per);
+      const uint4* col = reinterpret_cast<const uint4*>(X) + o;
+#pragma unroll 8
+      for (int j = j0; j < j1; ++j) {
+        const uint4 v = col[static_cast<size_t>(j) * noct];
+        const float rh = sh->rh[j], rl = sh->rl[j];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int g = 0; g < kCg; ++g)
-            if (g < cg) ff_add_products(acc[g], crow[g * nv + v], xi);
+        for (int hh = 0; hh < 4; ++hh) {
+          ff_add_scaled(acc[2 * hh], __uint_as_float(wv[hh] << 16), rh, rl);
+          ff_add_scaled(acc[2 * hh + 1], __uint_as_float(wv[hh] & 0xFFFF0000u), rh, rl);
         }
       }
-      for (int g = 0; g < cg; ++g) {
-        const int a = sh->cont[c0 + g];
-        const double cj = i < n ? (ff_value(acc[g]) * sh->rn64[a]) * sh->rn64[i] : 0.0;
-        if (i == a) sh->self64[g] = cj;
-        const double tot = block_sum64(cj, sh);  // contains barriers: self64 is set
-        if (tid == 0) sh->cont_val[c0 + g] = (tot - sh->self64[g]) / static_cast<double>(n - 1);
-      }
-      __syncthreads();  // crow is rewritten by the next group
+#pragma unroll
+      for (int e = 0; e < 8; ++e) Tp[static_cast<size_t>(g) * D + 8 * o + e] = acc[e];
     }
+    __syncthreads();
+    for (int k = tid; k < D; k += kThreads) {
+      FF tk = Tp[k];
+      for (int g = 1; g < ngrp; ++g) tk = ff_merge(tk, Tp[static_cast<size_t>(g) * D + k]);
+      T[k] = tk;
+    }
+    __syncthreads();
+    for (int c = warp; c < nc; c += kWarps) {
+      const int a = sh->cont[c];
+      const uint32_t* xa = reinterpret_cast<const uint32_t*>(X + static_cast<size_t>(a) * D);
+      FF acc{0.f, 0.f};
+      for (int k2 = 2 * lane; k2 < D; k2 += 64) {
+        const uint32_t w = xa[k2 / 2];
+        ff_add_scaled(acc, __uint_as_float(w << 16), T[k2].hi, T[k2].lo);
+        ff_add_scaled(acc, __uint_as_float(w & 0xFFFF0000u), T[k2 + 1].hi, T[k2 + 1].lo);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        FF other{__shfl_xor_sync(0xffffffffu, acc.hi, o), __shfl_xor_sync(0xffffffffu, acc.lo, o)};
+        acc = ff_merge(acc, other);
+      }
+      if (lane == 0) {
+        const double ra = sh->rn64[a];
+        const double self = (sh->n2_64[a] * ra) * ra;
+        sh->cont_val[c] = (ff_value(acc) * ra - self) / static_cast<double>(n - 1);
+      }
+    }
+    __syncthreads();
     if (tid == 0) {
       int best = -1;
       double bv = 0.0;
@@ -602,9 +627,7 @@ size_t fps_smem_bytes(int C) {
 cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, cudaStream_t st) {
   const int rows = fps_stage_rows(p.C);
   const size_t smem = fps_smem_bytes(p.C);
-  cudaError_t e = cudaFuncSetAttribute(fps_update_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fps_update_kernel), smem);
   if (e != cudaSuccess) return e;
   fps_update_kernel<<<p.U, kThreads, smem, st>>>(p, bufmap, rows);
   return cudaGetLastError();

@@ -112,51 +112,69 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
   }
   for (int r = tid; r < nrows; r += nthr) row_pos[r] = row_position(p, u, row0 + r, nb, cur);
   named_sync(bar, nthr);
-  // one thread per (row, pair of 8 consecutive rotary pairs)
+  // one thread per (row, pair of 8 consecutive rotary pairs), four items at
+  // a time: all of a batch's global loads are issued before any is used
   constexpr int kGroups = H / 8;
-  for (int idx = tid; idx < nrows * kGroups; idx += nthr) {
-    const int r = idx / kGroups, grp = idx % kGroups;
-    const int rr = row0 + r;
-    const int32_t pos = row_pos[r];
-    uint16_t hi0[8], hi1[8], lo0[8], lo1[8];
-    if (pos == INT32_MIN) {
+  constexpr int kBatch = 4;
+  const int total = nrows * kGroups;
+  for (int idx0 = tid; idx0 < total; idx0 += kBatch * nthr) {
+    uint4 va[kBatch], vb[kBatch];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) hi0[k] = hi1[k] = lo0[k] = lo1[k] = 0;
-    } else {
-      const int item = rr / p.G, g = rr % p.G;
-      const uint16_t* src;
-      if (item < p.W)
-        src = p.recent_q + ((static_cast<size_t>(u) * p.W + item) * p.G + g) * D;
-      else
-        src = p.beacons + ((static_cast<size_t>(u) * p.M + (item - p.W)) * p.G + g) * D;
-      const int age = cur - pos;
-      const uint4 va = *reinterpret_cast<const uint4*>(src + grp * 8);
-      const uint4 vb = *reinterpret_cast<const uint4*>(src + H + grp * 8);
-      const uint16_t* a16 = reinterpret_cast<const uint16_t*>(&va);
-      const uint16_t* b16 = reinterpret_cast<const uint16_t*>(&vb);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int i = grp * 8 + k;
-        const float2 csv = cs[age * H + i];
-        const float x0 = bf16_bits_to_float(a16[k]), x1 = bf16_bits_to_float(b16[k]);
-        const float y0 = (x0 * csv.x - x1 * csv.y) * p.qscale;
-        const float y1 = (x1 * csv.x + x0 * csv.y) * p.qscale;
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
-        const __nv_bfloat16 l0 = __float2bfloat16_rn(y0 - __bfloat162float(h0));
-        const __nv_bfloat16 l1 = __float2bfloat16_rn(y1 - __bfloat162float(h1));
-        hi0[k] = __bfloat16_as_ushort(h0);
-        hi1[k] = __bfloat16_as_ushort(h1);
-        lo0[k] = __bfloat16_as_ushort(l0);
-        lo1[k] = __bfloat16_as_ushort(l1);
+    for (int t = 0; t < kBatch; ++t) {
+      const int idx = idx0 + t * nthr;
+      va[t] = vb[t] = make_uint4(0u, 0u, 0u, 0u);
+      if (idx < total) {
+        const int r = idx / kGroups, grp = idx % kGroups;
+        const int rr = row0 + r;
+        if (row_pos[r] != INT32_MIN) {
+          const int item = rr / p.G, g = rr % p.G;
+          const uint16_t* src =
+              item < p.W
+                  ? p.recent_q + ((static_cast<size_t>(u) * p.W + item) * p.G + g) * D
+                  : p.beacons + ((static_cast<size_t>(u) * p.M + (item - p.W)) * p.G + g) * D;
+          va[t] = *reinterpret_cast<const uint4*>(src + grp * 8);
+          vb[t] = *reinterpret_cast<const uint4*>(src + H + grp * 8);
+        }
       }
     }
-    // 8 consecutive elements = one 16-byte chunk of the swizzled image
-    const uint32_t o0 = sw128_offset(r, grp * 8, nrows);
-    const uint32_t o1 = sw128_offset(r, H + grp * 8, nrows);
-    *reinterpret_cast<uint4*>(q_hi + o0) = *reinterpret_cast<const uint4*>(hi0);
-    *reinterpret_cast<uint4*>(q_hi + o1) = *reinterpret_cast<const uint4*>(hi1);
-    *reinterpret_cast<uint4*>(q_lo + o0) = *reinterpret_cast<const uint4*>(lo0);
-    *reinterpret_cast<uint4*>(q_lo + o1) = *reinterpret_cast<const uint4*>(lo1);
+#pragma unroll
+    for (int t = 0; t < kBatch; ++t) {
+      const int idx = idx0 + t * nthr;
+      if (idx >= total) break;
+      const int r = idx / kGroups, grp = idx % kGroups;
+      const int32_t pos = row_pos[r];
+      uint16_t hi0[8], hi1[8], lo0[8], lo1[8];
+      if (pos == INT32_MIN) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) hi0[k] = hi1[k] = lo0[k] = lo1[k] = 0;
+      } else {
+        const int age = cur - pos;
+        const uint16_t* a16 = reinterpret_cast<const uint16_t*>(&va[t]);
+        const uint16_t* b16 = reinterpret_cast<const uint16_t*>(&vb[t]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int i = grp * 8 + k;
+          const float2 csv = cs[age * H + i];
+          const float x0 = bf16_bits_to_float(a16[k]), x1 = bf16_bits_to_float(b16[k]);
+          const float y0 = (x0 * csv.x - x1 * csv.y) * p.qscale;
+          const float y1 = (x1 * csv.x + x0 * csv.y) * p.qscale;
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
+          const __nv_bfloat16 l0 = __float2bfloat16_rn(y0 - __bfloat162float(h0));
+          const __nv_bfloat16 l1 = __float2bfloat16_rn(y1 - __bfloat162float(h1));
+          hi0[k] = __bfloat16_as_ushort(h0);
+          hi1[k] = __bfloat16_as_ushort(h1);
+          lo0[k] = __bfloat16_as_ushort(l0);
+          lo1[k] = __bfloat16_as_ushort(l1);
+        }
+      }
+      // 8 consecutive elements = one 16-byte chunk of the swizzled image
+      const uint32_t o0 = sw128_offset(r, grp * 8, nrows);
+      const uint32_t o1 = sw128_offset(r, H + grp * 8, nrows);
+      *reinterpret_cast<uint4*>(q_hi + o0) = *reinterpret_cast<const uint4*>(hi0);
+      *reinterpret_cast<uint4*>(q_hi + o1) = *reinterpret_cast<const uint4*>(hi1);
+      *reinterpret_cast<uint4*>(q_lo + o0) = *reinterpret_cast<const uint4*>(lo0);
+      *reinterpret_cast<uint4*>(q_lo + o1) = *reinterpret_cast<const uint4*>(lo1);
+    }
   }
   fence_proxy_async_shared();  // generic smem writes -> visible to the tensor core
   named_sync(bar, nthr);
@@ -238,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* stages = q_lo + kQBytes;
   Barriers* bars = reinterpret_cast<Barriers*>(stages + NS * kStageBytes);
   int32_t* row_pos = reinterpret_cast<int32_t*>(bars + 1);  // [128]
-  int32_t* kp = row_pos + 128;                              // [128]
-  float2* cs = reinterpret_cast<float2*>(kp + 128);         // [max(W,1)][D/2]
+  int32_t* kp = row_pos + 128;                              // [2][128] key positions
+  float2* cs = reinterpret_cast<float2*>(kp + 256);         // [max(W,1)][D/2]
 
   const int s = blockIdx.x, rb = blockIdx.y, u = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -299,10 +317,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t rpos = row_pos[lrow];
       const int32_t lim = (p.causal || rpos == INT32_MIN) ? rpos : INT32_MAX - 1;
       float m = -INFINITY, z = 0.f;
+      // key positions of the tiles, one tile ahead, in two buffers (the
+      // barrier of tile i + 1 keeps tile i + 2 from rewriting tile i's)
+      const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
+      int32_t kp_next = (t0 * kTileKeys + et) < L && ntl > 0 ? kpu[t0 * kTileKeys + et] : INT32_MAX;
       for (int i = 0; i < ntl; ++i) {
         const int b = i & 1;
-        const int j = (t0 + i) * kTileKeys + et;
-        kp[et] = j < L ? p.kpos[static_cast<size_t>(u) * p.L_cap + j] : INT32_MAX;
+        int32_t* kpb = kp + (i & 1) * 128;
+        kpb[et] = kp_next;
+        const int jn = (t0 + i + 1) * kTileKeys + et;
+        kp_next = (i + 1 < ntl && jn < L) ? kpu[jn] : INT32_MAX;
         named_sync(2, kEpiThreads);
         if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
           tc_fence_after();
@@ -316,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(&bars->tempty[b]);
             }
-            const int4* kp4 = reinterpret_cast<const int4*>(kp + c * 32);
+            const int4* kp4 = reinterpret_cast<const int4*>(kpb + c * 32);
             float t[32];
             float mx = -INFINITY;
 #pragma unroll
@@ -342,7 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (lane == 0) {
           record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
         }
-        named_sync(2, kEpiThreads);  // kp is rewritten by the next tile
       }
       const int row = rb * 128 + lrow;
       p.part[(static_cast<size_t>(u) * p.nsplit + s) * p.nrows_part + row] = make_float2(m, z);
@@ -552,8 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Barriers* bars = reinterpret_cast<Barriers*>(stages + NS * kStageBytes);
   int32_t* row_pos = reinterpret_cast<int32_t*>(bars + 1);  // [kRows]
   float* lse = reinterpret_cast<float*>(row_pos + kRows);    // [kRows]
-  int32_t* kp = reinterpret_cast<int32_t*>(lse + kRows);      // [128] current pass-1 tile
-  float2* cs = reinterpret_cast<float2*>(kp + 128);           // [max(W,1)][D/2]
+  int32_t* kp = reinterpret_cast<int32_t*>(lse + kRows);      // [2][128] pass-1 key positions
+  float2* cs = reinterpret_cast<float2*>(kp + 256);           // [max(W,1)][D/2]
 
   const int u = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -655,11 +678,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         m[blk] = -INFINITY;
         z[blk] = 0.f;
       }
-      // pass 1: thread = row; running max and sum of exp2 over the keys
+      // pass 1: thread = row; running max and sum of exp2 over the keys.  Key
+      // positions are fetched one tile ahead into two buffers (the barrier of
+      // tile i + 1 keeps tile i + 2 from rewriting tile i's).
+      const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
+      int32_t kp_next = et < L ? kpu[et] : INT32_MAX;
       for (int i = 0; i < nt; ++i) {
         const int b = i & 1;
-        const int j = i * kTileKeys + et;
-        kp[et] = j < L ? p.kpos[static_cast<size_t>(u) * p.L_cap + j] : INT32_MAX;
+        int32_t* kpb = kp + (i & 1) * 128;
+        kpb[et] = kp_next;
+        const int jn = (i + 1) * kTileKeys + et;
+        kp_next = (i + 1 < nt && jn < L) ? kpu[jn] : INT32_MAX;
         named_sync(2, kEpiThreads);
         if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
           tc_fence_after();
@@ -677,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->tempty[b]);
               }
-              const int4* kp4 = reinterpret_cast<const int4*>(kp + c * 32);
+              const int4* kp4 = reinterpret_cast<const int4*>(kpb + c * 32);
               float t[32];
               float mx = -INFINITY;
 #pragma unroll
@@ -704,7 +733,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (lane == 0) {
           record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
         }
-        named_sync(2, kEpiThreads);  // kp is rewritten by the next tile
       }
       // each row's log2-sum-exp (empty rows: every probability is 0)
 #pragma unroll
@@ -785,13 +813,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int NS, int NR>
 size_t fused_smem(int W) {
   return 1024 + 2 * static_cast<size_t>(NR) * 128 * D * 2 + NS * kTileKeys * D * 2 +
-         sizeof(Barriers) + NR * 128 * 8 + 128 * 4 +
+         sizeof(Barriers) + NR * 128 * 8 + 256 * 4 +
          static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
 }
 
 template <int D, int NS>
 size_t stats_smem(int W) {
-  return 1024 + 2 * 128 * D * 2 + NS * kTileKeys * D * 2 + sizeof(Barriers) + 128 * 4 + 128 * 4 +
+  return 1024 + 2 * 128 * D * 2 + NS * kTileKeys * D * 2 + sizeof(Barriers) + 128 * 4 + 256 * 4 +
          static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
 }
 template <int D, int NS, int NMAX>
@@ -803,8 +831,7 @@ size_t final_smem(int W) {
 template <typename Kern>
 cudaError_t launch(Kern kernel, dim3 grid, size_t smem, cudaStream_t st, const ScoreParams& p,
                    const CUtensorMap& map) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
   kernel<<<grid, kThreads, smem, st>>>(p, map);
   return cudaGetLastError();

@@ -18,14 +18,14 @@
 //     slots first).
 // Compaction (row i <- row kept[i], kept[i] >= i) runs in waves over the
 // rows that move, [first, n_kept): wave w covers ncl consecutive slices of
-// RS rows, one per CTA.  Each CTA brings its slice's source rows of K and V
-// into a shared-memory ring with TMA bulk copies (one row per thread), the
-// cluster meets at a hardware barrier once every CTA's loads of the wave have
-// landed, and only then is each slice stored back (two bulk stores of
-// contiguous rows).  Sources of a wave lie at or above its first row, so
-// stores of earlier waves never touch them, and a wave's stores wait for all
-// of its loads: in-place compaction needs no second buffer and no spin-wait
-// between CTAs.  Loads run two waves ahead of the stores.
+// RS rows, one per CTA.  Each CTA gathers its slice's source rows of K and V
+// into a shared-memory ring with 16-byte cp.async copies spread over all its
+// threads, the cluster meets at a hardware barrier once every CTA's copies
+// of the wave have landed, and only then is each slice stored back (two TMA
+// bulk stores of contiguous rows).  Sources of a wave lie at or above its
+// first row, so stores of earlier waves never touch them, and a wave's
+// stores wait for all of its loads: in-place compaction needs no second
+// buffer and no spin-wait between CTAs.  Loads run nbufs - 2 waves ahead.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -60,7 +60,6 @@ __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot) {
 }
 
 struct __align__(16) Smem {
-  uint64_t full[kMaxBufs];
   int32_t hist[256];
   int32_t warp_tot[kWarps];
   uint32_t prefix;
@@ -187,11 +186,7 @@ __global__ void __launch_bounds__(kThreads)
     if (tid == 0 && rank == 0) record_error(p.ws, BKV_EDEVICE, kSiteSelectState);
     L = 0;
   }
-  if (tid == 0) {
-    for (int i = 0; i < nbufs; ++i) mbar_init(&sm->full[i], 1);
-    fence_mbar_init();
-    sm->first = 0x7fffffff;
-  }
+  if (tid == 0) sm->first = 0x7fffffff;
   // the unit's keys, staged in the (still idle) copy ring when they fit
   uint32_t* keys_s = nullptr;
   if (L > p.B && static_cast<size_t>(L) * 4 <= static_cast<size_t>(nbufs) * kBufBytes) {
@@ -234,47 +229,46 @@ __global__ void __launch_bounds__(kThreads)
     if (e % RS < cnt) kpn[e] = kp[kept_s[r0 + e % RS]];
   }
   __syncthreads();  // the keys in the ring are dead from here on
-  // thread t < RS loads K row t of the slice, thread 128 + t loads V row t
+  // All threads gather a wave's source rows of K and V into one ring buffer
+  // with 16-byte cp.async copies (K rows first, then V rows); thread 0 then
+  // writes the wave's contiguous destination rows back with two bulk stores.
+  const int ppr = static_cast<int>(rb / 16);  // 16-byte pieces per row
   auto issue = [&](int w) {
     int r0, cnt;
     slice(w, r0, cnt);
     uint8_t* buf = bufs + (w % nbufs) * kBufBytes;
-    if (tid == 0) mbar_arrive_expect_tx(&sm->full[w % nbufs], 2u * cnt * rb);
-    __syncthreads();
-    const int t = tid & 127;
-    if (t < cnt) {
-      const size_t src = static_cast<size_t>(kept_s[r0 + t]) * rb;
-      if (tid < 128)
-        bulk_load(buf + t * rb, Kb + src, rb, &sm->full[w % nbufs]);
-      else
-        bulk_load(buf + (RS + t) * rb, Vb + src, rb, &sm->full[w % nbufs]);
+    for (int e = tid; e < 2 * cnt * ppr; e += kThreads) {
+      const int t = e / ppr, pc = e % ppr;
+      const bool is_v = t >= cnt;
+      const int row = is_v ? t - cnt : t;
+      const size_t src = static_cast<size_t>(kept_s[r0 + row]) * rb + pc * 16;
+      cp_async16(buf + (is_v ? RS + row : row) * rb + pc * 16, (is_v ? Vb : Kb) + src);
     }
   };
-  // Waves w + 1 .. w + kAhead are loading while wave w is stored.  Wave
+  // Waves w + 1 .. w + kAhead are in flight while wave w is stored.  Wave
   // w + kAhead reuses the buffer of wave w + kAhead - nbufs = w - 2, whose
   // store is the older of the two outstanding ones (waves w - 2 and w - 1).
+  // Every thread commits one cp.async group per wave slot (empty past the
+  // last wave), so "wave w landed" is "at most kAhead groups pending".
   const int kAhead = nbufs - 2;
-  for (int w = 0; w < kAhead && w < nw; ++w) issue(w);
-  bool ok = true;
-  int waited = 0;
+  for (int w = 0; w < kAhead; ++w) {
+    if (w < nw) issue(w);
+    cp_async_commit();
+  }
   for (int w = 0; w < nw; ++w) {
-    const int wn = w + kAhead;
-    if (ok && wn < nw) {
-      if (tid == 0) bulk_wait_read<1>();  // all stores but wave w - 1's have read smem
-      issue(wn);
-    }
-    if (ok) {
-      ok = wait_bar(&sm->full[w % nbufs], (w / nbufs) & 1);
-      ok = __syncthreads_and(ok);
-      if (ok) waited = w + 1;
-    }
+    if (tid == 0) bulk_wait_read<1>();  // all stores but wave w - 1's have read smem
+    __syncthreads();
+    if (w + kAhead < nw) issue(w + kAhead);
+    cp_async_commit();
+    cp_async_wait_dyn(kAhead);
+    fence_proxy_async_shared();  // this thread's smem writes -> the bulk stores
+    __syncthreads();
     int r0, cnt;
     slice(w, r0, cnt);
-    // Every CTA's sources of wave w are in its shared memory (the loads have
-    // completed), so only execution order matters here; a one-CTA cluster
-    // needs nothing beyond the __syncthreads_and above.
+    // Every CTA's sources of wave w are in its shared memory, so only
+    // execution order matters here; a one-CTA cluster needs nothing more.
     if (ncl > 1) cluster_sync_relaxed();
-    if (ok && cnt > 0) {
+    if (cnt > 0) {
       if (tid == 0) {
         const uint8_t* buf = bufs + (w % nbufs) * kBufBytes;
         bulk_store(Kb + static_cast<size_t>(r0) * rb, buf, cnt * rb);
@@ -284,12 +278,7 @@ __global__ void __launch_bounds__(kThreads)
       if (tid < cnt) kp[r0 + tid] = kpn[w * RS + tid];
     }
   }
-  if (!ok) {
-    if (tid == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteSelectWait);
-    // let copies already in flight land before the CTA exits (bounded)
-    const int issued = min(nw, waited + kAhead + 1);  // waves 0 .. waited + kAhead
-    for (int w = waited; w < issued; ++w) wait_bar(&sm->full[w % nbufs], (w / nbufs) & 1);
-  }
+  cp_async_wait<0>();
   if (tid == 0) bulk_wait<0>();
   cluster_sync();  // every CTA of the unit has read L and finished its copies
   if (rank == 0 && tid == 0 && valid) p.L[u] = n_kept;
@@ -318,9 +307,7 @@ size_t select_smem_bytes(int B, int nbufs) {
 
 cudaError_t launch_select_compact(const SelectParams& p, cudaStream_t st) {
   const size_t smem = select_smem_bytes(p.B, p.nbufs);
-  cudaError_t e = cudaFuncSetAttribute(select_compact_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(select_compact_kernel), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(p.U * p.ncl));
