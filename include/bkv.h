@@ -71,7 +71,7 @@ enum { BKV_AGG_MAX = 0, BKV_AGG_MEAN = 1 };
  *   d      head dimension: 64 or 128
  *   W      recent queries scored (ring of the last W decode steps), 0 <= W <= 64
  *   M      beacons (FPS target size), 0 <= M <= 64, M < C
- *   C      continual-buffer capacity, 2 <= C <= 256 (this build)
+ *   C      continual-buffer capacity, 2 <= C <= 512
  *   B_KV   entries an eviction keeps, 1 <= B_KV <= 16384
  *   R      always-kept recent window: the last R cache slots, 0 <= R <= B_KV
  *   L_cap  row stride (slots) of K, V, kpos and scores; L_cap >= B_KV

@@ -36,7 +36,7 @@ int validate(const bkv_dims* d) {
   if (!(d->rope_theta > 1.0) || !std::isfinite(d->rope_theta)) return BKV_EINVAL;
   if (d->W + d->M < 1 || (d->W + d->M) * d->G > 1024) return BKV_EINVAL;
   if (static_cast<int64_t>(d->U) * d->L_cap * d->d >= (int64_t(1) << 40)) return BKV_EINVAL;
-  if (d->C > 256) return BKV_EUNSUPPORTED;
+  if (d->C > 512) return BKV_EUNSUPPORTED;
   return BKV_OK;
 }
 
@@ -208,7 +208,10 @@ int bkv_fps_update(const bkv_dims* dims, const void* q_new, int64_t step, void* 
   if (!aligned16(buf) || (q_new && !aligned16(q_new)) || (recent_q && !aligned16(recent_q)) ||
       (beacons && !aligned16(beacons)))
     return BKV_EINVAL;
-  if (bkv::fps_smem_bytes(dims->C) > static_cast<size_t>(kMaxSmem)) return BKV_EUNSUPPORTED;
+  const bool cluster = dims->C > 256;
+  if ((cluster ? bkv::fps_cluster_smem_bytes() : bkv::fps_smem_bytes(dims->C)) >
+      static_cast<size_t>(kMaxSmem))
+    return BKV_EUNSUPPORTED;
   const int D = dims->G * dims->d;
   bkv::FpsParams p{};
   p.q_new = static_cast<const uint16_t*>(q_new);
@@ -231,7 +234,8 @@ int bkv_fps_update(const bkv_dims* dims, const void* q_new, int64_t step, void* 
   v = make_map(&map, buf, static_cast<uint64_t>(D), static_cast<uint64_t>(dims->C),
                static_cast<uint64_t>(dims->U), box_rows);
   if (v != BKV_OK) return v;
-  return cuda_rc(bkv::launch_fps(p, map, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_rc(cluster ? bkv::launch_fps_cluster(p, map, st) : bkv::launch_fps(p, map, st));
 }
 
 int bkv_score(const bkv_dims* dims, const void* K, const int32_t* L, const int32_t* kpos,

@@ -70,5 +70,8 @@ struct FpsParams {
 };
 
 cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, cudaStream_t st);
+// Capacities of 257..512: one cluster of ceil(C / 128) CTAs per unit.
+cudaError_t launch_fps_cluster(const FpsParams& p, const CUtensorMap& bufmap, cudaStream_t st);
+size_t fps_cluster_smem_bytes();
 
 }  // namespace bkv

@@ -68,7 +68,7 @@ def test_reserved_must_be_zero():
 
 
 def test_large_buffer_capacity_reported_unsupported():
-    d = _dims(C=512)
+    d = _dims(C=513)
     n = ctypes.c_size_t(0)
     assert bkv.raw("bkv_workspace_size")(ctypes.byref(d), ctypes.byref(n)) == bkv.EUNSUPPORTED
 

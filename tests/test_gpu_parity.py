@@ -142,16 +142,11 @@ def test_score_parity_beacon_sweep(M):
 
 
 def test_score_parity_long_cache():
+    """Scoring alone on a 32768-key cache (the oracle's beacons)."""
     cfg = wl.CONFIGS[5]
     units = wl.make_units(cfg, range(1))
-    st = DeviceState(units, cfg.with_(C=256))  # scoring does not read the buffer
-    # the 32K workload's buffer holds C = 512 items; take beacons from its
-    # first 255 items (this build's FPS handles C <= 256)
-    for u in range(st.U):
-        un = _unit(units, u)
-        idx = oracle.fps(un["buf"][:255].reshape(255, -1), cfg.M)
-        st.nb[u] = len(idx)
-        st.beac[u, : len(idx)] = dev(un["buf"][idx])
+    st = DeviceState(units, cfg)
+    _upload_oracle_beacons(st, units, cfg)
     st.score()
     assert st.status() == 0
     _score_check(cfg, units, st)
@@ -231,10 +226,14 @@ def test_fps_stream_replay_tiny():
     assert np.array_equal(host_u16(ring)[:, slots], ring_ref)
 
 
-@pytest.mark.parametrize("cfgname", ["c2", "c4m1", "c4m4", "c4m16", "c4m32", "c4m64"])
+@pytest.mark.parametrize("cfgname", ["c2", "c4m1", "c4m4", "c4m16", "c4m32", "c4m64", "c5"])
 def test_fps_compress_and_select_parity(cfgname):
-    cfg = wl.CONFIGS[2] if cfgname == "c2" else wl.config4(int(cfgname[3:]))
-    units = wl.make_units(cfg, range(4))
+    """c5: the 32K workload's buffer (C = 512, G = 5) runs on the cluster path."""
+    if cfgname in ("c2", "c5"):
+        cfg = wl.CONFIGS[int(cfgname[1])]
+    else:
+        cfg = wl.config4(int(cfgname[3:]))
+    units = wl.make_units(cfg, range(2 if cfgname == "c5" else 4))
     D = cfg.G * cfg.d
     # (a) beacons of a C - 1 item buffer, no append
     st = DeviceState(units, cfg)
@@ -259,17 +258,20 @@ def test_fps_compress_and_select_parity(cfgname):
         assert np.array_equal(st.bidx[u].cpu().numpy(), idx)
 
 
-def test_fps_exact_ties_and_zero_vectors():
+@pytest.mark.parametrize("cid", [2, 5])
+def test_fps_exact_ties_and_zero_vectors(cid):
     """Duplicated items and a zero vector: decisions on exact ties must pick
-    the lowest index, as the fp64 definition does."""
-    cfg = wl.CONFIGS[2]
+    the lowest index, as the fp64 definition does.  With C = 512 (cluster
+    path) duplicates also sit in different CTAs' bands."""
+    cfg = wl.CONFIGS[cid]
     units = wl.make_units(cfg, range(3))
     D = cfg.G * cfg.d
     buf = units["buf"].reshape(3, cfg.C, D)
     buf[0, 10:20] = buf[0, 0:10]          # duplicates
+    buf[0, cfg.C - 20:cfg.C - 10] = buf[0, 0:10]
     buf[1, 7] = 0                          # zero vector
     buf[1, 100:140] = buf[1, 60:100]
-    base = buf[2, 0].copy()                # many near-parallel items
+    base = buf[2, 0].copy()                # many identical items
     for i in range(1, cfg.C):
         buf[2, i] = base if i % 3 == 0 else buf[2, i]
     units["buf"] = buf.reshape(units["buf"].shape)
@@ -340,3 +342,12 @@ def test_round_parity_bench_round_full():
     units = wl.make_units(cfg, range(cfg.U))
     units["ring"][:, int(units["step"]) % cfg.W] = units["q_new"]
     _round_parity(cfg, units, DeviceState(units, cfg), append=False)
+
+
+def test_round_parity_32k_cache_one_unit():
+    """One unit of the 32K-cache workload at full size: the append fills the
+    512-item buffer (cluster FPS compress), beacons, scoring of 32768 keys
+    (split two-launch path), select and compaction down to 2048."""
+    cfg = wl.CONFIGS[5]
+    units = wl.make_units(cfg, range(1))
+    _round_parity(cfg, units, DeviceState(units, cfg))
