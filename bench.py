@@ -43,6 +43,14 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, help="workload id (2 = the headline)")
+    ap.add_argument("--M", type=int, default=None,
+                    help="beacon count of the R1-Distill-Qwen-7B sweep (C = 4 M)")
+    ap.add_argument("--pool", type=int, default=256,
+                    help="distinct seeded units; larger workloads tile them on the device")
+    ap.add_argument("--cycle", action="store_true",
+                    help="also time a 128-step decode cycle (appends + compress + round)")
+    ap.add_argument("--e2e-max-gb", type=float, default=12.0,
+                    help="largest host staging for the end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -55,7 +63,9 @@ def peaks():
     return 6400.0, 1800.0, "fallback"
 
 
-def cfg_of(cid):
+def cfg_of(cid, M=None):
+    if cid == 4 and M is not None:
+        return wl.config4(M)
     return wl.CONFIGS[cid]
 
 
@@ -93,13 +103,16 @@ def oracle_round_time(cfg, units, n):
 
 
 def run_reference(args, rank, world):
-    """The oracle, as it stands, timed on the host cores (rank 0 only)."""
+    """The oracle, as it stands, timed on the host cores (rank 0 only).  Each
+    step scores a bounded sample of the workload's units (sized so that the
+    whole run takes about two minutes) and is scaled to the full round."""
     if rank != 0:
         return
-    cfg = cfg_of(args.config)
-    n = 8
-    units = round_units(cfg, range(n))
-    oracle_round_time(cfg, units, 1)  # builds / loads the oracle
+    cfg = cfg_of(args.config, args.M)
+    units = round_units(cfg, range(8))
+    t1 = oracle_round_time(cfg, units, 1)  # also builds / loads the oracle
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(8, budget // max(t1, 1e-3))))
     for _ in range(args.warmup):
         oracle_round_time(cfg, units, 1)
     times = [oracle_round_time(cfg, units, n) for _ in range(args.steps)]
@@ -111,7 +124,7 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded generator)", "config": workload_desc(cfg, 1),
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{n} of {cfg.U} units per step, scaled by unit count"},
+                         "sample": f"{n} of {cfg.U} units per step, single thread, scaled by unit count"},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -252,22 +265,23 @@ def run_ours(args, rank, world):
         import torch.distributed as dist
         dist.barrier()
     from kv_cache_eviction_04_b300 import bkv
+    from kv_cache_eviction_04_b300 import workload_device as wd
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = cfg_of(args.config)
+    cfg = cfg_of(args.config, args.M)
     U = cfg.U
-    units = round_units(cfg, range(U), seed=wl.SEED + rank)
-    t = lambda a: torch.from_numpy(  # noqa: E731
-        np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).to(dev)
-    pristine = {k: t(units[k]) for k in ("K", "V", "kpos", "L", "ring", "buf", "cnt")}
+    pool = min(U, args.pool)
+    host_units = wd.pool_units(cfg, pool, seed=wl.SEED + rank, current_in_ring=True)
+    tiled = wd.tile_to_device(host_units, U, dev)
+    pristine = {k: tiled[k] for k in ("K", "V", "kpos", "L", "ring", "buf", "cnt")}
     work = {k: v.clone() for k, v in pristine.items()}
-    cur = t(units["cur_pos"])
-    step = int(units["step"])
+    cur = tiled["cur_pos"]
+    step = tiled["step"]
     M, G, d, B = cfg.M, cfg.G, cfg.d, cfg.B_KV
-    bidx = torch.zeros((U, M), dtype=torch.int32, device=dev)
-    beac = torch.zeros((U, M, G, d), dtype=torch.int16, device=dev)
+    bidx = torch.zeros((U, max(M, 1)), dtype=torch.int32, device=dev)
+    beac = torch.zeros((U, max(M, 1), G, d), dtype=torch.int16, device=dev)
     nb = torch.zeros(U, dtype=torch.int32, device=dev)
     scores = torch.zeros((U, cfg.L), dtype=torch.float32, device=dev)
     kept = torch.zeros((U, B), dtype=torch.int32, device=dev)
@@ -323,51 +337,59 @@ def run_ours(args, rank, world):
     status = bkv.get_status(ws, stream)
     if status != 0:
         raise RuntimeError(f"device status {status} during the timed steps")
-    per = np.array(per)  # ms [steps][kernel]
-    total_ms = float(per.sum())
-    total_ms = max_over_ranks(total_ms, world, dev)
+    per = np.array(per)  # ms [steps][call]
+    total_ms = max_over_ranks(float(per.sum()), world, dev)
 
-    # ---------------- end to end through host buffers (pinned)
-    host = {k: v.cpu().pin_memory() for k, v in pristine.items()}
-    host_cur = cur.cpu().pin_memory()
-    out_host = {
-        "K": torch.empty((U, B, d), dtype=torch.int16).pin_memory(),
-        "V": torch.empty((U, B, d), dtype=torch.int16).pin_memory(),
-        "kpos": torch.empty((U, B), dtype=torch.int32).pin_memory(),
-        "L": torch.empty(U, dtype=torch.int32).pin_memory(),
-        "kept": torch.empty((U, B), dtype=torch.int32).pin_memory(),
-        "beacons": torch.empty((U, M, G, d), dtype=torch.int16).pin_memory(),
-    }
-    h2d = sum(v.numel() * v.element_size() for v in host.values()) + host_cur.numel() * 4
-    d2h = sum(v.numel() * v.element_size() for v in out_host.values())
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---------------- end to end through host buffers (pinned), when they fit
+    host = {k: v.cpu().pin_memory() for k, v in pristine.items()} if \
+        sum(v.numel() * v.element_size() for v in pristine.values()) <= args.e2e_max_gb * 1e9 \
+        else None
+    e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": None, "d2h_bytes_per_step": None,
+           "note": f"host staging above {args.e2e_max_gb} GB: not measured"}
+    if host is not None:
+        host_cur = cur.cpu().pin_memory()
+        out_host = {
+            "K": torch.empty((U, B, d), dtype=torch.int16).pin_memory(),
+            "V": torch.empty((U, B, d), dtype=torch.int16).pin_memory(),
+            "kpos": torch.empty((U, B), dtype=torch.int32).pin_memory(),
+            "L": torch.empty(U, dtype=torch.int32).pin_memory(),
+            "kept": torch.empty((U, B), dtype=torch.int32).pin_memory(),
+            "beacons": torch.empty(tuple(beac.shape), dtype=torch.int16).pin_memory(),
+        }
+        h2d = sum(v.numel() * v.element_size() for v in host.values()) + host_cur.numel() * 4
+        d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
-    def e2e_step():
-        flush.fill_(1)
-        e0.record(stream)
-        for k, v in host.items():
-            work[k].copy_(v, non_blocking=True)
-        cur.copy_(host_cur, non_blocking=True)
-        bkv.fps_update(dims, None, step, work["ring"], work["buf"], work["cnt"], True, bidx,
-                       beac, nb, ws, stream)
-        bkv.score(dims, work["K"], work["L"], work["kpos"], work["ring"], step, beac, nb, cur,
-                  scores, ws, stream)
-        bkv.select_compact(dims, scores, work["K"], work["V"], work["kpos"], work["L"], kept, ws,
-                           stream)
-        out_host["K"].copy_(work["K"][:, :B], non_blocking=True)
-        out_host["V"].copy_(work["V"][:, :B], non_blocking=True)
-        out_host["kpos"].copy_(work["kpos"][:, :B], non_blocking=True)
-        out_host["L"].copy_(work["L"], non_blocking=True)
-        out_host["kept"].copy_(kept, non_blocking=True)
-        out_host["beacons"].copy_(beac, non_blocking=True)
-        e1.record(stream)
-        e1.synchronize()
-        return e0.elapsed_time(e1)
+        def e2e_step():
+            flush.fill_(1)
+            e0.record(stream)
+            for k, v in host.items():
+                work[k].copy_(v, non_blocking=True)
+            cur.copy_(host_cur, non_blocking=True)
+            bkv.fps_update(dims, None, step, work["ring"], work["buf"], work["cnt"], True, bidx,
+                           beac, nb, ws, stream)
+            bkv.score(dims, work["K"], work["L"], work["kpos"], work["ring"], step, beac, nb,
+                      cur, scores, ws, stream)
+            bkv.select_compact(dims, scores, work["K"], work["V"], work["kpos"], work["L"], kept,
+                               ws, stream)
+            out_host["K"].copy_(work["K"][:, :B], non_blocking=True)
+            out_host["V"].copy_(work["V"][:, :B], non_blocking=True)
+            out_host["kpos"].copy_(work["kpos"][:, :B], non_blocking=True)
+            out_host["L"].copy_(work["L"], non_blocking=True)
+            out_host["kept"].copy_(kept, non_blocking=True)
+            out_host["beacons"].copy_(beac, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1)
 
-    for _ in range(3):
-        e2e_step()
-    e2e_ms = float(np.median([e2e_step() for _ in range(max(5, min(args.steps, 20)))]))
-    e2e_val = world * 1e3 / e2e_ms
+        for _ in range(3):
+            e2e_step()
+        e2e_ms = float(np.median([e2e_step() for _ in range(max(5, min(args.steps, 20)))]))
+        e2e = {"value": world * 1e3 / e2e_ms, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    cycle = run_cycle(args, cfg, dims, pristine, work, cur, step, bidx, beac, nb, scores, kept,
+                      ws, stream, restore) if args.cycle else None
 
     if rank != 0:
         return
@@ -405,18 +427,65 @@ def run_ours(args, rank, world):
         "roofline": roofs[names[dom]],
         "rooflines": roofs,
         "clocks": clk,
-        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+        "e2e": e2e,
         "gpu_launches": 4 * args.steps,
     }
+    if pool < U:
+        line["config"]["units"] = f"{pool} distinct seeded units tiled to {U} on the device"
+    if cycle is not None:
+        line["decode_cycle"] = cycle
     if not args.no_cpu_baseline and world == 1:
-        n = U
-        units_cpu = round_units(cfg, range(n), seed=wl.SEED)
-        secs = oracle_round_time(cfg, units_cpu, n)
+        # the oracle on a bounded sample of the same units (about 20 s), scaled
+        t1 = oracle_round_time(cfg, host_units, 1)
+        n = int(max(1, min(pool, U, round(20.0 / max(t1, 1e-3)))))
+        secs = oracle_round_time(cfg, host_units, n)
         line["cpu_baseline"] = {"value": 1.0 / (secs / n * U), "unit": UNIT, "cores": 1,
                                 "kind": "oracle",
-                                "sample": f"{n} of {U} units (one full round), single thread"}
+                                "sample": f"{n} of {U} units, single thread, scaled by unit count"}
     print(json.dumps(line), flush=True)
+
+
+def run_cycle(args, cfg, dims, pristine, work, cur, step, bidx, beac, nb, scores, kept, ws,
+              stream, restore):
+    """One eviction cycle of the decode loop: 128 per-step appends to the
+    continual buffer (the first fills it, so every unit compresses), then an
+    eviction round.  Queries of the 128 steps are seeded normal draws (their
+    values only decide which items FPS keeps)."""
+    import torch
+
+    from kv_cache_eviction_04_b300 import bkv
+    g = torch.Generator(device=cur.device).manual_seed(0xC1C1E)
+    qs = [(torch.randn((cfg.U, cfg.G, cfg.d), device=cur.device, generator=g) * 3.0)
+          .to(torch.bfloat16).view(torch.int16) for _ in range(128)]
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def cycle_once():
+        restore()
+        e[0].record(stream)
+        for t in range(128):
+            bkv.fps_update(dims, qs[t], step + 1 + t, work["ring"], work["buf"], work["cnt"],
+                           False, None, None, None, ws, stream)
+        e[1].record(stream)
+        s2 = step + 128
+        bkv.fps_update(dims, None, s2, work["ring"], work["buf"], work["cnt"], True, bidx, beac,
+                       nb, ws, stream)
+        bkv.score(dims, work["K"], work["L"], work["kpos"], work["ring"], s2, beac, nb, cur,
+                  scores, ws, stream)
+        bkv.select_compact(dims, scores, work["K"], work["V"], work["kpos"], work["L"], kept, ws,
+                           stream)
+        e[2].record(stream)
+        e[2].synchronize()
+        return e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])
+
+    cycle_once()
+    reps = [cycle_once() for _ in range(max(2, min(args.steps, 5)))]
+    if bkv.get_status(ws, stream) != 0:
+        raise RuntimeError("device status set during the decode cycle")
+    app = float(np.median([r[0] for r in reps]))
+    rnd = float(np.median([r[1] for r in reps]))
+    return {"what": "128 appends (first one compresses every buffer) + one eviction round",
+            "ms": app + rnd, "appends_ms": app, "round_ms": rnd, "cycles_per_s": 1e3 / (app + rnd),
+            "launches": 128 + 4}
 
 
 def main():
