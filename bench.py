@@ -47,6 +47,9 @@ def parse():
                     help="beacon count of the R1-Distill-Qwen-7B sweep (C = 4 M)")
     ap.add_argument("--pool", type=int, default=256,
                     help="distinct seeded units; larger workloads tile them on the device")
+    ap.add_argument("--units", type=int, default=None,
+                    help="run only this many units of the workload (same per-unit shape); "
+                         "for small profiling captures of the large workloads")
     ap.add_argument("--cycle", action="store_true",
                     help="also time a 128-step decode cycle (appends + compress + round)")
     ap.add_argument("--e2e-max-gb", type=float, default=12.0,
@@ -63,10 +66,12 @@ def peaks():
     return 6400.0, 1800.0, "fallback"
 
 
-def cfg_of(cid, M=None):
-    if cid == 4 and M is not None:
-        return wl.config4(M)
-    return wl.CONFIGS[cid]
+def cfg_of(cid, M=None, units=None):
+    cfg = wl.config4(M) if (cid == 4 and M is not None) else wl.CONFIGS[cid]
+    if units is not None and units != cfg.U:
+        # same per-unit shape, fewer units: one layer, `units` sequence-heads
+        cfg = cfg.with_(layers=1, batch=units, kv_heads=1)
+    return cfg
 
 
 def round_units(cfg, units_idx, seed=wl.SEED):
@@ -270,7 +275,7 @@ def run_ours(args, rank, world):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = cfg_of(args.config, args.M)
+    cfg = cfg_of(args.config, args.M, args.units)
     U = cfg.U
     pool = min(U, args.pool)
     host_units = wd.pool_units(cfg, pool, seed=wl.SEED + rank, current_in_ring=True)
@@ -432,6 +437,8 @@ def run_ours(args, rank, world):
     }
     if pool < U:
         line["config"]["units"] = f"{pool} distinct seeded units tiled to {U} on the device"
+    if args.units is not None:
+        line["config"]["subset"] = f"{U} units of workload {args.config} (per-unit shape unchanged)"
     if cycle is not None:
         line["decode_cycle"] = cycle
     if not args.no_cpu_baseline and world == 1:

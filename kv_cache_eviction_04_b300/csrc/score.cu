@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // --------------------------------------------------------------- pass 2
-template <int D, int NS, int NMAX>
+template <int D, int NS, int NMAX, bool kMax>
 __global__ void __launch_bounds__(kThreads, 1)
     score_final_kernel(const __grid_constant__ ScoreParams p,
                        const __grid_constant__ CUtensorMap kmap) {
@@ -482,10 +482,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nrec = p.step + 1 < p.W ? static_cast<int>(p.step + 1) : p.W;
       const float inv_rows = 1.f / static_cast<float>(max((nrec + nb) * p.G, 1));
       const int nchunks = (N + 31) / 32;
+      const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
+      // this key's position, fetched one tile ahead
+      int32_t kp_ahead = INT32_MAX;
+      {
+        const int j0 = t0 * kTileKeys + q * 32 + lane;
+        if (ntl > 0 && j0 < L) kp_ahead = kpu[j0];
+      }
       for (int i = 0; i < ntl; ++i) {
         const int b = i & 1;
         const int j = (t0 + i) * kTileKeys + q * 32 + lane;
-        const int32_t kpj = j < L ? p.kpos[static_cast<size_t>(u) * p.L_cap + j] : INT32_MAX;
+        const int32_t kpj = kp_ahead;
+        kp_ahead = (i + 1 < ntl && j + kTileKeys < L) ? kpu[j + kTileKeys] : INT32_MAX;
         if (!warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
           if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
           continue;
@@ -517,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 4; ++e) {
                 float x = __uint_as_float(v[k4 * 4 + e]) - ll[e];
                 if (!nomask && kpj > pp[e]) x = -INFINITY;
-                if (p.agg == BKV_AGG_MAX)
+                if constexpr (kMax)
                   best = fmaxf(best, x);
                 else
                   acc += ex2(x);
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (j < L) {
           float* dst = p.scores + static_cast<size_t>(u) * p.L_cap + j;
-          if (p.agg == BKV_AGG_MAX) {
+          if constexpr (kMax) {
             const float sc = best == -INFINITY ? 0.f : ex2(best);
             if (p.ngrp > 1)
               atomicMax(reinterpret_cast<int*>(dst), __float_as_int(sc));
@@ -556,8 +564,237 @@ __global__ void __launch_bounds__(kThreads, 1)
 // log2-sum-exp is formed locally (no partials, no second launch), and pass 2
 // streams the same tiles again through TMA (a unit's keys are then usually
 // still in L2).  NR = 128-row blocks of the query image (1 or 2).
+//
+// Ten warps: warp 0 issues TMA, warp 1 issues MMAs, warps 2..9 are the
+// epilogue, two per TMEM lane quarter (warps w and w + 4 share quarter
+// w & 3): in pass 1 they split each tile's keys (each keeps its own running
+// max and sum of exp2 per row, merged once at the end of the pass), in pass
+// 2 they split the rows (partial maxima merged per tile through shared
+// memory), so every SM sub-partition has two epilogue warps to interleave.
+constexpr int kFusedThreads = 320;
+constexpr int kFusedEpi = 256;
+
+// Epilogue of the fused kernel (warps 2..9; thread et = threadIdx.x - 64).
+// kMax: max aggregation (else the mean), a template parameter so that the
+// per-element loops carry no branch on it.
+template <int D, int NR, uint32_t kBufCols, bool kMax>
+__device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int nt, int L,
+                                               uint32_t tbase, Barriers* bars, int32_t* row_pos,
+                                               float* lse, float2* mz, float* part,
+                                               int32_t* kp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;           // TMEM lane quarter
+  const int h = (warp - 2) >> 2;    // 0: warps 2..5, 1: warps 6..9
+  const int et = threadIdx.x - 64;  // 0..255
+  const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+  const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
+
+  // ---- pass 1: thread = row (of each row block), keys [64 h, 64 h + 64) of
+  // every tile; running max and sum of exp2 (four partial sums per chunk)
+  float m[NR], z[NR];
+  int32_t lim[NR];
+#pragma unroll
+  for (int blk = 0; blk < NR; ++blk) {
+    const int32_t rp = row_pos[blk * 128 + q * 32 + lane];
+    lim[blk] = (p.causal || rp == INT32_MIN) ? rp : INT32_MAX - 1;
+    m[blk] = -INFINITY;
+    z[blk] = 0.f;
+  }
+  // Key positions two tiles ahead (registers), stored per tile into one of
+  // two shared buffers with the largest position of each 32-key chunk (the
+  // barrier of tile i + 1 keeps tile i + 2 from rewriting tile i's).  A warp
+  // whose rows all see every key of a chunk skips the per-key mask.
+  int32_t kp_n1 = (et < 128 && et < L) ? kpu[et] : INT32_MAX;
+  int32_t kp_n2 = (et < 128 && nt > 1 && kTileKeys + et < L) ? kpu[kTileKeys + et] : INT32_MAX;
+  int32_t* kpmax = kp + 256;  // [2][4]
+  for (int i = 0; i < nt; ++i) {
+    const int b = i & 1;
+    int32_t* kpb = kp + (i & 1) * 128;
+    if (et < 128) {
+      kpb[et] = kp_n1;
+      const int32_t cm = __reduce_max_sync(0xffffffffu, kp_n1);
+      if (lane == 0) kpmax[(i & 1) * 4 + (et >> 5)] = cm;
+      kp_n1 = kp_n2;
+      const int jn = (i + 2) * kTileKeys + et;
+      kp_n2 = (i + 2 < nt && jn < L) ? kpu[jn] : INT32_MAX;
+    }
+    named_sync(2, kFusedEpi);
+    if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
+      tc_fence_after();
+#pragma unroll
+      for (int blk = 0; blk < NR; ++blk) {
+        uint32_t v[64];  // this thread's keys 64 h .. 64 h + 63 of the tile
+        const uint32_t col = tbase + lane_addr + b * kBufCols + blk * 128 + h * 64;
+        tmem_ld32(col, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(col + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_wait_ld();
+        if (blk == NR - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->tempty[b]);
+        }
+        const int lm = lim[blk];
+        const bool open = __all_sync(0xffffffffu, kpmax[(i & 1) * 4 + 2 * h] <= lm &&
+                                                      kpmax[(i & 1) * 4 + 2 * h + 1] <= lm);
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+        if (!open) {
+          const int* kh = kpb + 64 * h;
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (kh[k] > lm) v[k] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int k = 0; k < 64; k += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(v[k]));
+          mx1 = fmaxf(mx1, __uint_as_float(v[k + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(v[k + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(v[k + 3]));
+        }
+        const float mn = fmaxf(m[blk], fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+        if (mn != -INFINITY) {
+          float a0 = (m[blk] == -INFINITY) ? 0.f : z[blk] * ex2(m[blk] - mn);
+          float a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+          for (int k = 0; k < 64; k += 4) {
+            a0 += ex2(__uint_as_float(v[k]) - mn);
+            a1 += ex2(__uint_as_float(v[k + 1]) - mn);
+            a2 += ex2(__uint_as_float(v[k + 2]) - mn);
+            a3 += ex2(__uint_as_float(v[k + 3]) - mn);
+          }
+          z[blk] = (a0 + a1) + (a2 + a3);
+          m[blk] = mn;
+        }
+      }
+    } else if (lane == 0) {
+      record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+    }
+  }
+  // merge the two halves of every row into its log2-sum-exp (empty rows:
+  // every probability is 0)
+#pragma unroll
+  for (int blk = 0; blk < NR; ++blk)
+    if (h == 1) mz[blk * 128 + q * 32 + lane] = make_float2(m[blk], z[blk]);
+  named_sync(2, kFusedEpi);
+  if (h == 0) {
+#pragma unroll
+    for (int blk = 0; blk < NR; ++blk) {
+      const int r = blk * 128 + q * 32 + lane;
+      const int32_t rp = row_pos[r];
+      const float2 o = mz[r];
+      const float mm = fmaxf(m[blk], o.x);
+      float l = INFINITY;
+      if (rp != INT32_MIN) {
+        float zz = 0.f;
+        if (mm != -INFINITY) {
+          if (m[blk] != -INFINITY) zz += z[blk] * ex2(m[blk] - mm);
+          if (o.x != -INFINITY) zz += o.y * ex2(o.x - mm);
+        }
+        if (zz > 0.f) l = mm + lg2(zz);
+        atomicMin(&bars->minpos, rp);
+        if (!p.causal) row_pos[r] = INT32_MAX;
+      }
+      lse[r] = l;
+    }
+  }
+  named_sync(2, kFusedEpi);
+
+  // ---- pass 2: thread = key q * 32 + lane, rows of half h; max (or mean)
+  // over rows of exp2(s - lse), the halves merged per tile
+  const int32_t minpos = bars->minpos;
+  const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
+  const int nrec = p.step + 1 < p.W ? static_cast<int>(p.step + 1) : p.W;
+  const float inv_rows = 1.f / static_cast<float>(max((nrec + nb) * p.G, 1));
+  const int N = p.NQ16;
+  const int nchunks = (N + 31) / 32;
+  const int nch0 = (nchunks + 1) / 2;
+  const int c_begin = h ? nch0 : 0, c_end = h ? nchunks : nch0;
+  constexpr bool is_max = kMax;
+  const int key = q * 32 + lane;
+  // this key's position, fetched two tiles ahead
+  int32_t kp_a1 = (nt > 0 && key < L) ? kpu[key] : INT32_MAX;
+  int32_t kp_a2 = (nt > 1 && kTileKeys + key < L) ? kpu[kTileKeys + key] : INT32_MAX;
+  for (int i = nt; i < 2 * nt; ++i) {
+    const int b = i & 1;
+    const int j = (i - nt) * kTileKeys + key;
+    const int32_t kpj = kp_a1;
+    kp_a1 = kp_a2;
+    {
+      const int jn = j + 2 * kTileKeys;
+      kp_a2 = (i + 2 < 2 * nt && jn < L) ? kpu[jn] : INT32_MAX;
+    }
+    float r0 = -INFINITY, r1 = -INFINITY, r2 = -INFINITY, r3 = -INFINITY;  // max
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;                          // mean
+    if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
+      tc_fence_after();
+      const bool nomask = __all_sync(0xffffffffu, kpj <= minpos);
+      if (c_begin == c_end) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->tempty[b]);
+      }
+      // chunks in pairs: both TMEM loads issued before one wait
+#pragma unroll 1
+      for (int c = c_begin; c < c_end; c += 2) {
+        const bool two = c + 1 < c_end;
+        uint32_t v[64];
+        const uint32_t col = tbase + lane_addr + b * kBufCols + c * 32;
+        tmem_ld32(col, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        if (two) tmem_ld32(col + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_wait_ld();
+        if (c + 2 >= c_end) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->tempty[b]);
+        }
+        const int nv = min(two ? 64 : 32, N - c * 32);  // valid rows here (multiple of 16)
+        const float4* l4 = reinterpret_cast<const float4*>(lse + c * 32);
+        const int4* p4 = reinterpret_cast<const int4*>(row_pos + c * 32);
+#pragma unroll
+        for (int k4 = 0; k4 < 16; ++k4) {
+          if (k4 * 4 < nv) {
+            const float4 lv = l4[k4];
+            float x0 = __uint_as_float(v[k4 * 4 + 0]) - lv.x;
+            float x1 = __uint_as_float(v[k4 * 4 + 1]) - lv.y;
+            float x2 = __uint_as_float(v[k4 * 4 + 2]) - lv.z;
+            float x3 = __uint_as_float(v[k4 * 4 + 3]) - lv.w;
+            if (!nomask) {
+              const int4 pv = p4[k4];
+              if (kpj > pv.x) x0 = -INFINITY;
+              if (kpj > pv.y) x1 = -INFINITY;
+              if (kpj > pv.z) x2 = -INFINITY;
+              if (kpj > pv.w) x3 = -INFINITY;
+            }
+            if constexpr (is_max) {
+              r0 = fmaxf(r0, x0);
+              r1 = fmaxf(r1, x1);
+              r2 = fmaxf(r2, x2);
+              r3 = fmaxf(r3, x3);
+            } else {
+              s0 += ex2(x0);
+              s1 += ex2(x1);
+              s2 += ex2(x2);
+              s3 += ex2(x3);
+            }
+          }
+        }
+      }
+    } else if (lane == 0) {
+      record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+    }
+    const float mine = is_max ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : (s0 + s1) + (s2 + s3);
+    float* pb = part + (i & 1) * 128;
+    if (h == 1) pb[key] = mine;
+    named_sync(3, kFusedEpi);
+    if (h == 0 && j < L) {
+      const float both = is_max ? fmaxf(mine, pb[key]) : mine + pb[key];
+      p.scores[static_cast<size_t>(u) * p.L_cap + j] =
+          is_max ? (both == -INFINITY ? 0.f : ex2(both)) : both * inv_rows;
+    }
+  }
+}
+
 template <int D, int NS, int NR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kFusedThreads, 1)
     score_fused_kernel(const __grid_constant__ ScoreParams p,
                        const __grid_constant__ CUtensorMap kmap) {
   constexpr int kRows = NR * 128;
@@ -575,8 +812,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   Barriers* bars = reinterpret_cast<Barriers*>(stages + NS * kStageBytes);
   int32_t* row_pos = reinterpret_cast<int32_t*>(bars + 1);  // [kRows]
   float* lse = reinterpret_cast<float*>(row_pos + kRows);    // [kRows]
-  int32_t* kp = reinterpret_cast<int32_t*>(lse + kRows);      // [2][128] pass-1 key positions
-  float2* cs = reinterpret_cast<float2*>(kp + 256);           // [max(W,1)][D/2]
+  float2* mz = reinterpret_cast<float2*>(lse + kRows);        // [kRows] second half's (m, z)
+  float* part = reinterpret_cast<float*>(mz + kRows);         // [2][128] second half's maxima
+  int32_t* kp = reinterpret_cast<int32_t*>(part + 256);       // [2][128] pass-1 key positions + [2][4] chunk maxima
+  float2* cs = reinterpret_cast<float2*>(kp + 264);           // [max(W,1)][D/2]
 
   const int u = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -584,7 +823,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   split_tiles(p, u, 0, t0, t1, L);  // tiles_per_split covers the whole cache here
   const int nt = t1 - t0;
 
-  if (threadIdx.x == 0) init_barriers(bars, NS);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->tfull[i], 1);
+      mbar_init(&bars->tempty[i], 8);  // one arrival per epilogue warp
+    }
+    bars->abort_flag = 0;
+    bars->minpos = INT32_MAX;
+    fence_mbar_init();
+  }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kCols);
     tmem_relinquish();
@@ -615,8 +866,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    build_queries<D>(p, u, 0, kRows, q_hi, q_lo, row_pos, cs, threadIdx.x - 32, kThreads - 32,
-                     1);
+    build_queries<D>(p, u, 0, kRows, q_hi, q_lo, row_pos, cs, threadIdx.x - 32,
+                     kFusedThreads - 32, 1);
     if (warp == 1) {
       // ---------------- MMA issuer
       const uint32_t idesc2 = idesc_bf16_f32(128, static_cast<uint32_t>(p.NQ16));
@@ -636,28 +887,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int blk = 0; blk < NR; ++blk)
 #pragma unroll
-              for (int part = 0; part < 2; ++part) {
-                const uint32_t qbase = smem_u32(part ? q_lo : q_hi) + blk * 128 * 128;
+              for (int part2 = 0; part2 < 2; ++part2) {
+                const uint32_t qbase = smem_u32(part2 ? q_lo : q_hi) + blk * 128 * 128;
 #pragma unroll
                 for (int a = 0; a < D / 64; ++a)
 #pragma unroll
                   for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(dt + blk * 128, sdesc_sw128(qbase + a * (kRows * 128) + kk * 32),
                              sdesc_sw128(kbase + a * 16384 + kk * 32), kIdesc1,
-                             (part | a | kk) != 0);
+                             (part2 | a | kk) != 0);
               }
           } else {
             // pass 2: D[key][row] = K[key] . Q[row], N = NQ16 rows
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-              const uint32_t qbase = smem_u32(part ? q_lo : q_hi);
+            for (int part2 = 0; part2 < 2; ++part2) {
+              const uint32_t qbase = smem_u32(part2 ? q_lo : q_hi);
 #pragma unroll
               for (int a = 0; a < D / 64; ++a)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                   mma_bf16(dt, sdesc_sw128(kbase + a * 16384 + kk * 32),
                            sdesc_sw128(qbase + a * (kRows * 128) + kk * 32), idesc2,
-                           (part | a | kk) != 0);
+                           (part2 | a | kk) != 0);
             }
           }
           mma_commit(&bars->empty[st]);
@@ -666,142 +917,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     } else {
-      // ---------------- epilogue (warps 2..5; TMEM lane quarter q)
-      const int q = warp & 3;
-      const int et = threadIdx.x - 64;  // 0..127
-      float m[NR], z[NR];
-      int32_t lim[NR];
-#pragma unroll
-      for (int blk = 0; blk < NR; ++blk) {
-        const int32_t rp = row_pos[blk * 128 + q * 32 + lane];
-        lim[blk] = (p.causal || rp == INT32_MIN) ? rp : INT32_MAX - 1;
-        m[blk] = -INFINITY;
-        z[blk] = 0.f;
-      }
-      // pass 1: thread = row; running max and sum of exp2 over the keys.  Key
-      // positions are fetched one tile ahead into two buffers (the barrier of
-      // tile i + 1 keeps tile i + 2 from rewriting tile i's).
-      const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
-      int32_t kp_next = et < L ? kpu[et] : INT32_MAX;
-      for (int i = 0; i < nt; ++i) {
-        const int b = i & 1;
-        int32_t* kpb = kp + (i & 1) * 128;
-        kpb[et] = kp_next;
-        const int jn = (i + 1) * kTileKeys + et;
-        kp_next = (i + 1 < nt && jn < L) ? kpu[jn] : INT32_MAX;
-        named_sync(2, kEpiThreads);
-        if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
-          tc_fence_after();
-#pragma unroll
-          for (int blk = 0; blk < NR; ++blk) {
-#pragma unroll 1
-            for (int c = 0; c < kTileKeys / 32; ++c) {
-              uint32_t v[32];
-              tmem_ld32(tbase + (static_cast<uint32_t>(q * 32) << 16) + b * kBufCols +
-                            blk * 128 + c * 32,
-                        v);
-              tmem_wait_ld();
-              if (blk == NR - 1 && c == kTileKeys / 32 - 1) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->tempty[b]);
-              }
-              const int4* kp4 = reinterpret_cast<const int4*>(kpb + c * 32);
-              float t[32];
-              float mx = -INFINITY;
-#pragma unroll
-              for (int k4 = 0; k4 < 8; ++k4) {
-                const int4 kk = kp4[k4];
-                const int kv[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int k = k4 * 4 + e;
-                  t[k] = (kv[e] <= lim[blk]) ? __uint_as_float(v[k]) : -INFINITY;
-                  mx = fmaxf(mx, t[k]);
-                }
-              }
-              const float mn = fmaxf(m[blk], mx);
-              if (mn != -INFINITY) {
-                float acc = (m[blk] == -INFINITY) ? 0.f : z[blk] * ex2(m[blk] - mn);
-#pragma unroll
-                for (int k = 0; k < 32; ++k) acc += ex2(t[k] - mn);
-                z[blk] = acc;
-                m[blk] = mn;
-              }
-            }
-          }
-        } else if (lane == 0) {
-          record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
-        }
-      }
-      // each row's log2-sum-exp (empty rows: every probability is 0)
-#pragma unroll
-      for (int blk = 0; blk < NR; ++blk) {
-        const int r = blk * 128 + q * 32 + lane;
-        const int32_t rp = row_pos[r];
-        float l = INFINITY;
-        if (rp != INT32_MIN) {
-          if (z[blk] > 0.f) l = m[blk] + lg2(z[blk]);
-          atomicMin(&bars->minpos, rp);
-          if (!p.causal) row_pos[r] = INT32_MAX;
-        }
-        lse[r] = l;
-      }
-      named_sync(2, kEpiThreads);
-      // pass 2: thread = key; max (or mean) over rows of exp2(s - lse)
-      const int32_t minpos = bars->minpos;
-      const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
-      const int nrec = p.step + 1 < p.W ? static_cast<int>(p.step + 1) : p.W;
-      const float inv_rows = 1.f / static_cast<float>(max((nrec + nb) * p.G, 1));
-      const int N = p.NQ16;
-      const int nchunks = (N + 31) / 32;
-      for (int i = nt; i < 2 * nt; ++i) {
-        const int b = i & 1;
-        const int j = (i - nt) * kTileKeys + q * 32 + lane;
-        const int32_t kpj = j < L ? p.kpos[static_cast<size_t>(u) * p.L_cap + j] : INT32_MAX;
-        if (!warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
-          if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
-          continue;
-        }
-        tc_fence_after();
-        const bool nomask = __all_sync(0xffffffffu, kpj <= minpos);
-        float best = -INFINITY, acc = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < nchunks; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tbase + (static_cast<uint32_t>(q * 32) << 16) + b * kBufCols + c * 32, v);
-          tmem_wait_ld();
-          if (c == nchunks - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->tempty[b]);
-          }
-          const int nv = min(32, N - c * 32);
-          const float4* l4 = reinterpret_cast<const float4*>(lse + c * 32);
-          const int4* p4 = reinterpret_cast<const int4*>(row_pos + c * 32);
-#pragma unroll
-          for (int k4 = 0; k4 < 8; ++k4) {
-            if (k4 * 4 < nv) {
-              const float4 lv = l4[k4];
-              const int4 pv = p4[k4];
-              const float ll[4] = {lv.x, lv.y, lv.z, lv.w};
-              const int pp[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float x = __uint_as_float(v[k4 * 4 + e]) - ll[e];
-                if (!nomask && kpj > pp[e]) x = -INFINITY;
-                if (p.agg == BKV_AGG_MAX)
-                  best = fmaxf(best, x);
-                else
-                  acc += ex2(x);
-              }
-            }
-          }
-        }
-        if (j < L)
-          p.scores[static_cast<size_t>(u) * p.L_cap + j] =
-              p.agg == BKV_AGG_MAX ? (best == -INFINITY ? 0.f : ex2(best)) : acc * inv_rows;
-      }
+      if (p.agg == BKV_AGG_MAX)
+        fused_epilogue<D, NR, kBufCols, true>(p, u, nt, L, tbase, bars, row_pos, lse, mz, part,
+                                              kp);
+      else
+        fused_epilogue<D, NR, kBufCols, false>(p, u, nt, L, tbase, bars, row_pos, lse, mz, part,
+                                               kp);
     }
   }
   tc_fence_before();
@@ -813,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int NS, int NR>
 size_t fused_smem(int W) {
   return 1024 + 2 * static_cast<size_t>(NR) * 128 * D * 2 + NS * kTileKeys * D * 2 +
-         sizeof(Barriers) + NR * 128 * 8 + 256 * 4 +
+         sizeof(Barriers) + NR * 128 * (4 + 4 + 8) + 256 * 4 + 264 * 4 +
          static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
 }
 
@@ -830,10 +951,10 @@ size_t final_smem(int W) {
 
 template <typename Kern>
 cudaError_t launch(Kern kernel, dim3 grid, size_t smem, cudaStream_t st, const ScoreParams& p,
-                   const CUtensorMap& map) {
+                   const CUtensorMap& map, int threads = kThreads) {
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads, smem, st>>>(p, map);
+  kernel<<<grid, threads, smem, st>>>(p, map);
   return cudaGetLastError();
 }
 
@@ -842,7 +963,7 @@ cudaError_t launch(Kern kernel, dim3 grid, size_t smem, cudaStream_t st, const S
 size_t score_smem_bytes(int d, int NQ16, int W, bool fused) {
   if (fused) {
     const bool one = NQ16 <= 128;
-    if (d == 128) return one ? fused_smem<128, 3, 1>(W) : fused_smem<128, 2, 2>(W);
+    if (d == 128) return one ? fused_smem<128, 4, 1>(W) : fused_smem<128, 2, 2>(W);
     return one ? fused_smem<64, 4, 1>(W) : fused_smem<64, 4, 2>(W);
   }
   const bool small = NQ16 <= 128;
@@ -860,32 +981,43 @@ cudaError_t launch_score(const ScoreParams& p, const CUtensorMap& kmap, cudaStre
   if (p.fused) {
     const dim3 g(p.U);
     const bool one = p.NQ16 <= 128;
+    const int T = kFusedThreads;
     if (p.d == 128)
-      return one ? launch(score_fused_kernel<128, 3, 1>, g, fused_smem<128, 3, 1>(p.W), st, p,
-                          kmap)
+      return one ? launch(score_fused_kernel<128, 4, 1>, g, fused_smem<128, 4, 1>(p.W), st, p,
+                          kmap, T)
                  : launch(score_fused_kernel<128, 2, 2>, g, fused_smem<128, 2, 2>(p.W), st, p,
-                          kmap);
-    return one ? launch(score_fused_kernel<64, 4, 1>, g, fused_smem<64, 4, 1>(p.W), st, p, kmap)
-               : launch(score_fused_kernel<64, 4, 2>, g, fused_smem<64, 4, 2>(p.W), st, p, kmap);
+                          kmap, T);
+    return one ? launch(score_fused_kernel<64, 4, 1>, g, fused_smem<64, 4, 1>(p.W), st, p, kmap, T)
+               : launch(score_fused_kernel<64, 4, 2>, g, fused_smem<64, 4, 2>(p.W), st, p, kmap,
+                        T);
   }
   const dim3 g1(p.nsplit, p.nrows_part / 128, p.U);
   const dim3 g2(p.nsplit, p.ngrp, p.U);
   const bool small = p.NQ16 <= 128;
+  const bool mx = p.agg == BKV_AGG_MAX;
   cudaError_t e;
   if (p.d == 128) {
     e = launch(score_stats_kernel<128, 3>, g1, stats_smem<128, 3>(p.W), st, p, kmap);
     if (e != cudaSuccess) return e;
-    if (small)
-      return launch(score_final_kernel<128, 3, 128>, g2, final_smem<128, 3, 128>(p.W), st, p,
-                    kmap);
-    return launch(score_final_kernel<128, 2, 256>, g2, final_smem<128, 2, 256>(p.W), st, p,
-                  kmap);
+    if (small) {
+      const size_t sm = final_smem<128, 3, 128>(p.W);
+      return mx ? launch(score_final_kernel<128, 3, 128, true>, g2, sm, st, p, kmap)
+                : launch(score_final_kernel<128, 3, 128, false>, g2, sm, st, p, kmap);
+    }
+    const size_t sm = final_smem<128, 2, 256>(p.W);
+    return mx ? launch(score_final_kernel<128, 2, 256, true>, g2, sm, st, p, kmap)
+              : launch(score_final_kernel<128, 2, 256, false>, g2, sm, st, p, kmap);
   }
   e = launch(score_stats_kernel<64, 4>, g1, stats_smem<64, 4>(p.W), st, p, kmap);
   if (e != cudaSuccess) return e;
-  if (small)
-    return launch(score_final_kernel<64, 4, 128>, g2, final_smem<64, 4, 128>(p.W), st, p, kmap);
-  return launch(score_final_kernel<64, 4, 256>, g2, final_smem<64, 4, 256>(p.W), st, p, kmap);
+  if (small) {
+    const size_t sm = final_smem<64, 4, 128>(p.W);
+    return mx ? launch(score_final_kernel<64, 4, 128, true>, g2, sm, st, p, kmap)
+              : launch(score_final_kernel<64, 4, 128, false>, g2, sm, st, p, kmap);
+  }
+  const size_t sm = final_smem<64, 4, 256>(p.W);
+  return mx ? launch(score_final_kernel<64, 4, 256, true>, g2, sm, st, p, kmap)
+            : launch(score_final_kernel<64, 4, 256, false>, g2, sm, st, p, kmap);
 }
 
 }  // namespace bkv
