@@ -10,8 +10,8 @@
 #include "kernels.h"
 
 namespace bkv {
-size_t select_smem_bytes(int B, int nbufs);
-int select_ring_buffers(int B, int L_cap, bool many_units);
+size_t select_smem_bytes(int B, int nbufs, int buf_bytes);
+void select_ring(int B, int L_cap, bool many_units, int* nbufs, int* buf_bytes);
 size_t fps_smem_bytes(int C);
 }  // namespace bkv
 
@@ -303,8 +303,10 @@ int bkv_select_compact(const bkv_dims* dims, const float* scores, void* K, void*
       workspace == nullptr)
     return BKV_EINVAL;
   if (!aligned16(K) || !aligned16(V)) return BKV_EINVAL;
-  const int nbufs = bkv::select_ring_buffers(dims->B_KV, dims->L_cap, dims->U >= 2 * sm_count());
-  if (nbufs < 3 || bkv::select_smem_bytes(dims->B_KV, nbufs) > static_cast<size_t>(kMaxSmem))
+  int nbufs = 0, buf_bytes = 0;
+  bkv::select_ring(dims->B_KV, dims->L_cap, dims->U >= 2 * sm_count(), &nbufs, &buf_bytes);
+  if (nbufs < 3 ||
+      bkv::select_smem_bytes(dims->B_KV, nbufs, buf_bytes) > static_cast<size_t>(kMaxSmem))
     return BKV_EUNSUPPORTED;
   bkv::SelectParams p{};
   p.scores = scores;
@@ -321,6 +323,7 @@ int bkv_select_compact(const bkv_dims* dims, const float* scores, void* K, void*
   p.row_bytes = dims->d * 2;
   p.ncl = select_cluster_size(dims->U);
   p.nbufs = nbufs;
+  p.buf_bytes = buf_bytes;
   return cuda_rc(bkv::launch_select_compact(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -49,7 +49,8 @@ struct SelectParams {
   WsHeader* ws;
   int32_t U, L_cap, B, R, row_bytes;
   int32_t ncl;    // CTAs (one cluster) per unit, 1..8
-  int32_t nbufs;  // wave buffers of 32 KB in the ring, 3..8
+  int32_t nbufs;      // wave buffers in the ring, 3..8
+  int32_t buf_bytes;  // bytes of one wave buffer (32768 or 16384)
 };
 
 cudaError_t launch_select_compact(const SelectParams& p, cudaStream_t st);

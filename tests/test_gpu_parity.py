@@ -47,7 +47,8 @@ def _select_case(rng, U, d, L_cap, B, R, Ls, tie_frac=0.3):
 
 @pytest.mark.parametrize("d,L_cap,B,R", [(128, 2176, 2048, 16), (64, 512, 128, 16),
                                          (128, 1000, 300, 0), (128, 700, 64, 64),
-                                         (64, 4224, 4096, 16), (128, 5000, 200, 7)])
+                                         (64, 4224, 4096, 16), (128, 5000, 200, 7),
+                                         (128, 16500, 16384, 16)])
 def test_select_compact_bit_exact(d, L_cap, B, R):
     rng = np.random.default_rng(d + L_cap + B + R)
     U = 9
