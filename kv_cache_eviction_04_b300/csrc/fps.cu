@@ -7,21 +7,22 @@
 // similarity on pre-RoPE queries; each head keeps a bounded buffer that is
 // FPS-compressed to a smaller size whenever it fills up.
 //
-// One CTA (256 threads) per unit.  For a buffer of n items (each the G*d
-// pre-RoPE vector of one decode step):
+// One CTA per unit: eight item warps (thread i owns item i) and a producer
+// warp.  For a buffer of n items (each the G*d pre-RoPE vector of one
+// decode step):
 //   1. Gram matrix G = X X^T on the tensor core: TMA streams 64-column
-//      slices of X (128-byte swizzle) into shared memory and one thread
-//      issues tcgen05 MMAs; rows 0..127 and 128..255 land in TMEM columns
-//      [0, 256) and [256, 512) with fp32 accumulation.  The Gram stays in
-//      TMEM for the whole selection.
+//      slices of X (128-byte swizzle) into shared memory and one thread of
+//      the producer warp issues tcgen05 MMAs; rows 0..127 and 128..255 land
+//      in TMEM columns [0, 256) and [256, 512) with fp32 accumulation.  The
+//      Gram stays in TMEM for the whole selection.
 //      While a chunk is staged, thread i also accumulates the exact squared
 //      norm of item i from it (exact bf16 products, TwoSum sums).
 //   2. Thread i owns item i (its TMEM lane): its mean cosine to the others
-//      from its TMEM row (error-free sum) -> seed = argmin.
+//      from its TMEM row (pairwise fp32 sum) -> seed = argmin.
 //   3. Greedy: each step reads the new pick's Gram column (one TMEM column:
 //      every thread gets its own item's entry), updates its min distance
-//      1 - cos in a register and a block argmax (warp shuffles, then shared
-//      memory) picks the next item.
+//      1 - cos in a register, and a block argmax (redux.sync on
+//      order-preserving keys per warp, then one barrier) picks the next item.
 //   4. Exactness guard: an fp32 decision is final only when the winner leads
 //      the runner-up by more than twice a bound on the fp32 error; otherwise
 //      every contender within that band is re-evaluated from the bf16 inputs
@@ -38,8 +39,9 @@ namespace {
 
 using namespace fps;
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kItems = 256;                // item threads: warps 0..7, thread t = item t
+constexpr int kItemWarps = kItems / 32;
+constexpr int kThreads = kItems + 32;      // + warp 8: TMA and MMA issue for the Gram
 constexpr int kStages = 6;  // Gram chunk stages (8 chunks at D = 512: two refills)
 constexpr int kMaxSel = 64;
 constexpr int kMaxPairs = 256;   // near-minimum (contender, chosen) pairs per greedy recheck
@@ -53,272 +55,301 @@ struct __align__(16) FpsShared {
   int32_t n_sel;
   int32_t winner;
   int32_t npairs;
-  float inv[256];         // fp32 1/||x_i|| (from the exact norm)
+  int32_t pad_;
+  uint4 red[2][kItemWarps];  // per-warp {key, item, runner-up key, -} of a block top-2
+  float inv[kItems];         // fp32 1/||x_i|| from the exact squared norm
+  float n2h[kItems], n2l[kItems];  // exact squared norm ||x_i||^2 as an unevaluated float pair
   int32_t sel[kMaxSel];
   int32_t surv[kMaxSel];
-  int32_t wcount[kWarps];
-  int32_t cont[256];      // contenders of a recheck, ascending item index
-  double cont_val[256];
-  double rn64[256];       // fp64 1/||x_i|| from the exact squared norm
-  double n2_64[256];      // exact squared norm ||x_i||^2
-  float rh[256], rl[256];  // 1/||x_i|| as an unevaluated float pair
+  int32_t wcount[kItemWarps];
+  int32_t cont[kItems];      // contenders of a recheck, ascending item index
+  double cont_val[kItems];
+  double rn64[kItems];       // seed recheck: fp64 1/||x_i||
+  float2 rr[kItems];         // seed recheck: 1/||x_i|| as an unevaluated float pair
+  FF tpart[kItemWarps][64];  // seed recheck: per-warp partial sums of T over one chunk
+  FF cacc[kItems];           // seed recheck: running x_a . T of every contender
   double pair64[kMaxPairs];
   int16_t pair_a[kMaxPairs];  // item of a pair's contender
   int16_t pair_s[kMaxPairs];  // its chosen item
-  float red_v1[2][kWarps];
-  float red_v2[2][kWarps];
-  int32_t red_i1[2][kWarps];
 };
 
-// Block-wide Top2 (all threads call; result valid in every thread).  One
-// barrier: consecutive calls alternate between two reduction buffers
-// (`par` = call count & 1), so a call never overwrites what a thread of the
-// previous call may still read.
-__device__ Top2 block_top2(Top2 t, FpsShared* sh, int par) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    Top2 o2;
-    o2.v1 = __shfl_xor_sync(0xffffffffu, t.v1, o);
-    o2.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
-    o2.v2 = __shfl_xor_sync(0xffffffffu, t.v2, o);
-    t = top2_merge(t, o2);
-  }
-  if (lane == 0) {
-    sh->red_v1[par][warp] = t.v1;
-    sh->red_i1[par][warp] = t.i1;
-    sh->red_v2[par][warp] = t.v2;
-  }
-  __syncthreads();
-  Top2 r{sh->red_v1[par][0], sh->red_i1[par][0], sh->red_v2[par][0]};
-  for (int w = 1; w < kWarps; ++w)
-    r = top2_merge(r, Top2{sh->red_v1[par][w], sh->red_i1[par][w], sh->red_v2[par][w]});
-  return r;
+// Barrier of the eight item warps only (the producer warp idles after the
+// Gram), plain and with an AND reduction.
+__device__ __forceinline__ void item_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kItems) : "memory"); }
+__device__ __forceinline__ bool item_sync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kItems)
+      : "memory");
+  return r != 0;
 }
 
-// Ordered list of the items whose flag is set (thread i = item i): writes
-// them to sh->cont in ascending index order and returns how many there are.
-// Every thread calls; no cap, so a recheck always sees every contender.
+// Top2 over the items (thread t < 256 = item t, every item thread calls)
+// under the order "smaller value first, then smaller item"; the result is
+// valid in every item thread.  Warps reduce order-preserving keys with
+// redux.sync; one barrier, then every thread merges the eight warp
+// results.  Consecutive calls alternate between two buffers (`par` = call
+// count & 1), so a call never overwrites what a thread of the previous call
+// may still read.
+__device__ Top2 block_top2(float v, FpsShared* sh, int par) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const KeyTop2 w = warp_key_top2(fkey(v), warp * 32);
+  if (lane == 0) sh->red[par][warp] = make_uint4(w.k1, static_cast<uint32_t>(w.i1), w.k2, 0u);
+  item_sync();
+  uint64_t best = ~0ull;
+  uint32_t second = 0xffffffffu;
+#pragma unroll
+  for (int q = 0; q < kItemWarps; ++q) key_top2_merge(best, second, sh->red[par][q]);
+  return Top2{fkey_value(static_cast<uint32_t>(best >> 32)),
+              static_cast<int>(best & 0xffffffffu), fkey_value(second)};
+}
+
+// Ordered list of the items whose flag is set (item threads): writes them
+// to sh->cont in ascending index order and returns how many there are.
+// No cap, so a recheck always sees every contender.
 __device__ int collect_contenders(bool flag, FpsShared* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t b = __ballot_sync(0xffffffffu, flag);
   if (lane == 0) sh->wcount[warp] = __popc(b);
-  __syncthreads();
+  item_sync();
   int off = 0, total = 0;
-  for (int w = 0; w < kWarps; ++w) {
+  for (int w = 0; w < kItemWarps; ++w) {
     const int c = sh->wcount[w];
     off += w < warp ? c : 0;
     total += c;
   }
   if (flag) sh->cont[off + __popc(b & ((1u << lane) - 1u))] = threadIdx.x;
-  __syncthreads();
+  item_sync();
   return total;
 }
 
-// FPS of m items out of the first n rows of unit u's buffer.  Writes the
-// selection order to sh->sel and returns its length.  A CTA runs at most one
-// non-trivial selection per launch (after a compress the buffer holds M
-// items and the beacon pass takes all of them), so the mbarriers start from
-// phase 0 here.
-__device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
-                          uint8_t* stages, int stage_rows, int u, int n, int m) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (m <= 0) return 0;
-  if (n <= m) {
-    for (int i = tid; i < n; i += kThreads) sh->sel[i] = i;
-    __syncthreads();
-    return n;
+// fp64 1/||x_a|| from the exact squared norm (0 for a zero row).
+__device__ __forceinline__ double exact_rnorm(const FpsShared* sh, int a) {
+  return ff_value(ff_rsqrt(FF{sh->n2h[a], sh->n2l[a]}));
+}
+
+// Element (row j, column k) of a staged 64-column chunk: rows of 128 bytes
+// whose 16-byte pieces are swizzled by row & 7.
+__device__ __forceinline__ float staged_elem(const uint8_t* sb, int j, int k) {
+  const uint16_t b = *reinterpret_cast<const uint16_t*>(
+      sb + j * 128 + ((((k >> 3) ^ (j & 7)) << 4) | ((k & 7) << 1)));
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Streaming the buffer's 64-column chunks through the stage ring once more
+// (item threads only; thread 0 issues the TMA loads): chunk c goes to stage
+// c % kStages, and a stage is refilled once all item threads are done with
+// it.  Bit s of `fph` is the parity of the next completion of full[s].
+struct ChunkStream {
+  FpsShared* sh;
+  const CUtensorMap* bmap;
+  uint8_t* stages;
+  uint32_t stage_bytes, box_bytes;
+  int u, nchunks;
+  __device__ __forceinline__ void load(int c, int st) const {
+    mbar_arrive_expect_tx(&sh->full[st], box_bytes);
+    tma_load_3d(stages + st * stage_bytes, bmap, &sh->full[st], 64 * c, 0, u);
   }
+  __device__ __forceinline__ void begin() const {
+    if (threadIdx.x == 0)
+      for (int c = 0; c < min(kStages, nchunks); ++c) load(c, c);
+  }
+  // Waits for chunk c in every item thread; null when it does not arrive.
+  __device__ __forceinline__ const uint8_t* wait(int c, uint32_t& fph) const {
+    const int st = c % kStages;
+    const bool ok = item_sync_and(wait_bar(&sh->full[st], (fph >> st) & 1));
+    fph ^= 1u << st;
+    return ok ? stages + st * stage_bytes : nullptr;
+  }
+  // After all item threads are done with chunk c.
+  __device__ __forceinline__ void release(int c) const {
+    item_sync();
+    if (threadIdx.x == 0 && c + kStages < nchunks) load(c + kStages, c % kStages);
+  }
+};
+
+// Seed and greedy steps over the Gram in TMEM (the eight item warps only;
+// thread i owns item i and its TMEM lane).  Writes sh->sel[0, m).
+__device__ void fps_pick(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
+                         uint8_t* stages, uint32_t stage_bytes, uint32_t box_bytes,
+                         uint32_t tbase, uint32_t fph, bool gram_ok, int u, int n, int m) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = tid;
   const int D = p.D;
+  const float tauc = tau_cos(D), taum = tau_mean(D);
   const uint16_t* X = p.buf + static_cast<size_t>(u) * p.C * D;
   const int N = (n + 15) & ~15;
   const int nbands = (n + 127) / 128;
   const int nchunks = D / 64;
-  const uint32_t stage_bytes = static_cast<uint32_t>(stage_rows) * 128;
-  const uint32_t box_bytes = static_cast<uint32_t>(min(stage_rows, (p.C + 15) & ~15)) * 128;
-
-  if (warp == 0) tmem_alloc(&sh->tmem_base, 512);  // no relinquish: a CTA may select twice
-  if (tid == 0) sh->npairs = 0;
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = sh->tmem_base;
-  const int i = tid;  // this thread's item
-
-  // ---- Gram on the tensor core (thread 0 issues TMA and MMA).  Meanwhile
-  // every thread accumulates the exact squared norm of its own item from
-  // the staged 64-column chunks (rows of 128 bytes, whose 16-byte pieces are
-  // swizzled by row & 7).  A stage is refilled once the MMAs and all eight
-  // warps are done with it.
-  FF n2{0.f, 0.f};
-  const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(N));
-  if (tid == 0)
-    for (int c = 0; c < min(kStages, nchunks); ++c) {
-      mbar_arrive_expect_tx(&sh->full[c], box_bytes);
-      tma_load_3d(stages + c * stage_bytes, bmap, &sh->full[c], 64 * c, 0, u);
-    }
-  bool ok = true;
-  for (int c = 0; c < nchunks; ++c) {
-    const int st = c % kStages;
-    ok = __all_sync(0xffffffffu, ok && wait_bar(&sh->full[st], (c / kStages) & 1));
-    if (!ok) break;
-    const uint8_t* sb = stages + st * stage_bytes;
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t sbase = smem_u32(sb);
-      for (int h = 0; h < nbands; ++h)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16(tbase + h * 256, sdesc_sw128(sbase + h * 16384 + kk * 32),
-                   sdesc_sw128(sbase + kk * 32), idesc, (c | kk) != 0);
-      mma_commit(&sh->empty[st]);
-    }
-    if (i < n) {
-      const uint8_t* row = sb + i * 128;
-#pragma unroll
-      for (int lc = 0; lc < 8; ++lc) {
-        const uint4 v = *reinterpret_cast<const uint4*>(row + ((lc ^ (i & 7)) << 4));
-        ff_add_products(n2, v, v);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh->empty[st]);
-    if (tid == 0 && c + kStages < nchunks) {
-      if (!wait_bar(&sh->empty[st], (c / kStages) & 1)) {
-        ok = false;
-      } else {
-        mbar_arrive_expect_tx(&sh->full[st], box_bytes);
-        tma_load_3d(stages + st * stage_bytes, bmap, &sh->full[st], 64 * (c + kStages), 0, u);
-      }
-    }
-  }
-  if (tid == 0) mma_commit(&sh->done);
-  if (!ok) {
-    sh->abort_flag = 1;
-    if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteFpsWait);
-  }
-  __syncthreads();
-  warp_wait(&sh->done, 0, &sh->abort_flag);
-  tc_fence_after();
-  __syncthreads();
-  const bool gram_ok = sh->abort_flag == 0;  // block-uniform
-
   // item of this thread: band h = warp / 4, TMEM lane quarter = warp % 4
   const int h = warp >> 2, q = warp & 3;
   const bool band_live = h < nbands;
   const uint32_t trow = tbase + (static_cast<uint32_t>(q * 32) << 16) + h * 256;
-  {
-    const double nn = i < n ? ff_value(n2) : 0.0;
-    const double r = nn > 0.0 ? 1.0 / sqrt(nn) : 0.0;
-    sh->rn64[i] = r;
-    sh->n2_64[i] = nn;
-    const float rhi = static_cast<float>(r);
-    sh->rh[i] = rhi;
-    sh->rl[i] = static_cast<float>(r - static_cast<double>(rhi));
-    sh->inv[i] = static_cast<float>(r);
-  }
-  __syncthreads();
   const float inv_i = sh->inv[i];
   int tb = 0;  // block_top2 calls so far
 
-  // ---- seed: lowest mean cosine to the other items (error-free sum of the
-  // fp32 cosines, so the mean's error is that of one cosine)
+  // ---- seed: lowest mean cosine to the other items.  The fp32 cosines of a
+  // 32-column block are summed pairwise, two blocks are added and the pair
+  // sums accumulated in order (at most 9 roundings per term); the loop stays
+  // rolled so that its code is fetched once.
   float mean = INFINITY;
   if (band_live) {
-    FF acc{0.f, 0.f};
-    for (int c = 0; c < (N + 31) / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32(trow + c * 32, v);
+    float total = 0.f;
+#pragma unroll 1
+    for (int c0 = 0; c0 < N; c0 += 64) {
+      uint32_t v[2][32];
+      tmem_ld32(trow + c0, v[0]);  // columns up to c0 + 63 < 512: inside the allocation
+      tmem_ld32(trow + c0 + 32, v[1]);
       tmem_wait_ld();
+      float ps[2];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const int j = c * 32 + k;  // columns past n were never written: skip them
-        if (j < n && j != i) ff_add(acc, __uint_as_float(v[k]) * sh->inv[j]);
+      for (int b = 0; b < 2; ++b) {
+        float s[32];
+#pragma unroll
+        for (int k4 = 0; k4 < 32; k4 += 4) {
+          const float4 r4 = *reinterpret_cast<const float4*>(&sh->inv[c0 + 32 * b + k4]);
+          const float rv[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = c0 + 32 * b + k4 + e;  // columns past n hold no item: skip them
+            s[k4 + e] = (j < n && j != i) ? __uint_as_float(v[b][k4 + e]) * rv[e] : 0.f;
+          }
+        }
+#pragma unroll
+        for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+          for (int k = 0; k < w; ++k) s[k] += s[k + w];
+        ps[b] = s[0];
       }
+      total += ps[0] + ps[1];
     }
-    if (i < n) mean = (acc.hi + acc.lo) * inv_i / static_cast<float>(n - 1);
+    if (i < n) mean = total * inv_i / static_cast<float>(n - 1);
   }
-  Top2 t = block_top2(Top2{mean, i, INFINITY}, sh, tb++ & 1);
+  Top2 t = block_top2(mean, sh, tb++ & 1);
   int seed = t.i1;
-  if (!(t.v2 - t.v1 > 2.f * kTauMean) && gram_ok) {
+  if (!(t.v2 - t.v1 > 2.f * taum) && gram_ok) {
     // Near-tie: re-decide among the contenders with exact-product sums.
-    // sum_j cos(a, j) = r_a * (x_a . T) with T = sum_j r_j x_j, so T is built
-    // once (slot order, float-float, exact bf16 x fp32 products by TwoProd)
-    // and each contender needs one dot product with it; the item's own term
-    // (n2_a r_a) r_a is then removed.  Two identical items get bit-identical
-    // values, so the lowest slot wins an exact tie.
-    const int nc = collect_contenders(i < n && mean <= t.v1 + 2.f * kTauMean, sh);
-    // T in two steps, in a fixed order: thread (group g, octet o) sums items
-    // [g * per, (g + 1) * per) over columns 8o .. 8o + 7 (16-byte loads, many
-    // in flight), then the groups' partial sums are merged in group order.
-    const int noct = D / 8;
-    const int ngrp = max(1, kThreads / noct);
-    const int per = (n + ngrp - 1) / ngrp;
-    FF* Tp = reinterpret_cast<FF*>(stages);  // [ngrp][D] partials (the Gram's stages are free)
-    FF* T = Tp + static_cast<size_t>(ngrp) * D;
-    for (int w = tid; w < ngrp * noct; w += kThreads) {
-      const int g = w / noct, o = w % noct;
-      FF acc[8];
+    // sum_j cos(a, j) = r_a * (x_a . T) with T = sum_j r_j x_j, so T is
+    // built once and each contender needs one dot product with it; the
+    // item's own term (n2_a r_a) r_a is then removed.  The buffer streams
+    // through the stage ring again.  Per 64-column chunk, warp w sums the
+    // items [32 w, 32 w + 32) of every column (exact bf16 x fp32 products by
+    // TwoProd, TwoSum sums); the eight warps' partial sums are then merged
+    // in a fixed order, and one warp
+    // per contender adds that chunk's part of x_a . T.  Two identical items
+    // get bit-identical values, so the lowest slot wins an exact tie.
+    const int nc = collect_contenders(i < n && mean <= t.v1 + 2.f * taum, sh);
+    {
+      const FF r = i < n ? ff_rsqrt(FF{sh->n2h[i], sh->n2l[i]}) : FF{0.f, 0.f};
+      sh->rn64[i] = ff_value(r);
+      sh->rr[i] = make_float2(r.hi, r.lo);
+    }
+    const ChunkStream cs{sh, bmap, stages, stage_bytes, box_bytes, u, nchunks};
+    bool rok = true;
+    for (int c = tid; c < nc; c += kItems) sh->cacc[c] = FF{0.f, 0.f};
+    item_sync();
+    // With at most eight contenders, warp cc keeps contender cc's per-lane
+    // partial sums in a register across chunks and merges the lanes once at
+    // the end; otherwise each chunk's part is merged and added to cacc.  All
+    // contenders of a recheck take the same path, so identical items still
+    // get identical values.
+    const bool in_regs = nc <= kItemWarps;
+    FF dreg{0.f, 0.f};
+    cs.begin();
+    for (int c = 0; c < nchunks && rok; ++c) {
+      const uint8_t* sb = cs.wait(c, fph);
+      rok = sb != nullptr;
+      if (!rok) break;
+      // warp w: items [32 w, 32 w + 32) in four groups of eight; lane l:
+      // columns 2l and 2l + 1 (one 32-bit word of a row).  Eight independent
+      // sums per thread, merged in a fixed order.  Row j has swizzle pattern
+      // j & 7 = e for the e-th item of a group.
+      FF acc[4][2];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = FF{0.f, 0.f};
-      const int j0 = g * per, j1 = min(n, j0 + per);
-      const uint4* col = reinterpret_cast<const uint4*>(X) + o;
-#pragma unroll 8
-      for (int j = j0; j < j1; ++j) {
-        const uint4 v = col[static_cast<size_t>(j) * noct];
-        const float rh = sh->rh[j], rl = sh->rl[j];
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      for (int g = 0; g < 4; ++g) acc[g][0] = acc[g][1] = FF{0.f, 0.f};
+      const uint8_t* colb = sb + (lane & 3) * 4;
+      const int pc = lane >> 2;
+      if (32 * warp < n) {  // rows up to 32 (warp + 1) - 1 < stage rows
 #pragma unroll
-        for (int hh = 0; hh < 4; ++hh) {
-          ff_add_scaled(acc[2 * hh], __uint_as_float(wv[hh] << 16), rh, rl);
-          ff_add_scaled(acc[2 * hh + 1], __uint_as_float(wv[hh] & 0xFFFF0000u), rh, rl);
+        for (int e = 0; e < 8; ++e)
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            // rows past n hold no item: a zero value and weight add exactly nothing
+            const int j = 32 * warp + 8 * g + e;
+            uint32_t w = *reinterpret_cast<const uint32_t*>(colb + j * 128 + ((pc ^ e) << 4));
+            w = j < n ? w : 0u;
+            const float2 r = sh->rr[j];
+            ff_add_scaled(acc[g][0], __uint_as_float(w << 16), r.x, r.y);
+            ff_add_scaled(acc[g][1], __uint_as_float(w & 0xFFFF0000u), r.x, r.y);
+          }
+      }
+#pragma unroll
+      for (int q2 = 0; q2 < 2; ++q2)
+        sh->tpart[warp][2 * lane + q2] =
+            ff_merge(ff_merge(acc[0][q2], acc[1][q2]), ff_merge(acc[2][q2], acc[3][q2]));
+      item_sync();
+      for (int cc = warp; cc < nc; cc += kItemWarps) {
+        const int a = sh->cont[cc];
+        FF d{0.f, 0.f};
+#pragma unroll
+        for (int kk = lane; kk < 64; kk += 32) {
+          const FF(*tp)[64] = sh->tpart;
+          const FF tk = ff_merge(ff_merge(ff_merge(tp[0][kk], tp[1][kk]), ff_merge(tp[2][kk], tp[3][kk])),
+                                 ff_merge(ff_merge(tp[4][kk], tp[5][kk]), ff_merge(tp[6][kk], tp[7][kk])));
+          ff_add_scaled(d, staged_elem(sb, a, kk), tk.hi, tk.lo);
+        }
+        if (in_regs) {
+          dreg = ff_merge(dreg, d);
+        } else {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const FF other{__shfl_xor_sync(0xffffffffu, d.hi, o), __shfl_xor_sync(0xffffffffu, d.lo, o)};
+            d = ff_merge(d, other);
+          }
+          if (lane == 0) sh->cacc[cc] = ff_merge(sh->cacc[cc], d);
         }
       }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) Tp[static_cast<size_t>(g) * D + 8 * o + e] = acc[e];
+      cs.release(c);
     }
-    __syncthreads();
-    for (int k = tid; k < D; k += kThreads) {
-      FF tk = Tp[k];
-      for (int g = 1; g < ngrp; ++g) tk = ff_merge(tk, Tp[static_cast<size_t>(g) * D + k]);
-      T[k] = tk;
-    }
-    __syncthreads();
-    for (int c = warp; c < nc; c += kWarps) {
-      const int a = sh->cont[c];
-      const uint32_t* xa = reinterpret_cast<const uint32_t*>(X + static_cast<size_t>(a) * D);
-      FF acc{0.f, 0.f};
-      for (int k2 = 2 * lane; k2 < D; k2 += 64) {
-        const uint32_t w = xa[k2 / 2];
-        ff_add_scaled(acc, __uint_as_float(w << 16), T[k2].hi, T[k2].lo);
-        ff_add_scaled(acc, __uint_as_float(w & 0xFFFF0000u), T[k2 + 1].hi, T[k2 + 1].lo);
-      }
+    if (rok && in_regs && warp < nc) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        FF other{__shfl_xor_sync(0xffffffffu, acc.hi, o), __shfl_xor_sync(0xffffffffu, acc.lo, o)};
-        acc = ff_merge(acc, other);
+        const FF other{__shfl_xor_sync(0xffffffffu, dreg.hi, o), __shfl_xor_sync(0xffffffffu, dreg.lo, o)};
+        dreg = ff_merge(dreg, other);
       }
-      if (lane == 0) {
+      if (lane == 0) sh->cacc[warp] = dreg;
+    }
+    item_sync();
+    if (rok) {
+      for (int cc = tid; cc < nc; cc += kItems) {
+        const int a = sh->cont[cc];
         const double ra = sh->rn64[a];
-        const double self = (sh->n2_64[a] * ra) * ra;
-        sh->cont_val[c] = (ff_value(acc) * ra - self) / static_cast<double>(n - 1);
+        const double n2a = static_cast<double>(sh->n2h[a]) + static_cast<double>(sh->n2l[a]);
+        sh->cont_val[cc] = (ff_value(sh->cacc[cc]) * ra - (n2a * ra) * ra) / static_cast<double>(n - 1);
       }
-    }
-    __syncthreads();
-    if (tid == 0) {
-      int best = -1;
-      double bv = 0.0;
-      for (int c = 0; c < nc; ++c) {  // ascending index: strict < keeps the lowest
-        const double v = sh->cont_val[c];
-        if (best < 0 || v < bv) {
-          best = sh->cont[c];
-          bv = v;
+      item_sync();
+      if (tid == 0) {
+        int best = -1;
+        double bv = 0.0;
+        for (int c = 0; c < nc; ++c) {  // ascending index: strict < keeps the lowest
+          const double v = sh->cont_val[c];
+          if (best < 0 || v < bv) {
+            best = sh->cont[c];
+            bv = v;
+          }
         }
+        sh->winner = best;
       }
-      sh->winner = best;
+      item_sync();
+      seed = sh->winner;
+    } else if (tid == 0) {
+      record_error(p.ws, BKV_ETIMEOUT, kSiteFpsWait);
     }
-    __syncthreads();
-    seed = sh->winner;
   }
 
   // ---- greedy farthest-point steps
@@ -339,17 +370,17 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   dist = fminf(dist, 1.f - gram(seed));
   for (int k = 1; k < m; ++k) {
     const bool live = i < n && !chosen;
-    Top2 r = block_top2(Top2{live ? -dist : INFINITY, i, INFINITY}, sh, tb++ & 1);
+    Top2 r = block_top2(live ? -dist : INFINITY, sh, tb++ & 1);
     int win = r.i1;
-    if (!(r.v2 - r.v1 > 2.f * kTauCos) && gram_ok) {
-      const bool cont = live && -dist <= r.v1 + 2.f * kTauCos;
+    if (!(r.v2 - r.v1 > 2.f * tauc) && gram_ok) {
+      const bool cont = live && -dist <= r.v1 + 2.f * tauc;
       const int nc = collect_contenders(cont, sh);
       // A contender's exact distance is the min over the chosen items; only
       // those whose fp32 distance is within 2 tau of its fp32 min can attain
       // it, so only those pairs are re-evaluated.
       for (int s2 = 0; s2 < k; ++s2) {
         const float dv = 1.f - gram(sh->sel[s2]);
-        if (cont && dv <= dist + 2.f * kTauCos) {
+        if (cont && dv <= dist + 2.f * tauc) {
           const int slot = atomicAdd(&sh->npairs, 1);
           if (slot < kMaxPairs) {
             sh->pair_a[slot] = static_cast<int16_t>(i);
@@ -357,16 +388,16 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
           }
         }
       }
-      __syncthreads();
+      item_sync();
       const int np = sh->npairs;
       if (np <= kMaxPairs) {
-        for (int pr = warp; pr < np; pr += kWarps) {
+        for (int pr = warp; pr < np; pr += kItemWarps) {
           const int a = sh->pair_a[pr], b = sh->pair_s[pr];
-          const double cv = (warp_dot_rows(X, D, a, b) * sh->rn64[a]) * sh->rn64[b];
+          const double cv = (warp_dot_rows(X, D, a, b) * exact_rnorm(sh, a)) * exact_rnorm(sh, b);
           if (lane == 0) sh->pair64[pr] = 1.0 - cv;
         }
-        __syncthreads();
-        for (int c = tid; c < nc; c += kThreads) {
+        item_sync();
+        for (int c = tid; c < nc; c += kItems) {
           const int a = sh->cont[c];
           double dmin = INFINITY;
           for (int pr = 0; pr < np; ++pr)
@@ -375,17 +406,18 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
         }
       } else {
         // too many near-minimum pairs: every (contender, chosen) pair
-        for (int c = warp; c < nc; c += kWarps) {
+        for (int c = warp; c < nc; c += kItemWarps) {
           const int a = sh->cont[c];
+          const double ra = exact_rnorm(sh, a);
           double dmin = INFINITY;
           for (int s2 = 0; s2 < k; ++s2) {
             const int b = sh->sel[s2];
-            dmin = fmin(dmin, 1.0 - (warp_dot_rows(X, D, a, b) * sh->rn64[a]) * sh->rn64[b]);
+            dmin = fmin(dmin, 1.0 - (warp_dot_rows(X, D, a, b) * ra) * exact_rnorm(sh, b));
           }
           if (lane == 0) sh->cont_val[c] = dmin;
         }
       }
-      __syncthreads();
+      item_sync();
       if (tid == 0) {
         sh->npairs = 0;
         int best = -1;
@@ -399,13 +431,139 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
         }
         sh->winner = best;
       }
-      __syncthreads();
+      item_sync();
       win = sh->winner;
     }
     if (tid == 0) sh->sel[k] = win;
     chosen = chosen || (i == win);
     dist = fminf(dist, 1.f - gram(win));
   }
+}
+
+// FPS of m items out of the first n rows of unit u's buffer.  Writes the
+// selection order to sh->sel and returns its length (all threads call).  A
+// CTA runs at most one non-trivial selection per launch (after a compress
+// the buffer holds M items and the beacon pass takes all of them), so the
+// mbarriers start from phase 0 here.
+__device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
+                          uint8_t* stages, int stage_rows, int u, int n, int m) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (m <= 0) return 0;
+  if (n <= m) {
+    for (int i = tid; i < n; i += kThreads) sh->sel[i] = i;
+    __syncthreads();
+    return n;
+  }
+  const int D = p.D;
+  const int N = (n + 15) & ~15;
+  const int nbands = (n + 127) / 128;
+  const int nchunks = D / 64;
+  const uint32_t stage_bytes = static_cast<uint32_t>(stage_rows) * 128;
+  const uint32_t box_bytes = static_cast<uint32_t>(min(stage_rows, (p.C + 15) & ~15)) * 128;
+
+  if (warp == 0) tmem_alloc(&sh->tmem_base, 512);  // no relinquish: a CTA may select twice
+  if (tid == 0) sh->npairs = 0;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sh->tmem_base;
+
+  // Chunk c of the buffer goes to stage c % kStages; bit s of `fph` is the
+  // parity of the next completion of full[s] (the same in every thread).
+  uint32_t fph = 0;
+  auto load_chunk = [&](int c, int st) {
+    mbar_arrive_expect_tx(&sh->full[st], box_bytes);
+    tma_load_3d(stages + st * stage_bytes, bmap, &sh->full[st], 64 * c, 0, u);
+  };
+
+  // ---- Gram on the tensor core.  One thread of the producer warp streams
+  // 64-column chunks of the buffer into the stage ring by TMA and issues the
+  // tcgen05 MMAs of every chunk as soon as it lands.  Meanwhile every item
+  // thread accumulates the exact squared norm of its own item from the
+  // staged chunks.  A stage is refilled once its MMAs have completed and
+  // all eight item warps are done with it; the producer refills without
+  // waiting while it still has landed chunks to multiply.
+  FF n2p[8];  // eight independent partial sums, one per 16-byte piece of a row
+#pragma unroll
+  for (int lc = 0; lc < 8; ++lc) n2p[lc] = FF{0.f, 0.f};
+  if (warp == kItemWarps) {
+    if (lane == 0) {
+      bool ok = true;
+      const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(N));
+      for (int c = 0; c < min(kStages, nchunks); ++c) load_chunk(c, c);
+      int next = min(kStages, nchunks);  // next chunk to load
+      for (int c = 0; c < nchunks && ok; ++c) {
+        // chunk c must have been loaded: block on its stage's release if not
+        while (ok && next <= c) {
+          ok = wait_bar(&sh->empty[next % kStages], ((next - kStages) / kStages) & 1);
+          if (ok) load_chunk(next, next % kStages), ++next;
+        }
+        const int st = c % kStages;
+        if (!ok || !wait_bar(&sh->full[st], (c / kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sbase = smem_u32(stages + st * stage_bytes);
+        for (int h = 0; h < nbands; ++h)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tbase + h * 256, sdesc_sw128(sbase + h * 16384 + kk * 32),
+                     sdesc_sw128(sbase + kk * 32), idesc, (c | kk) != 0);
+        mma_commit(&sh->empty[st]);
+        // refill released stages without blocking
+        while (next < nchunks &&
+               mbar_test_wait(&sh->empty[next % kStages], ((next - kStages) / kStages) & 1)) {
+          load_chunk(next, next % kStages);
+          ++next;
+        }
+      }
+      mma_commit(&sh->done);
+      if (!ok) {
+        sh->abort_flag = 1;
+        record_error(p.ws, BKV_ETIMEOUT, kSiteFpsWait);
+      }
+    }
+    __syncwarp();
+  } else {
+    const int i = tid;
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c % kStages;
+      ok = __all_sync(0xffffffffu, ok && wait_bar(&sh->full[st], (c / kStages) & 1));
+      if (!ok) break;
+      if (i < n) {
+        const uint8_t* row = stages + st * stage_bytes + i * 128;
+#pragma unroll
+        for (int lc = 0; lc < 8; ++lc) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row + ((lc ^ (i & 7)) << 4));
+          ff_add_products(n2p[lc], v, v);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->empty[st]);
+    }
+    if (!ok) {
+      sh->abort_flag = 1;
+      if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteFpsWait);
+    }
+  }
+  for (int c = 0; c < nchunks; ++c) fph ^= 1u << (c % kStages);
+  warp_wait(&sh->done, 0, &sh->abort_flag);
+  tc_fence_after();
+  if (tid < kItems) {
+    const int i = tid;
+    const FF n2 = ff_merge(ff_merge(ff_merge(n2p[0], n2p[1]), ff_merge(n2p[2], n2p[3])),
+                           ff_merge(ff_merge(n2p[4], n2p[5]), ff_merge(n2p[6], n2p[7])));
+    const float nn = n2.hi + n2.lo;
+    sh->n2h[i] = i < n ? n2.hi : 0.f;
+    sh->n2l[i] = i < n ? n2.lo : 0.f;
+    sh->inv[i] = (i < n && nn > 0.f) ? 1.f / sqrtf(nn) : 0.f;
+  }
+  __syncthreads();
+  const bool gram_ok = sh->abort_flag == 0;  // block-uniform
+  if (warp < kItemWarps)
+    fps_pick(p, bmap, sh, stages, stage_bytes, box_bytes, tbase, fph, gram_ok, u, n, m);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -428,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sh->full[s], 1);
-      mbar_init(&sh->empty[s], kWarps + 1);  // every warp read it + the MMAs ran
+      mbar_init(&sh->empty[s], kItemWarps + 1);  // every item warp read it + the MMAs ran
     }
     mbar_init(&sh->done, 1);
     sh->abort_flag = 0;

@@ -153,6 +153,7 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
     return n;
   }
   const int D = p.D;
+  const float tauc = tau_cos(D), taum = tau_mean(D);
   const uint16_t* X = p.buf + static_cast<size_t>(u) * p.C * D;
   const int N = (n + 15) & ~15;
   const int N1 = min(N, 256), N2 = N - N1;  // column blocks: items 0..255, 256..N-1
@@ -170,7 +171,13 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
 
   // ---- Gram rows of this CTA's items against all items; exact norms of all
   // items (thread t: items t and t + 256) from the staged chunks
-  FF n2a{0.f, 0.f}, n2b{0.f, 0.f};
+  // squared norms of items t and t + 256: four partial sums each
+  // (independent chains), merged in order at the end
+  FF n2p[2][4];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) n2p[hh][e] = FF{0.f, 0.f};
   const uint32_t id1 = idesc_bf16_f32(128, static_cast<uint32_t>(N1));
   const uint32_t id2 = idesc_bf16_f32(128, static_cast<uint32_t>(N2 > 0 ? N2 : 16));
   auto load_chunk = [&](int c, int st) {
@@ -208,7 +215,7 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
 #pragma unroll
         for (int lc = 0; lc < 8; ++lc) {
           const uint4 v = *reinterpret_cast<const uint4*>(row + ((lc ^ (j & 7)) << 4));
-          ff_add_products(half ? n2b : n2a, v, v);
+          ff_add_products(n2p[half][lc & 3], v, v);
         }
       }
     }
@@ -232,14 +239,13 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int j = tid + 256 * half;
-    const double nn = j < n ? ff_value(half ? n2b : n2a) : 0.0;
-    const double r = nn > 0.0 ? 1.0 / sqrt(nn) : 0.0;
-    sh->rn64[j] = r;
-    sh->n2_64[j] = nn;
-    const float rhi = static_cast<float>(r);
-    sh->rh[j] = rhi;
-    sh->rl[j] = static_cast<float>(r - static_cast<double>(rhi));
-    sh->inv[j] = rhi;
+    const FF n2 = ff_merge(ff_merge(n2p[half][0], n2p[half][1]), ff_merge(n2p[half][2], n2p[half][3]));
+    const FF r = j < n ? ff_rsqrt(n2) : FF{0.f, 0.f};
+    sh->rn64[j] = ff_value(r);
+    sh->n2_64[j] = j < n ? ff_value(n2) : 0.0;
+    sh->rh[j] = r.hi;
+    sh->rl[j] = r.lo;
+    sh->inv[j] = r.hi;
   }
   __syncthreads();
   const uint32_t trow = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
@@ -266,9 +272,9 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
   }
   Top2 t = cluster_top2(cta_top2(Top2{mean, i, INFINITY}, sh, tb++ & 1), sh, xc++ & 1, R);
   int seed = t.i1;
-  if (!(t.v2 - t.v1 > 2.f * kTauMean)) {
+  if (!(t.v2 - t.v1 > 2.f * taum)) {
     // near-tie: as in fps.cu, sum_j cos(a, j) = r_a (x_a . T), T = sum_j r_j x_j
-    const int nc = collect_own(live_item && mean <= t.v1 + 2.f * kTauMean, base, sh);
+    const int nc = collect_own(live_item && mean <= t.v1 + 2.f * taum, base, sh);
     const int noct = D / 8;
     const int ngrp = max(1, kCT / noct);
     const int per = (n + ngrp - 1) / ngrp;
@@ -354,12 +360,12 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
         cluster_top2(cta_top2(Top2{live ? -dist : INFINITY, i, INFINITY}, sh, tb++ & 1), sh,
                      xc++ & 1, R);
     int win = r.i1;
-    if (!(r.v2 - r.v1 > 2.f * kTauCos)) {
-      const bool cont = live && -dist <= r.v1 + 2.f * kTauCos;
+    if (!(r.v2 - r.v1 > 2.f * tauc)) {
+      const bool cont = live && -dist <= r.v1 + 2.f * tauc;
       const int nc = collect_own(cont, base, sh);
       for (int s2 = 0; s2 < k; ++s2) {  // near-minimum pairs only (see fps.cu)
         const float dv = 1.f - gram(sh->sel[s2]);
-        if (cont && dv <= dist + 2.f * kTauCos) {
+        if (cont && dv <= dist + 2.f * tauc) {
           const int slot = atomicAdd(&sh->npairs, 1);
           if (slot < kMaxPairsC) {
             sh->pair_a[slot] = static_cast<int16_t>(i);

@@ -7,13 +7,18 @@
 namespace bkv {
 namespace fps {
 
-// Bound on |fp32 cosine - exact cosine| for the tensor-core Gram (bf16
-// products are exact; fp32 accumulation over up to 2048 terms in blocks of
-// 16, plus the normalisation by exact norms) with a safety factor.  The
-// seed's mean sums its terms error-free, so its bound is the same plus the
-// final rounding.
-constexpr float kTauCos = 4e-5f;
-constexpr float kTauMean = 4.1e-5f;
+// Bound on |fp32 cosine - exact cosine| for a tensor-core Gram over rows of
+// D bf16 values, normalised by 1/||x|| from exact norms (rounded to fp32).
+// bf16 products are exact; the fp32 accumulation in steps of 16 products is
+// taken to lose at most 2 ulp (2^-22) of the running sum per step, so an
+// entry is within e = (D / 16) 2^-22 ||x_i|| ||x_j||; the bound is 1.3 e
+// plus 1e-6 for the fp32 normalisation (a few roundings of at most 2^-24).
+// The seed's mean sums at most 512 such cosines in fp32 with at most 9
+// roundings per term (below 1e-6 in all), so its bound is 1e-6 more.
+__device__ __forceinline__ float tau_cos(int D) {
+  return 1.3f * static_cast<float>(D / 16) * 0x1p-22f + 1e-6f;
+}
+__device__ __forceinline__ float tau_mean(int D) { return tau_cos(D) + 1e-6f; }
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* abort) {
   bool ok = *reinterpret_cast<volatile int32_t*>(abort) == 0 && wait_bar(bar, parity);
   ok = __all_sync(0xffffffffu, ok);
@@ -42,6 +47,44 @@ __device__ __forceinline__ Top2 top2_merge(Top2 a, Top2 b) {
   }
   return r;
 }
+// Order-preserving integer key of a float (smaller value -> smaller key,
+// -0 counts as +0) and its inverse: the top-2 reductions compare keys with
+// redux.sync.
+__device__ __forceinline__ uint32_t fkey(float v) {
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+// Warp-wide Top2 of (key, item) with item = lane + base: the minimum by
+// redux.sync, its lowest lane by ballot, the runner-up by a second redux
+// with that lane masked.  Every lane gets the result.
+struct KeyTop2 {
+  uint32_t k1;
+  int i1;
+  uint32_t k2;
+};
+__device__ __forceinline__ KeyTop2 warp_key_top2(uint32_t key, int base) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t k1 = __reduce_min_sync(0xffffffffu, key);
+  const int l1 = __ffs(__ballot_sync(0xffffffffu, key == k1)) - 1;
+  const uint32_t k2 = __reduce_min_sync(0xffffffffu, lane == l1 ? 0xffffffffu : key);
+  return KeyTop2{k1, base + l1, k2};
+}
+// Merge of per-warp KeyTop2 entries {k1, i1, k2, -} in any order: the
+// result is the top-2 of the union.
+__device__ __forceinline__ void key_top2_merge(uint64_t& best, uint32_t& second, uint4 e) {
+  const uint64_t c = (static_cast<uint64_t>(e.x) << 32) | e.y;
+  if (c < best) {
+    second = min(static_cast<uint32_t>(best >> 32), e.z);
+    best = c;
+  } else {
+    second = min(second, e.x);
+  }
+}
+
 // Warp-wide Top2 by xor shuffles (every lane gets the result).
 __device__ __forceinline__ Top2 warp_top2(Top2 t) {
 #pragma unroll
@@ -99,11 +142,39 @@ __device__ __forceinline__ double ff_value(FF a) {
   return static_cast<double>(a.hi) + static_cast<double>(a.lo);
 }
 
+// 1/sqrt(a) for a = a.hi + a.lo as an unevaluated pair, about 2^-46
+// relative, on the fp32 pipes (B300's fp64 square root and division are
+// slow): y0 = rsqrtf(a.hi), then one step of the series
+// (1 - t)^(-1/2) = 1 + t/2 + 3 t^2 / 8 + O(t^3) with t = 1 - a y0^2 formed
+// from exact products (TwoProd by fma); 1 - q below is exact (Sterbenz,
+// q within 2^-20 of 1).  Far-from-unit a is scaled by a power of two first.
+// a <= 0 gives 0.
+__device__ __forceinline__ FF ff_rsqrt(FF a) {
+  if (!(a.hi > 0.f)) return FF{0.f, 0.f};
+  float sc = 1.f;
+  if (a.hi < 0x1p-100f) {
+    a.hi *= 0x1p100f;
+    a.lo *= 0x1p100f;
+    sc = 0x1p50f;
+  } else if (a.hi > 0x1p100f) {
+    a.hi *= 0x1p-100f;
+    a.lo *= 0x1p-100f;
+    sc = 0x1p-50f;
+  }
+  const float y0 = rsqrtf(a.hi);
+  const float p = y0 * y0, pe = fmaf(y0, y0, -p);    // y0^2 = p + pe exactly
+  const float q = a.hi * p, qe = fmaf(a.hi, p, -q);  // a.hi p = q + qe exactly
+  const float t = (1.f - q) - (qe + fmaf(a.hi, pe, a.lo * p));
+  const float d = y0 * fmaf(0.375f * t, t, 0.5f * t);
+  const float rh = y0 + d;
+  return FF{rh * sc, (d - (rh - y0)) * sc};
+}
+
 // Exact-product dot product of rows a and b of X by one warp: lane l takes
 // the 16-byte pieces l, l + 32, ...; the partial pairs are merged by an
 // xor butterfly (TwoSum is exact in either operand order, so every lane ends
 // with the same value, and the result is symmetric in a and b).
-__device__ __forceinline__ double warp_dot_rows(const uint16_t* X, int D, int a, int b) {
+__device__ __forceinline__ FF warp_dot_rows_ff(const uint16_t* X, int D, int a, int b) {
   const int lane = threadIdx.x & 31;
   const uint4* ra = reinterpret_cast<const uint4*>(X + static_cast<size_t>(a) * D);
   const uint4* rb = reinterpret_cast<const uint4*>(X + static_cast<size_t>(b) * D);
@@ -114,7 +185,14 @@ __device__ __forceinline__ double warp_dot_rows(const uint16_t* X, int D, int a,
     FF other{__shfl_xor_sync(0xffffffffu, acc.hi, o), __shfl_xor_sync(0xffffffffu, acc.lo, o)};
     acc = ff_merge(acc, other);
   }
-  return ff_value(acc);
+  return acc;
+}
+__device__ __forceinline__ double warp_dot_rows(const uint16_t* X, int D, int a, int b) {
+  return ff_value(warp_dot_rows_ff(X, D, a, b));
+}
+// fp64 1/||x_a|| from the exact squared norm of row a (one warp).
+__device__ __forceinline__ double warp_rnorm(const uint16_t* X, int D, int a) {
+  return ff_value(ff_rsqrt(warp_dot_rows_ff(X, D, a, a)));
 }
 
 }  // namespace fps
