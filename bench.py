@@ -59,6 +59,7 @@ def parse():
 
 
 def peaks():
+    """HBM GB/s and dense bf16 TFLOP/s (burst) from MEASURED_PEAKS.json."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
@@ -233,10 +234,16 @@ class ClockSampler:
 # ------------------------------------------------------------------ ours
 
 
-def traffic_for(kernel_file, kernel):
+def workload_key(cfg):
+    """Name of a workload as run: its shape name, beacon count and unit count."""
+    return f"{cfg.name}:M{cfg.M}:U{cfg.U}"
+
+
+def traffic_for(kernel_file, kernel, wkey):
     """ncu DRAM bytes (read + write) per call recorded in
-    profiles/ncu_traffic.txt for this kernel's current source, else None.
-    Line format: <call> <sha256[:16] of its .cu file> <bytes per call> <workload>."""
+    profiles/ncu_traffic.txt for this kernel's current source on this
+    workload, else None.  Line format: <call> <sha256[:16] of its .cu file>
+    <bytes per call> <workload key>."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -244,7 +251,8 @@ def traffic_for(kernel_file, kernel):
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for line in open(p):
         f = line.split()
-        if len(f) >= 3 and not line.startswith("#") and f[0] == kernel and f[1] == h:
+        if (len(f) >= 4 and not line.startswith("#") and f[0] == kernel and f[1] == h
+                and f[3] == wkey):
             return float(f[2])
     return None
 
@@ -412,13 +420,27 @@ def run_ours(args, rank, world):
     }
     kfile = {"fps_update": "fps.cu", "score": "score.cu", "select_compact": "select_compact.cu"}
     launches = {"fps_update": 1, "score": 2, "select_compact": 1}
+    # scoring FLOPs: 2 N_q L d per unit (N_q = (W + M) G rows; the hi/lo
+    # split, the second pass and row padding are executed work, not counted)
+    score_flops = U * 2.0 * (cfg.W + M) * cfg.G * Lr * d
+    ridge = tfl * 1e12 / (hbm * 1e9)  # FLOP per byte where the two roofs meet
+    wkey = workload_key(cfg)
     roofs = {}
     for k, n in enumerate(names):
-        ach = alg[n] / (mean_ms[k] * 1e-3) / 1e9
-        roofs[n] = {"kernel": n, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                    "frac": ach / hbm, "peak_source": src, "ms": float(mean_ms[k]),
-                    "launches_per_call": launches[n], "traffic": traffic_for(kfile[n], n),
-                    "algorithmic_bytes_per_launch": alg[n]}
+        t = mean_ms[k] * 1e-3
+        common = {"kernel": n, "peak_source": src, "ms": float(mean_ms[k]),
+                  "launches_per_call": launches[n], "traffic": traffic_for(kfile[n], n, wkey),
+                  "algorithmic_bytes_per_launch": alg[n]}
+        if n == "score" and score_flops / alg[n] >= ridge:
+            ach = score_flops / t / 1e12
+            roofs[n] = {**common, "bound": "tensor", "achieved": ach, "peak": tfl,
+                        "unit": "TFLOP/s", "frac": ach / tfl, "peak_kind": "bf16 dense, burst",
+                        "algorithmic_flops_per_call": score_flops,
+                        "intensity_flop_per_byte": score_flops / alg[n], "ridge": ridge}
+        else:
+            ach = alg[n] / t / 1e9
+            roofs[n] = {**common, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                        "frac": ach / hbm}
     kv_bytes = U * (Lr * d * 2 + 2 * Lr * d * 2)  # K scored + K and V compacted (logical)
     rounds = world * args.steps / (total_ms * 1e-3)
     line = {
