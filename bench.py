@@ -239,6 +239,18 @@ def workload_key(cfg):
     return f"{cfg.name}:M{cfg.M}:U{cfg.U}"
 
 
+def kernel_source_sha(kernel_file):
+    """sha256[:16] over a kernel's .cu file and every shared header of the
+    library (a header change invalidates recorded counters too)."""
+    csrc = os.path.join(ROOT, "kv_cache_eviction_04_b300", "csrc")
+    h = hashlib.sha256(open(os.path.join(csrc, kernel_file), "rb").read())
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cuh", ".h")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "bkv.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def traffic_for(kernel_file, kernel, wkey):
     """ncu DRAM bytes (read + write) per call recorded in
     profiles/ncu_traffic.txt for this kernel's current source on this
@@ -247,8 +259,7 @@ def traffic_for(kernel_file, kernel, wkey):
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
-    src = os.path.join(ROOT, "kv_cache_eviction_04_b300", "csrc", kernel_file)
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = kernel_source_sha(kernel_file)
     for line in open(p):
         f = line.split()
         if (len(f) >= 4 and not line.startswith("#") and f[0] == kernel and f[1] == h
@@ -418,7 +429,8 @@ def run_ours(args, rank, world):
         "score": U * (Lr * d * 2 + Lr * 4 + Lr * 4 + (cfg.W + M) * D * 2),
         "select_compact": U * (Lr * 4 + B * 4) + n_moved * (2 * 2 * d * 2 + 2 * 4),
     }
-    kfile = {"fps_update": "fps.cu", "score": "score.cu", "select_compact": "select_compact.cu"}
+    kfile = {"fps_update": "fps_cluster.cu" if cfg.C > 256 else "fps.cu", "score": "score.cu",
+             "select_compact": "select_compact.cu"}
     launches = {"fps_update": 1, "score": 2, "select_compact": 1}
     # scoring FLOPs: 2 N_q L d per unit (N_q = (W + M) G rows; the hi/lo
     # split, the second pass and row padding are executed work, not counted)
