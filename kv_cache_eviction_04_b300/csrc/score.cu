@@ -94,11 +94,48 @@ __device__ __forceinline__ int row_position(const ScoreParams& p, int u, int r, 
 // Build the rotated, scaled, hi/lo-split query operand for rows
 // [row0, row0 + nrows) in two K-major 128B-swizzled smem images.  Run by
 // `nthr` threads with ids tid in [0, nthr); ends with named barrier `bar`.
+// Loads the query rows of items idx0, idx0 + nthr, ... (kBatch of them) of
+// build_queries: item = (row, group of 8 rotary pairs).  Rows past the
+// recent and beacon slots load nothing (zeros).
+template <int D, int kBatch>
+__device__ __forceinline__ void load_query_batch(const ScoreParams& p, int u, int row0, int total,
+                                                 int idx0, int nthr, uint4 (&va)[kBatch],
+                                                 uint4 (&vb)[kBatch]) {
+  constexpr int H = D / 2;
+  constexpr int kGroups = H / 8;
+#pragma unroll
+  for (int t = 0; t < kBatch; ++t) {
+    const int idx = idx0 + t * nthr;
+    va[t] = vb[t] = make_uint4(0u, 0u, 0u, 0u);
+    if (idx < total) {
+      const int rr = row0 + idx / kGroups, grp = idx % kGroups;
+      const int item = rr / p.G, g = rr % p.G;
+      if (item < p.W + p.M) {
+        const uint16_t* src =
+            item < p.W ? p.recent_q + ((static_cast<size_t>(u) * p.W + item) * p.G + g) * D
+                       : p.beacons + ((static_cast<size_t>(u) * p.M + (item - p.W)) * p.G + g) * D;
+        va[t] = *reinterpret_cast<const uint4*>(src + grp * 8);
+        vb[t] = *reinterpret_cast<const uint4*>(src + H + grp * 8);
+      }
+    }
+  }
+}
+
 template <int D>
 __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, uint8_t* q_hi,
                               uint8_t* q_lo, int32_t* row_pos, float2* cs, int tid, int nthr,
                               int bar) {
   constexpr int H = D / 2;
+  // one thread per (row, pair of 8 consecutive rotary pairs), four items at
+  // a time: all of a batch's global loads are issued before any is used.
+  // The first batch is loaded before anything else that waits on global
+  // memory; rows without an item (no beacon there) are loaded where the
+  // memory exists and zeroed below.
+  constexpr int kGroups = H / 8;
+  constexpr int kBatch = 4;
+  const int total = nrows * kGroups;
+  uint4 va[kBatch], vb[kBatch];
+  load_query_batch<D, kBatch>(p, u, row0, total, tid, nthr, va, vb);
   const int32_t cur = p.cur_pos[u];
   const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
   const int nage = max(p.W, 1);
@@ -112,31 +149,8 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
   }
   for (int r = tid; r < nrows; r += nthr) row_pos[r] = row_position(p, u, row0 + r, nb, cur);
   named_sync(bar, nthr);
-  // one thread per (row, pair of 8 consecutive rotary pairs), four items at
-  // a time: all of a batch's global loads are issued before any is used
-  constexpr int kGroups = H / 8;
-  constexpr int kBatch = 4;
-  const int total = nrows * kGroups;
   for (int idx0 = tid; idx0 < total; idx0 += kBatch * nthr) {
-    uint4 va[kBatch], vb[kBatch];
-#pragma unroll
-    for (int t = 0; t < kBatch; ++t) {
-      const int idx = idx0 + t * nthr;
-      va[t] = vb[t] = make_uint4(0u, 0u, 0u, 0u);
-      if (idx < total) {
-        const int r = idx / kGroups, grp = idx % kGroups;
-        const int rr = row0 + r;
-        if (row_pos[r] != INT32_MIN) {
-          const int item = rr / p.G, g = rr % p.G;
-          const uint16_t* src =
-              item < p.W
-                  ? p.recent_q + ((static_cast<size_t>(u) * p.W + item) * p.G + g) * D
-                  : p.beacons + ((static_cast<size_t>(u) * p.M + (item - p.W)) * p.G + g) * D;
-          va[t] = *reinterpret_cast<const uint4*>(src + grp * 8);
-          vb[t] = *reinterpret_cast<const uint4*>(src + H + grp * 8);
-        }
-      }
-    }
+    if (idx0 != tid) load_query_batch<D, kBatch>(p, u, row0, total, idx0, nthr, va, vb);
 #pragma unroll
     for (int t = 0; t < kBatch; ++t) {
       const int idx = idx0 + t * nthr;
@@ -180,16 +194,28 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
   named_sync(bar, nthr);
 }
 
-struct __align__(8) Barriers {
+// Shared-memory arrays read with 16-byte vector loads follow this struct,
+// so its size is a multiple of 16.
+struct __align__(16) Barriers {
   uint64_t full[8];
   uint64_t empty[8];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t tmax_ready;  // fused kernel: the per-tile key-position maxima are in place
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t minpos;
-  int32_t pad;
+  int32_t minrow;       // fused kernel: smallest key-position limit over the rows
 };
+
+static_assert(sizeof(Barriers) % 16 == 0, "arrays after the barriers need 16-byte alignment");
+
+// The fused kernel keeps the largest key position of each of the first
+// kTmaxTiles tiles in shared memory: a tile whose largest position is within
+// every row's limit needs no causal mask and no per-key positions.
+constexpr int kTmaxTiles = 512;
+// Tiles pulled into L2 ahead of the TMA loads (iterations of both passes).
+constexpr int kPrefetchAhead = 8;
 
 // Key tile range of split `s` for unit u.
 __device__ __forceinline__ void split_tiles(const ScoreParams& p, int u, int s, int& t0, int& t1,
@@ -581,7 +607,7 @@ template <int D, int NR, uint32_t kBufCols, bool kMax>
 __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int nt, int L,
                                                uint32_t tbase, Barriers* bars, int32_t* row_pos,
                                                float* lse, float2* mz, float* part,
-                                               int32_t* kp) {
+                                               int32_t* kp, const int32_t* tmax) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;           // TMEM lane quarter
   const int h = (warp - 2) >> 2;    // 0: warps 2..5, 1: warps 6..9
@@ -593,32 +619,39 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
   // every tile; running max and sum of exp2 (four partial sums per chunk)
   float m[NR], z[NR];
   int32_t lim[NR];
+  int32_t lmin = INT32_MAX;  // smallest limit over this thread's live rows
 #pragma unroll
   for (int blk = 0; blk < NR; ++blk) {
     const int32_t rp = row_pos[blk * 128 + q * 32 + lane];
     lim[blk] = (p.causal || rp == INT32_MIN) ? rp : INT32_MAX - 1;
+    if (rp != INT32_MIN) lmin = min(lmin, lim[blk]);
     m[blk] = -INFINITY;
     z[blk] = 0.f;
   }
-  // Key positions two tiles ahead (registers), stored per tile into one of
-  // two shared buffers with the largest position of each 32-key chunk (the
-  // barrier of tile i + 1 keeps tile i + 2 from rewriting tile i's).  A warp
-  // whose rows all see every key of a chunk skips the per-key mask.
-  int32_t kp_n1 = (et < 128 && et < L) ? kpu[et] : INT32_MAX;
-  int32_t kp_n2 = (et < 128 && nt > 1 && kTileKeys + et < L) ? kpu[kTileKeys + et] : INT32_MAX;
-  int32_t* kpmax = kp + 256;  // [2][4]
+  lmin = __reduce_min_sync(0xffffffffu, lmin);
+  if (lane == 0) atomicMin(&bars->minrow, lmin);
+  warp_wait(&bars->tmax_ready, 0, &bars->abort_flag);
+  named_sync(2, kFusedEpi);
+  const int32_t minrow = bars->minrow;
+  // A tile whose largest key position is within every live row's limit (and
+  // that has no key past L) needs no mask.  Other tiles stage their key
+  // positions and the largest of each 32-key chunk in shared memory, between
+  // two barriers of the epilogue warps.
+  int32_t* kpmax = kp + 256;  // [4]
   for (int i = 0; i < nt; ++i) {
     const int b = i & 1;
-    int32_t* kpb = kp + (i & 1) * 128;
-    if (et < 128) {
-      kpb[et] = kp_n1;
-      const int32_t cm = __reduce_max_sync(0xffffffffu, kp_n1);
-      if (lane == 0) kpmax[(i & 1) * 4 + (et >> 5)] = cm;
-      kp_n1 = kp_n2;
-      const int jn = (i + 2) * kTileKeys + et;
-      kp_n2 = (i + 2 < nt && jn < L) ? kpu[jn] : INT32_MAX;
+    const bool masked = !(i < kTmaxTiles && tmax[i] <= minrow);  // uniform
+    if (masked) {
+      named_sync(2, kFusedEpi);  // every warp is done with the previous staged tile
+      if (et < 128) {
+        const int j = i * kTileKeys + et;
+        const int32_t kv = j < L ? kpu[j] : INT32_MAX;
+        kp[et] = kv;
+        const int32_t cm = __reduce_max_sync(0xffffffffu, kv);
+        if (lane == 0) kpmax[et >> 5] = cm;
+      }
+      named_sync(2, kFusedEpi);
     }
-    named_sync(2, kFusedEpi);
     if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
       tc_fence_after();
 #pragma unroll
@@ -634,11 +667,11 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
           if (lane == 0) mbar_arrive(&bars->tempty[b]);
         }
         const int lm = lim[blk];
-        const bool open = __all_sync(0xffffffffu, kpmax[(i & 1) * 4 + 2 * h] <= lm &&
-                                                      kpmax[(i & 1) * 4 + 2 * h + 1] <= lm);
+        const bool open =
+            !masked || __all_sync(0xffffffffu, kpmax[2 * h] <= lm && kpmax[2 * h + 1] <= lm);
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
         if (!open) {
-          const int* kh = kpb + 64 * h;
+          const int* kh = kp + 64 * h;
 #pragma unroll
           for (int k = 0; k < 64; ++k)
             if (kh[k] > lm) v[k] = __float_as_uint(-INFINITY);
@@ -710,23 +743,19 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
   const int c_begin = h ? nch0 : 0, c_end = h ? nchunks : nch0;
   constexpr bool is_max = kMax;
   const int key = q * 32 + lane;
-  // this key's position, fetched two tiles ahead
-  int32_t kp_a1 = (nt > 0 && key < L) ? kpu[key] : INT32_MAX;
-  int32_t kp_a2 = (nt > 1 && kTileKeys + key < L) ? kpu[kTileKeys + key] : INT32_MAX;
   for (int i = nt; i < 2 * nt; ++i) {
     const int b = i & 1;
-    const int j = (i - nt) * kTileKeys + key;
-    const int32_t kpj = kp_a1;
-    kp_a1 = kp_a2;
-    {
-      const int jn = j + 2 * kTileKeys;
-      kp_a2 = (i + 2 < 2 * nt && jn < L) ? kpu[jn] : INT32_MAX;
-    }
+    const int ti = i - nt;
+    const int j = ti * kTileKeys + key;
+    // a tile whose largest key position is at most every row's position
+    // (and that has no key past L) needs no mask and no per-key position
+    const bool tile_open = ti < kTmaxTiles && tmax[ti] <= minpos;
+    const int32_t kpj = tile_open ? INT32_MIN : (j < L ? kpu[j] : INT32_MAX);
     float r0 = -INFINITY, r1 = -INFINITY, r2 = -INFINITY, r3 = -INFINITY;  // max
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;                          // mean
     if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
       tc_fence_after();
-      const bool nomask = __all_sync(0xffffffffu, kpj <= minpos);
+      const bool nomask = tile_open || __all_sync(0xffffffffu, kpj <= minpos);
       if (c_begin == c_end) {
         tc_fence_before();
         __syncwarp();
@@ -749,32 +778,33 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
         const int nv = min(two ? 64 : 32, N - c * 32);  // valid rows here (multiple of 16)
         const float4* l4 = reinterpret_cast<const float4*>(lse + c * 32);
         const int4* p4 = reinterpret_cast<const int4*>(row_pos + c * 32);
+        // No branch per group of four rows: rows past nv read whatever lies
+        // past them in shared memory (lse and row_pos are followed by other
+        // arrays of the kernel) and are discarded by the selects.
+        const int32_t kpm = nomask ? INT32_MIN : kpj;
 #pragma unroll
         for (int k4 = 0; k4 < 16; ++k4) {
-          if (k4 * 4 < nv) {
-            const float4 lv = l4[k4];
-            float x0 = __uint_as_float(v[k4 * 4 + 0]) - lv.x;
-            float x1 = __uint_as_float(v[k4 * 4 + 1]) - lv.y;
-            float x2 = __uint_as_float(v[k4 * 4 + 2]) - lv.z;
-            float x3 = __uint_as_float(v[k4 * 4 + 3]) - lv.w;
-            if (!nomask) {
-              const int4 pv = p4[k4];
-              if (kpj > pv.x) x0 = -INFINITY;
-              if (kpj > pv.y) x1 = -INFINITY;
-              if (kpj > pv.z) x2 = -INFINITY;
-              if (kpj > pv.w) x3 = -INFINITY;
-            }
-            if constexpr (is_max) {
-              r0 = fmaxf(r0, x0);
-              r1 = fmaxf(r1, x1);
-              r2 = fmaxf(r2, x2);
-              r3 = fmaxf(r3, x3);
-            } else {
-              s0 += ex2(x0);
-              s1 += ex2(x1);
-              s2 += ex2(x2);
-              s3 += ex2(x3);
-            }
+          const bool ok = k4 * 4 < nv;
+          const float4 lv = l4[k4];
+          const int4 pv = p4[k4];
+          float x0 = __uint_as_float(v[k4 * 4 + 0]) - lv.x;
+          float x1 = __uint_as_float(v[k4 * 4 + 1]) - lv.y;
+          float x2 = __uint_as_float(v[k4 * 4 + 2]) - lv.z;
+          float x3 = __uint_as_float(v[k4 * 4 + 3]) - lv.w;
+          x0 = (ok && kpm <= pv.x) ? x0 : -INFINITY;
+          x1 = (ok && kpm <= pv.y) ? x1 : -INFINITY;
+          x2 = (ok && kpm <= pv.z) ? x2 : -INFINITY;
+          x3 = (ok && kpm <= pv.w) ? x3 : -INFINITY;
+          if constexpr (is_max) {
+            r0 = fmaxf(r0, x0);
+            r1 = fmaxf(r1, x1);
+            r2 = fmaxf(r2, x2);
+            r3 = fmaxf(r3, x3);
+          } else {
+            s0 += ex2(x0);
+            s1 += ex2(x1);
+            s2 += ex2(x2);
+            s3 += ex2(x3);
           }
         }
       }
@@ -816,6 +846,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   float* part = reinterpret_cast<float*>(mz + kRows);         // [2][128] second half's maxima
   int32_t* kp = reinterpret_cast<int32_t*>(part + 256);       // [2][128] pass-1 key positions + [2][4] chunk maxima
   float2* cs = reinterpret_cast<float2*>(kp + 264);           // [max(W,1)][D/2]
+  int32_t* tmax = reinterpret_cast<int32_t*>(cs + (p.W > 0 ? p.W : 1) * (D / 2));  // [kTmaxTiles]
 
   const int u = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -832,8 +863,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       mbar_init(&bars->tfull[i], 1);
       mbar_init(&bars->tempty[i], 8);  // one arrival per epilogue warp
     }
+    mbar_init(&bars->tmax_ready, 1);
     bars->abort_flag = 0;
     bars->minpos = INT32_MAX;
+    bars->minrow = INT32_MAX;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -846,10 +879,71 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const uint32_t tbase = bars->tmem_base;
 
   if (warp == 0) {
-    if (elect_one()) {
-      // ---------------- TMA producer: every tile twice (pass 1, then pass 2)
-      prefetch_tmap(&kmap);
-      for (int i = 0; i < 2 * nt; ++i) {
+    // ---------------- TMA producer: every tile twice (pass 1, then pass 2).
+    // Iteration i loads tile i % nt; iteration i + kPrefetchAhead is pulled
+    // into L2 when iteration i is loaded, so HBM latency is covered beyond
+    // the NS stages of shared memory.
+    const int niter = 2 * nt;
+    auto issue = [&](int i) {  // stage i % NS is free
+      const int st = i % NS;
+      mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
+      const int j0 = (i % nt) * kTileKeys;
+#pragma unroll
+      for (int a = 0; a < D / 64; ++a)
+        tma_load_3d(stages + st * kStageBytes + a * 16384, &kmap, &bars->full[st], 64 * a, j0, u);
+    };
+    auto prefetch = [&](int i) {
+      if (i < niter)
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a) tma_prefetch_l2_3d(&kmap, 64 * a, (i % nt) * kTileKeys, u);
+    };
+    const int first = min(NS, niter);
+    if (lane == 0) prefetch_tmap(&kmap);
+    // Largest key position of every tile (keys past L count as unbounded),
+    // while the first tiles load.  Lane l reads keys 4l .. 4l + 3 of a tile
+    // with one 16-byte load (the address clamped into the row; clamped
+    // loads only cover keys past L), so sixteen tiles' loads are in flight
+    // before any is reduced.  Rows that are not 16-byte aligned take
+    // element loads.
+    {
+      const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
+      const bool vec = (reinterpret_cast<uintptr_t>(p.kpos) & 15u) == 0 && (p.L_cap & 3) == 0 &&
+                       p.L_cap >= 4;
+      const int ntm = min(nt, kTmaxTiles);
+      for (int t0 = 0; t0 < ntm; t0 += 16) {
+        int32_t mx[16];
+        if (vec) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int j = (t0 + k) * kTileKeys + 4 * lane;
+            const int4 v = *reinterpret_cast<const int4*>(kpu + min(j, p.L_cap - 4));
+            mx[k] = max(max(j < L ? v.x : INT32_MAX, j + 1 < L ? v.y : INT32_MAX),
+                        max(j + 2 < L ? v.z : INT32_MAX, j + 3 < L ? v.w : INT32_MAX));
+          }
+        } else {
+#pragma unroll 1
+          for (int k = 0; k < 16; ++k) {
+            const int j = (t0 + k) * kTileKeys + 4 * lane;
+            int32_t m = INT32_MIN;
+            for (int e = 0; e < 4; ++e) m = max(m, j + e < L ? kpu[j + e] : INT32_MAX);
+            mx[k] = m;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int32_t r = __reduce_max_sync(0xffffffffu, mx[k]);
+          if (lane == 0 && t0 + k < ntm) tmax[t0 + k] = r;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tmax_ready);
+    }
+    // The small loads above and the query build's go first; the first tiles
+    // and the L2 run-ahead follow (the run-ahead starts once the pipeline
+    // turns, after the first tile's MMAs).
+    if (lane == 0) {
+      for (int i = 0; i < first; ++i) issue(i);
+      for (int i = first; i < niter; ++i) {
         const int st = i % NS;
         if (*reinterpret_cast<volatile int32_t*>(&bars->abort_flag) != 0 ||
             !wait_bar(&bars->empty[st], ((i / NS) & 1) ^ 1)) {
@@ -857,14 +951,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
           break;
         }
-        mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
-        const int j0 = (i % nt) * kTileKeys;
-#pragma unroll
-        for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(stages + st * kStageBytes + a * 16384, &kmap, &bars->full[st], 64 * a, j0,
-                      u);
+        issue(i);
+        if (i == first)
+          for (int k = 1; k <= kPrefetchAhead; ++k) prefetch(i + k);
+        else
+          prefetch(i + kPrefetchAhead);
       }
     }
+    __syncwarp();
   } else {
     build_queries<D>(p, u, 0, kRows, q_hi, q_lo, row_pos, cs, threadIdx.x - 32,
                      kFusedThreads - 32, 1);
@@ -919,10 +1013,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     } else {
       if (p.agg == BKV_AGG_MAX)
         fused_epilogue<D, NR, kBufCols, true>(p, u, nt, L, tbase, bars, row_pos, lse, mz, part,
-                                              kp);
+                                              kp, tmax);
       else
         fused_epilogue<D, NR, kBufCols, false>(p, u, nt, L, tbase, bars, row_pos, lse, mz, part,
-                                               kp);
+                                               kp, tmax);
     }
   }
   tc_fence_before();
@@ -935,7 +1029,7 @@ template <int D, int NS, int NR>
 size_t fused_smem(int W) {
   return 1024 + 2 * static_cast<size_t>(NR) * 128 * D * 2 + NS * kTileKeys * D * 2 +
          sizeof(Barriers) + NR * 128 * (4 + 4 + 8) + 256 * 4 + 264 * 4 +
-         static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
+         static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8 + kTmaxTiles * 4;
 }
 
 template <int D, int NS>
