@@ -592,13 +592,56 @@ __global__ void __launch_bounds__(kThreads, 1)
 // still in L2).  NR = 128-row blocks of the query image (1 or 2).
 //
 // Ten warps: warp 0 issues TMA, warp 1 issues MMAs, warps 2..9 are the
-// epilogue, two per TMEM lane quarter (warps w and w + 4 share quarter
-// w & 3): in pass 1 they split each tile's keys (each keeps its own running
-// max and sum of exp2 per row, merged once at the end of the pass), in pass
-// 2 they split the rows (partial maxima merged per tile through shared
-// memory), so every SM sub-partition has two epilogue warps to interleave.
+// epilogue.  The two TMEM accumulators alternate between tiles, and each
+// half of the epilogue (warps 2..5 and 6..9, one warp per TMEM lane quarter
+// and per SM sub-partition) owns one of them: half h takes the tiles
+// i with i % 2 == h, whole.  Two tiles are in the epilogue at once and no
+// tile needs a barrier across the halves.  In pass 1 a thread keeps the
+// running max and sum of exp2 of its row over its half's tiles (the halves
+// are merged once at the end); in pass 2 a thread reduces its key over all
+// rows and writes its score.
 constexpr int kFusedThreads = 320;
 constexpr int kFusedEpi = 256;
+
+// Arrival of one of the four warps of a half on a TMEM-empty barrier that
+// counts eight: each warp stands for two.
+__device__ __forceinline__ void arrive_tempty(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], 2;" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier of one half of the epilogue (named barriers 3 and 4, 128 threads).
+__device__ __forceinline__ void half_sync(int h) {
+  if (h == 0)
+    named_sync(3, 128);
+  else
+    named_sync(4, 128);
+}
+
+// Running max and sum of exp2 of one row over 64 keys (TMEM words).
+__device__ __forceinline__ void row_update(float& m, float& z, const uint32_t (&v)[64]) {
+  float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 64; k += 4) {
+    mx0 = fmaxf(mx0, __uint_as_float(v[k]));
+    mx1 = fmaxf(mx1, __uint_as_float(v[k + 1]));
+    mx2 = fmaxf(mx2, __uint_as_float(v[k + 2]));
+    mx3 = fmaxf(mx3, __uint_as_float(v[k + 3]));
+  }
+  const float mn = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+  if (mn != -INFINITY) {
+    float a0 = (m == -INFINITY) ? 0.f : z * ex2(m - mn);
+    float a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 64; k += 4) {
+      a0 += ex2(__uint_as_float(v[k]) - mn);
+      a1 += ex2(__uint_as_float(v[k + 1]) - mn);
+      a2 += ex2(__uint_as_float(v[k + 2]) - mn);
+      a3 += ex2(__uint_as_float(v[k + 3]) - mn);
+    }
+    z = (a0 + a1) + (a2 + a3);
+    m = mn;
+  }
+}
 
 // Epilogue of the fused kernel (warps 2..9; thread et = threadIdx.x - 64).
 // kMax: max aggregation (else the mean), a template parameter so that the
@@ -609,14 +652,17 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
                                                float* lse, float2* mz, float* part,
                                                int32_t* kp, const int32_t* tmax) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q = warp & 3;           // TMEM lane quarter
-  const int h = (warp - 2) >> 2;    // 0: warps 2..5, 1: warps 6..9
-  const int et = threadIdx.x - 64;  // 0..255
+  const int q = warp & 3;                      // TMEM lane quarter
+  const int h = (warp - 2) >> 2;               // half: 0 = warps 2..5, 1 = warps 6..9
+  const int ht = (threadIdx.x - 64) & 127;     // thread within the half
   const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+  const uint32_t buf = tbase + lane_addr + h * kBufCols;  // this half's accumulator
   const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
+  int32_t* kph = kp + h * 128;                 // this half's staged key positions
+  (void)part;
 
-  // ---- pass 1: thread = row (of each row block), keys [64 h, 64 h + 64) of
-  // every tile; running max and sum of exp2 (four partial sums per chunk)
+  // ---- pass 1: thread = row (of each row block) over all keys of its
+  // half's tiles; running max and sum of exp2
   float m[NR], z[NR];
   int32_t lim[NR];
   int32_t lmin = INT32_MAX;  // smallest limit over this thread's live rows
@@ -634,70 +680,41 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
   named_sync(2, kFusedEpi);
   const int32_t minrow = bars->minrow;
   // A tile whose largest key position is within every live row's limit (and
-  // that has no key past L) needs no mask.  Other tiles stage their key
-  // positions and the largest of each 32-key chunk in shared memory, between
-  // two barriers of the epilogue warps.
-  int32_t* kpmax = kp + 256;  // [4]
-  for (int i = 0; i < nt; ++i) {
-    const int b = i & 1;
+  // that has no key past L) needs no mask; for another tile the half stages
+  // its key positions in shared memory between two barriers of the half.
+  for (int i = h; i < nt; i += 2) {
     const bool masked = !(i < kTmaxTiles && tmax[i] <= minrow);  // uniform
     if (masked) {
-      named_sync(2, kFusedEpi);  // every warp is done with the previous staged tile
-      if (et < 128) {
-        const int j = i * kTileKeys + et;
-        const int32_t kv = j < L ? kpu[j] : INT32_MAX;
-        kp[et] = kv;
-        const int32_t cm = __reduce_max_sync(0xffffffffu, kv);
-        if (lane == 0) kpmax[et >> 5] = cm;
-      }
-      named_sync(2, kFusedEpi);
+      half_sync(h);  // the half is done with its previous staged tile
+      const int j = i * kTileKeys + ht;
+      kph[ht] = j < L ? kpu[j] : INT32_MAX;
+      half_sync(h);
     }
-    if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
+    if (warp_wait(&bars->tfull[h], (i >> 1) & 1, &bars->abort_flag)) {
       tc_fence_after();
 #pragma unroll
-      for (int blk = 0; blk < NR; ++blk) {
-        uint32_t v[64];  // this thread's keys 64 h .. 64 h + 63 of the tile
-        const uint32_t col = tbase + lane_addr + b * kBufCols + blk * 128 + h * 64;
-        tmem_ld32(col, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld32(col + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        tmem_wait_ld();
-        if (blk == NR - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->tempty[b]);
-        }
-        const int lm = lim[blk];
-        const bool open =
-            !masked || __all_sync(0xffffffffu, kpmax[2 * h] <= lm && kpmax[2 * h + 1] <= lm);
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-        if (!open) {
-          const int* kh = kp + 64 * h;
+      for (int blk = 0; blk < NR; ++blk)
 #pragma unroll
-          for (int k = 0; k < 64; ++k)
-            if (kh[k] > lm) v[k] = __float_as_uint(-INFINITY);
-        }
-#pragma unroll
-        for (int k = 0; k < 64; k += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(v[k]));
-          mx1 = fmaxf(mx1, __uint_as_float(v[k + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(v[k + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(v[k + 3]));
-        }
-        const float mn = fmaxf(m[blk], fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
-        if (mn != -INFINITY) {
-          float a0 = (m[blk] == -INFINITY) ? 0.f : z[blk] * ex2(m[blk] - mn);
-          float a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-          for (int k = 0; k < 64; k += 4) {
-            a0 += ex2(__uint_as_float(v[k]) - mn);
-            a1 += ex2(__uint_as_float(v[k + 1]) - mn);
-            a2 += ex2(__uint_as_float(v[k + 2]) - mn);
-            a3 += ex2(__uint_as_float(v[k + 3]) - mn);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[64];  // keys 64 c .. 64 c + 63 of the tile
+          const uint32_t col = buf + blk * 128 + c * 64;
+          tmem_ld32(col, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(col + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_wait_ld();
+          if (blk == NR - 1 && c == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive_tempty(&bars->tempty[h]);
           }
-          z[blk] = (a0 + a1) + (a2 + a3);
-          m[blk] = mn;
+          if (masked) {
+            const int lm = lim[blk];
+            const int* kh = kph + 64 * c;
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+              v[k] = kh[k] > lm ? __float_as_uint(-INFINITY) : v[k];
+          }
+          row_update(m[blk], z[blk], v);
         }
-      }
     } else if (lane == 0) {
       record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
     }
@@ -731,20 +748,19 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
   }
   named_sync(2, kFusedEpi);
 
-  // ---- pass 2: thread = key q * 32 + lane, rows of half h; max (or mean)
-  // over rows of exp2(s - lse), the halves merged per tile
+  // ---- pass 2: thread = key q * 32 + lane of its half's tiles, over every
+  // row; max (or mean) of exp2(s - lse), written directly
   const int32_t minpos = bars->minpos;
   const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
   const int nrec = p.step + 1 < p.W ? static_cast<int>(p.step + 1) : p.W;
   const float inv_rows = 1.f / static_cast<float>(max((nrec + nb) * p.G, 1));
   const int N = p.NQ16;
   const int nchunks = (N + 31) / 32;
-  const int nch0 = (nchunks + 1) / 2;
-  const int c_begin = h ? nch0 : 0, c_end = h ? nchunks : nch0;
   constexpr bool is_max = kMax;
   const int key = q * 32 + lane;
-  for (int i = nt; i < 2 * nt; ++i) {
-    const int b = i & 1;
+  // the first pass-2 iteration of this half (iterations nt .. 2 nt - 1)
+  const int i0 = nt + ((h - nt) & 1);
+  for (int i = i0; i < 2 * nt; i += 2) {
     const int ti = i - nt;
     const int j = ti * kTileKeys + key;
     // a tile whose largest key position is at most every row's position
@@ -753,27 +769,23 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
     const int32_t kpj = tile_open ? INT32_MIN : (j < L ? kpu[j] : INT32_MAX);
     float r0 = -INFINITY, r1 = -INFINITY, r2 = -INFINITY, r3 = -INFINITY;  // max
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;                          // mean
-    if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
+    if (warp_wait(&bars->tfull[h], (i >> 1) & 1, &bars->abort_flag)) {
       tc_fence_after();
       const bool nomask = tile_open || __all_sync(0xffffffffu, kpj <= minpos);
-      if (c_begin == c_end) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->tempty[b]);
-      }
-      // chunks in pairs: both TMEM loads issued before one wait
+      const int32_t kpm = nomask ? INT32_MIN : kpj;
+      // chunks of 32 rows in pairs: both TMEM loads issued before one wait
 #pragma unroll 1
-      for (int c = c_begin; c < c_end; c += 2) {
-        const bool two = c + 1 < c_end;
+      for (int c = 0; c < nchunks; c += 2) {
+        const bool two = c + 1 < nchunks;
         uint32_t v[64];
-        const uint32_t col = tbase + lane_addr + b * kBufCols + c * 32;
+        const uint32_t col = buf + c * 32;
         tmem_ld32(col, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         if (two) tmem_ld32(col + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         tmem_wait_ld();
-        if (c + 2 >= c_end) {
+        if (c + 2 >= nchunks) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->tempty[b]);
+          if (lane == 0) arrive_tempty(&bars->tempty[h]);
         }
         const int nv = min(two ? 64 : 32, N - c * 32);  // valid rows here (multiple of 16)
         const float4* l4 = reinterpret_cast<const float4*>(lse + c * 32);
@@ -781,7 +793,6 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
         // No branch per group of four rows: rows past nv read whatever lies
         // past them in shared memory (lse and row_pos are followed by other
         // arrays of the kernel) and are discarded by the selects.
-        const int32_t kpm = nomask ? INT32_MIN : kpj;
 #pragma unroll
         for (int k4 = 0; k4 < 16; ++k4) {
           const bool ok = k4 * 4 < nv;
@@ -811,14 +822,10 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
     } else if (lane == 0) {
       record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
     }
-    const float mine = is_max ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : (s0 + s1) + (s2 + s3);
-    float* pb = part + (i & 1) * 128;
-    if (h == 1) pb[key] = mine;
-    named_sync(3, kFusedEpi);
-    if (h == 0 && j < L) {
-      const float both = is_max ? fmaxf(mine, pb[key]) : mine + pb[key];
+    if (j < L) {
+      const float all = is_max ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : (s0 + s1) + (s2 + s3);
       p.scores[static_cast<size_t>(u) * p.L_cap + j] =
-          is_max ? (both == -INFINITY ? 0.f : ex2(both)) : both * inv_rows;
+          is_max ? (all == -INFINITY ? 0.f : ex2(all)) : all * inv_rows;
     }
   }
 }
