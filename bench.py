@@ -2,14 +2,16 @@
 
 One step = one eviction round over every unit: FPS beacon selection over
 the continual buffer (C - 1 items), eviction scoring, top-B_KV selection and
-in-place K/V compaction -- the calls bkv_fps_update (no append),
-bkv_score and bkv_select_compact of libbkv.  The workload is the Qwen3-4B-shaped
+in-place K/V compaction -- one bkv_round call of libbkv (bkv_fps_update with
+no append, bkv_score and bkv_select_compact in one call).  The workload is the Qwen3-4B-shaped
 one-layer round: 14 sequences x 8 KV heads (GQA 4), d = 128, cache length
 2176 -> B_KV 2048, W = 16 recent queries, M = 16 beacons, buffer C = 256.
 
 Before every timed step the cache state is restored from a pristine device
 copy and L2 is flushed by writing a 256 MiB buffer; each step is timed with
-CUDA events on the launching stream around the three calls only.
+CUDA events on the launching stream around the round call only.  Each
+call's own time (for the rooflines) comes from further steps made as three
+calls with events between them.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own units (weak scaling, no collective on
@@ -92,7 +94,7 @@ def workload_desc(cfg, world):
         "units_per_gpu": cfg.U, "global_units": cfg.U * world,
         "parallelism": f"units sharded over {world} GPU(s)",
         "l2": "flushed (256 MiB write) and state restored before every timed step",
-        "step": "fps_update(beacon select over C-1 items) + score + select_compact",
+        "step": "bkv_round: fps_update (beacon select over C-1 items) + score + select_compact",
     }
 
 
@@ -321,21 +323,32 @@ def run_ours(args, rank, world):
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
 
-    def one_step(timed):
+    def one_step(timed, per_call=False):
+        # A step is one round through bkv_round, timed whole (events before
+        # and after): its kernels overlap their launch and set-up with the
+        # previous kernel's tail (programmatic dependent launch).  per_call
+        # makes the three calls separately with events between them, which
+        # gives each call's own time, for the rooflines.
         restore()
         ev[0].record(stream)
-        bkv.fps_update(dims, None, step, work["ring"], work["buf"], work["cnt"], True, bidx,
-                       beac, nb, ws, stream)
-        ev[1].record(stream)
-        bkv.score(dims, work["K"], work["L"], work["kpos"], work["ring"], step, beac, nb, cur,
-                  scores, ws, stream)
-        ev[2].record(stream)
-        bkv.select_compact(dims, scores, work["K"], work["V"], work["kpos"], work["L"], kept, ws,
-                           stream)
+        if per_call:
+            bkv.fps_update(dims, None, step, work["ring"], work["buf"], work["cnt"], True, bidx,
+                           beac, nb, ws, stream)
+            ev[1].record(stream)
+            bkv.score(dims, work["K"], work["L"], work["kpos"], work["ring"], step, beac, nb, cur,
+                      scores, ws, stream)
+            ev[2].record(stream)
+            bkv.select_compact(dims, scores, work["K"], work["V"], work["kpos"], work["L"], kept,
+                               ws, stream)
+        else:
+            bkv.round(dims, None, step, work["ring"], work["buf"], work["cnt"], bidx, beac, nb,
+                      work["K"], work["V"], work["L"], work["kpos"], cur, scores, kept, ws, stream)
         ev[3].record(stream)
         if timed:
             ev[3].synchronize()
-            return [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+            if per_call:
+                return [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+            return ev[0].elapsed_time(ev[3])
         return None
 
     for _ in range(max(args.warmup, 3)):
@@ -353,16 +366,17 @@ def run_ours(args, rank, world):
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    per = []
+    step_ms = []
     for _ in range(args.steps):
-        per.append(one_step(True))
+        step_ms.append(one_step(True))
     torch.cuda.synchronize()
     clk = clocks.stop()
     status = bkv.get_status(ws, stream)
     if status != 0:
         raise RuntimeError(f"device status {status} during the timed steps")
-    per = np.array(per)  # ms [steps][call]
-    total_ms = max_over_ranks(float(per.sum()), world, dev)
+    total_ms = max_over_ranks(float(np.sum(step_ms)), world, dev)
+    # each call's own time (events between the calls), for the rooflines
+    per = np.array([one_step(True, per_call=True) for _ in range(args.steps)])  # ms [steps][call]
 
     # ---------------- end to end through host buffers (pinned), when they fit
     host = {k: v.cpu().pin_memory() for k, v in pristine.items()} if \
@@ -390,12 +404,8 @@ def run_ours(args, rank, world):
             for k, v in host.items():
                 work[k].copy_(v, non_blocking=True)
             cur.copy_(host_cur, non_blocking=True)
-            bkv.fps_update(dims, None, step, work["ring"], work["buf"], work["cnt"], True, bidx,
-                           beac, nb, ws, stream)
-            bkv.score(dims, work["K"], work["L"], work["kpos"], work["ring"], step, beac, nb,
-                      cur, scores, ws, stream)
-            bkv.select_compact(dims, scores, work["K"], work["V"], work["kpos"], work["L"], kept,
-                               ws, stream)
+            bkv.round(dims, None, step, work["ring"], work["buf"], work["cnt"], bidx, beac, nb,
+                      work["K"], work["V"], work["L"], work["kpos"], cur, scores, kept, ws, stream)
             out_host["K"].copy_(work["K"][:, :B], non_blocking=True)
             out_host["V"].copy_(work["V"][:, :B], non_blocking=True)
             out_host["kpos"].copy_(work["kpos"][:, :B], non_blocking=True)
@@ -431,7 +441,12 @@ def run_ours(args, rank, world):
     }
     kfile = {"fps_update": "fps_cluster.cu" if cfg.C > 256 else "fps.cu", "score": "score.cu",
              "select_compact": "select_compact.cu"}
-    launches = {"fps_update": 1, "score": 2, "select_compact": 1}
+    # the library runs scoring as one launch per unit when its rows fit one
+    # CTA and the units fill the GPU (or the cache is short), else as two
+    nq16 = ((cfg.W + M) * cfg.G + 15) // 16 * 16
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fused = nq16 <= 256 and (2 * U >= sms or (cfg.L + 127) // 128 <= 24)
+    launches = {"fps_update": 1, "score": 1 if fused else 2, "select_compact": 1}
     # scoring FLOPs: 2 N_q L d per unit (N_q = (W + M) G rows; the hi/lo
     # split, the second pass and row padding are executed work, not counted)
     score_flops = U * 2.0 * (cfg.W + M) * cfg.G * Lr * d
@@ -467,7 +482,7 @@ def run_ours(args, rank, world):
         "rooflines": roofs,
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": sum(launches.values()) * args.steps,
     }
     if pool < U:
         line["config"]["units"] = f"{pool} distinct seeded units tiled to {U} on the device"

@@ -179,6 +179,28 @@ int bkv_select_compact(const bkv_dims* dims, const float* scores, void* K, void*
                        bkv_stream_t stream);
 
 /*
+ * One eviction round: bkv_fps_update (want_beacons = 1), bkv_score and
+ * bkv_select_compact on `stream`, with the arguments of those calls (K is
+ * both the scored and the compacted cache).  BeaconKV pages: the
+ * inkeast.github.io reading, section 三 (scoring with recent and beacon
+ * queries, then I = TopK over the scores), and the wzjinhao.cn explainer on
+ * FPS beacons.
+ *
+ * The results equal those of the three calls made one after the other.
+ * Inside a round the library knows that scoring follows the beacon
+ * selection, which writes none of K, kpos, L and cur_pos, so the scoring
+ * kernel launches while the selection finishes and sets itself up (tile
+ * maxima of the key positions, first key tiles, RoPE table) before waiting
+ * for the beacons; select + compact likewise launches while scoring
+ * finishes and waits for it before touching memory.  Every argument is
+ * validated before anything is enqueued; on an error nothing runs.
+ */
+int bkv_round(const bkv_dims* dims, const void* q_new, int64_t step, void* recent_q, void* buf,
+              int32_t* cnt, int32_t* beacon_idx, void* beacons, int32_t* n_beacons, void* K,
+              void* V, int32_t* L, int32_t* kpos, const int32_t* cur_pos, float* scores,
+              int32_t* kept, void* workspace, bkv_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the workspace status word:
  * *device_status = BKV_OK or the first BKV_ETIMEOUT / BKV_EDEVICE recorded
  * by a kernel since the last read.  Returns BKV_OK or BKV_ECUDA.

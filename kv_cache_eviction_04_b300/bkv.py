@@ -52,16 +52,19 @@ _lib.bkv_fps_update.argtypes = [_dp, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _vp, _
 _lib.bkv_score.argtypes = [_dp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.bkv_select_compact.argtypes = [_dp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.bkv_score_noalloc.argtypes = [_dp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp]
+_lib.bkv_round.argtypes = [_dp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                           _vp, _vp, _vp, _vp]
 _lib.bkv_get_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
 _lib.bkv_strerror.argtypes = [ctypes.c_int]
 _lib.bkv_strerror.restype = ctypes.c_char_p
 for _f in ("bkv_workspace_size", "bkv_workspace_init", "bkv_fps_update", "bkv_score",
-           "bkv_select_compact", "bkv_get_status", "bkv_version", "bkv_score_noalloc"):
+           "bkv_select_compact", "bkv_get_status", "bkv_version", "bkv_score_noalloc",
+           "bkv_round"):
     getattr(_lib, _f).restype = ctypes.c_int
 
 EXPORTS = ("bkv_workspace_size", "bkv_workspace_init", "bkv_fps_update", "bkv_score",
            "bkv_select_compact", "bkv_get_status", "bkv_strerror", "bkv_version",
-           "bkv_score_noalloc")
+           "bkv_score_noalloc", "bkv_round")
 
 # Bytes of the library's fixed scratch behind bkv_score_noalloc.
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -140,6 +143,15 @@ def select_compact(dims: Dims, scores, K, V, kpos, L, kept=None, workspace=None,
     _check(_lib.bkv_select_compact(ctypes.byref(dims), _ptr(scores), _ptr(K), _ptr(V),
                                    _ptr(kpos), _ptr(L), _ptr(kept), _ptr(workspace),
                                    _stream(stream)), "bkv_select_compact")
+
+
+def round(dims: Dims, q_new, step: int, recent_q, buf, cnt, beacon_idx, beacons, n_beacons,
+          K, V, L, kpos, cur_pos, scores, kept=None, workspace=None, stream=None):
+    """One eviction round (bkv_round): beacon selection, scoring, select + compact."""
+    _check(_lib.bkv_round(ctypes.byref(dims), _ptr(q_new), int(step), _ptr(recent_q), _ptr(buf),
+                          _ptr(cnt), _ptr(beacon_idx), _ptr(beacons), _ptr(n_beacons), _ptr(K),
+                          _ptr(V), _ptr(L), _ptr(kpos), _ptr(cur_pos), _ptr(scores), _ptr(kept),
+                          _ptr(workspace), _stream(stream)), "bkv_round")
 
 
 def get_status(workspace, stream=None) -> int:

@@ -169,6 +169,141 @@ int noalloc_scratch(void** out) {
 
 }  // namespace
 
+namespace {
+
+// Validation and parameters of the beacon-selection call (nothing launched).
+int fps_prepare(const bkv_dims* dims, const void* q_new, int64_t step, void* recent_q, void* buf,
+                int32_t* cnt, int32_t want_beacons, int32_t* beacon_idx, void* beacons,
+                int32_t* n_beacons, void* workspace, bkv::FpsParams* out, CUtensorMap* map,
+                bool* cluster_out) {
+  int v = validate(dims);
+  if (v != BKV_OK) return v;
+  if (buf == nullptr || cnt == nullptr || workspace == nullptr || step < 0) return BKV_EINVAL;
+  if (q_new != nullptr && dims->W > 0 && recent_q == nullptr) return BKV_EINVAL;
+  if (!aligned16(buf) || (q_new && !aligned16(q_new)) || (recent_q && !aligned16(recent_q)) ||
+      (beacons && !aligned16(beacons)))
+    return BKV_EINVAL;
+  const bool cluster = dims->C > 256;
+  *cluster_out = cluster;
+  if ((cluster ? bkv::fps_cluster_smem_bytes() : bkv::fps_smem_bytes(dims->C)) >
+      static_cast<size_t>(kMaxSmem))
+    return BKV_EUNSUPPORTED;
+  const int D = dims->G * dims->d;
+  bkv::FpsParams& p = *out;
+  p = bkv::FpsParams{};
+  p.q_new = static_cast<const uint16_t*>(q_new);
+  p.recent_q = static_cast<uint16_t*>(recent_q);
+  p.buf = static_cast<uint16_t*>(buf);
+  p.cnt = cnt;
+  p.beacon_idx = beacon_idx;
+  p.beacons = static_cast<uint16_t*>(beacons);
+  p.n_beacons = n_beacons;
+  p.ws = static_cast<WsHeader*>(workspace);
+  p.step = step;
+  p.U = dims->U;
+  p.D = D;
+  p.W = dims->W;
+  p.M = dims->M;
+  p.C = dims->C;
+  p.want_beacons = want_beacons != 0;
+  const uint32_t box_rows = static_cast<uint32_t>(std::min(256, (dims->C + 15) & ~15));
+  return make_map(map, buf, static_cast<uint64_t>(D), static_cast<uint64_t>(dims->C),
+                  static_cast<uint64_t>(dims->U), box_rows);
+}
+
+// Validation and parameters of the scoring call (nothing launched).  The
+// partials and status word live in `workspace` (a caller workspace, or the
+// library's static scratch).
+int score_prepare(const bkv_dims* dims, const void* K, const int32_t* L, const int32_t* kpos,
+                  const void* recent_q, int64_t step, const void* beacons,
+                  const int32_t* n_beacons, const int32_t* cur_pos, float* scores,
+                  void* workspace, bkv::ScoreParams* out, CUtensorMap* map) {
+  int v = validate(dims);
+  if (v != BKV_OK) return v;
+  if (K == nullptr || L == nullptr || kpos == nullptr || cur_pos == nullptr ||
+      scores == nullptr || step < 0)
+    return BKV_EINVAL;
+  if (dims->W > 0 && recent_q == nullptr) return BKV_EINVAL;
+  if (dims->M > 0 && (beacons == nullptr || n_beacons == nullptr)) return BKV_EINVAL;
+  if (!aligned16(K) || (recent_q && !aligned16(recent_q)) || (beacons && !aligned16(beacons)))
+    return BKV_EINVAL;
+  const ScoreShape s = score_shape(dims);
+  if (bkv::score_smem_bytes(dims->d, s.NQ16, dims->W, s.fused) > static_cast<size_t>(kMaxSmem))
+    return BKV_EUNSUPPORTED;
+  bkv::ScoreParams& p = *out;
+  p = bkv::ScoreParams{};
+  p.L = L;
+  p.kpos = kpos;
+  p.recent_q = static_cast<const uint16_t*>(recent_q);
+  p.beacons = static_cast<const uint16_t*>(beacons);
+  p.n_beacons = n_beacons;
+  p.cur_pos = cur_pos;
+  p.scores = scores;
+  p.part = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + bkv::kWsHeaderBytes);
+  p.ws = static_cast<WsHeader*>(workspace);
+  p.step = step;
+  p.U = dims->U;
+  p.G = dims->G;
+  p.d = dims->d;
+  p.W = dims->W;
+  p.M = dims->M;
+  p.L_cap = dims->L_cap;
+  p.NQ = s.NQ;
+  p.NQ16 = s.NQ16;
+  p.nrows_part = s.nrows_part;
+  p.ngrp = s.ngrp;
+  p.nsplit = s.nsplit;
+  p.tiles_per_split = s.tiles_per_split;
+  p.fused = s.fused ? 1 : 0;
+  p.agg = dims->agg;
+  p.causal = dims->causal_recent;
+  p.early_reads = 0;
+  p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dims->d)));
+  for (int i = 0; i < dims->d / 2; ++i) {
+    const double f = std::pow(dims->rope_theta, -2.0 * i / static_cast<double>(dims->d));
+    p.freq_hi[i] = static_cast<float>(f);
+    p.freq_lo[i] = static_cast<float>(f - static_cast<double>(p.freq_hi[i]));
+  }
+  return make_map(map, K, static_cast<uint64_t>(dims->d), static_cast<uint64_t>(dims->L_cap),
+                  static_cast<uint64_t>(dims->U), 128);
+}
+
+// Validation and parameters of the select + compact call (nothing launched).
+int select_prepare(const bkv_dims* dims, const float* scores, void* K, void* V, int32_t* kpos,
+                   int32_t* L, int32_t* kept, void* workspace, bkv::SelectParams* out) {
+  const int v = validate(dims);
+  if (v != BKV_OK) return v;
+  if (scores == nullptr || K == nullptr || V == nullptr || kpos == nullptr || L == nullptr ||
+      workspace == nullptr)
+    return BKV_EINVAL;
+  if (!aligned16(K) || !aligned16(V)) return BKV_EINVAL;
+  int nbufs = 0, buf_bytes = 0;
+  bkv::select_ring(dims->B_KV, dims->L_cap, dims->U >= 2 * sm_count(), &nbufs, &buf_bytes);
+  if (nbufs < 3 ||
+      bkv::select_smem_bytes(dims->B_KV, nbufs, buf_bytes) > static_cast<size_t>(kMaxSmem))
+    return BKV_EUNSUPPORTED;
+  bkv::SelectParams& p = *out;
+  p = bkv::SelectParams{};
+  p.scores = scores;
+  p.K = static_cast<uint8_t*>(K);
+  p.V = static_cast<uint8_t*>(V);
+  p.kpos = kpos;
+  p.L = L;
+  p.kept = kept;
+  p.ws = static_cast<WsHeader*>(workspace);
+  p.U = dims->U;
+  p.L_cap = dims->L_cap;
+  p.B = dims->B_KV;
+  p.R = dims->R;
+  p.row_bytes = dims->d * 2;
+  p.ncl = select_cluster_size(dims->U);
+  p.nbufs = nbufs;
+  p.buf_bytes = buf_bytes;
+  return BKV_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int bkv_version(void) { return 1; }
@@ -201,38 +336,11 @@ int bkv_workspace_init(void* workspace, size_t bytes, bkv_stream_t stream) {
 int bkv_fps_update(const bkv_dims* dims, const void* q_new, int64_t step, void* recent_q,
                    void* buf, int32_t* cnt, int32_t want_beacons, int32_t* beacon_idx,
                    void* beacons, int32_t* n_beacons, void* workspace, bkv_stream_t stream) {
-  int v = validate(dims);
-  if (v != BKV_OK) return v;
-  if (buf == nullptr || cnt == nullptr || workspace == nullptr || step < 0) return BKV_EINVAL;
-  if (q_new != nullptr && dims->W > 0 && recent_q == nullptr) return BKV_EINVAL;
-  if (!aligned16(buf) || (q_new && !aligned16(q_new)) || (recent_q && !aligned16(recent_q)) ||
-      (beacons && !aligned16(beacons)))
-    return BKV_EINVAL;
-  const bool cluster = dims->C > 256;
-  if ((cluster ? bkv::fps_cluster_smem_bytes() : bkv::fps_smem_bytes(dims->C)) >
-      static_cast<size_t>(kMaxSmem))
-    return BKV_EUNSUPPORTED;
-  const int D = dims->G * dims->d;
   bkv::FpsParams p{};
-  p.q_new = static_cast<const uint16_t*>(q_new);
-  p.recent_q = static_cast<uint16_t*>(recent_q);
-  p.buf = static_cast<uint16_t*>(buf);
-  p.cnt = cnt;
-  p.beacon_idx = beacon_idx;
-  p.beacons = static_cast<uint16_t*>(beacons);
-  p.n_beacons = n_beacons;
-  p.ws = static_cast<WsHeader*>(workspace);
-  p.step = step;
-  p.U = dims->U;
-  p.D = D;
-  p.W = dims->W;
-  p.M = dims->M;
-  p.C = dims->C;
-  p.want_beacons = want_beacons != 0;
   CUtensorMap map;
-  const uint32_t box_rows = static_cast<uint32_t>(std::min(256, (dims->C + 15) & ~15));
-  v = make_map(&map, buf, static_cast<uint64_t>(D), static_cast<uint64_t>(dims->C),
-               static_cast<uint64_t>(dims->U), box_rows);
+  bool cluster = false;
+  const int v = fps_prepare(dims, q_new, step, recent_q, buf, cnt, want_beacons, beacon_idx,
+                            beacons, n_beacons, workspace, &p, &map, &cluster);
   if (v != BKV_OK) return v;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return cuda_rc(cluster ? bkv::launch_fps_cluster(p, map, st) : bkv::launch_fps(p, map, st));
@@ -242,54 +350,11 @@ int bkv_score(const bkv_dims* dims, const void* K, const int32_t* L, const int32
               const void* recent_q, int64_t step, const void* beacons,
               const int32_t* n_beacons, const int32_t* cur_pos, float* scores,
               void* workspace, bkv_stream_t stream) {
-  int v = validate(dims);
-  if (v != BKV_OK) return v;
-  if (K == nullptr || L == nullptr || kpos == nullptr || cur_pos == nullptr ||
-      scores == nullptr || workspace == nullptr || step < 0)
-    return BKV_EINVAL;
-  if (dims->W > 0 && recent_q == nullptr) return BKV_EINVAL;
-  if (dims->M > 0 && (beacons == nullptr || n_beacons == nullptr)) return BKV_EINVAL;
-  if (!aligned16(K) || (recent_q && !aligned16(recent_q)) || (beacons && !aligned16(beacons)))
-    return BKV_EINVAL;
-  const ScoreShape s = score_shape(dims);
-  if (bkv::score_smem_bytes(dims->d, s.NQ16, dims->W, s.fused) > static_cast<size_t>(kMaxSmem))
-    return BKV_EUNSUPPORTED;
-  const WsLayout w = ws_layout(dims);
+  if (workspace == nullptr) return BKV_EINVAL;
   bkv::ScoreParams p{};
-  p.L = L;
-  p.kpos = kpos;
-  p.recent_q = static_cast<const uint16_t*>(recent_q);
-  p.beacons = static_cast<const uint16_t*>(beacons);
-  p.n_beacons = n_beacons;
-  p.cur_pos = cur_pos;
-  p.scores = scores;
-  p.part = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + w.part);
-  p.ws = static_cast<WsHeader*>(workspace);
-  p.step = step;
-  p.U = dims->U;
-  p.G = dims->G;
-  p.d = dims->d;
-  p.W = dims->W;
-  p.M = dims->M;
-  p.L_cap = dims->L_cap;
-  p.NQ = s.NQ;
-  p.NQ16 = s.NQ16;
-  p.nrows_part = s.nrows_part;
-  p.ngrp = s.ngrp;
-  p.nsplit = s.nsplit;
-  p.tiles_per_split = s.tiles_per_split;
-  p.fused = s.fused ? 1 : 0;
-  p.agg = dims->agg;
-  p.causal = dims->causal_recent;
-  p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dims->d)));
-  for (int i = 0; i < dims->d / 2; ++i) {
-    const double f = std::pow(dims->rope_theta, -2.0 * i / static_cast<double>(dims->d));
-    p.freq_hi[i] = static_cast<float>(f);
-    p.freq_lo[i] = static_cast<float>(f - static_cast<double>(p.freq_hi[i]));
-  }
   CUtensorMap map;
-  v = make_map(&map, K, static_cast<uint64_t>(dims->d), static_cast<uint64_t>(dims->L_cap),
-               static_cast<uint64_t>(dims->U), 128);
+  const int v = score_prepare(dims, K, L, kpos, recent_q, step, beacons, n_beacons, cur_pos,
+                              scores, workspace, &p, &map);
   if (v != BKV_OK) return v;
   return cuda_rc(bkv::launch_score(p, map, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -297,34 +362,43 @@ int bkv_score(const bkv_dims* dims, const void* K, const int32_t* L, const int32
 int bkv_select_compact(const bkv_dims* dims, const float* scores, void* K, void* V,
                        int32_t* kpos, int32_t* L, int32_t* kept, void* workspace,
                        bkv_stream_t stream) {
-  const int v = validate(dims);
-  if (v != BKV_OK) return v;
-  if (scores == nullptr || K == nullptr || V == nullptr || kpos == nullptr || L == nullptr ||
-      workspace == nullptr)
-    return BKV_EINVAL;
-  if (!aligned16(K) || !aligned16(V)) return BKV_EINVAL;
-  int nbufs = 0, buf_bytes = 0;
-  bkv::select_ring(dims->B_KV, dims->L_cap, dims->U >= 2 * sm_count(), &nbufs, &buf_bytes);
-  if (nbufs < 3 ||
-      bkv::select_smem_bytes(dims->B_KV, nbufs, buf_bytes) > static_cast<size_t>(kMaxSmem))
-    return BKV_EUNSUPPORTED;
   bkv::SelectParams p{};
-  p.scores = scores;
-  p.K = static_cast<uint8_t*>(K);
-  p.V = static_cast<uint8_t*>(V);
-  p.kpos = kpos;
-  p.L = L;
-  p.kept = kept;
-  p.ws = static_cast<WsHeader*>(workspace);
-  p.U = dims->U;
-  p.L_cap = dims->L_cap;
-  p.B = dims->B_KV;
-  p.R = dims->R;
-  p.row_bytes = dims->d * 2;
-  p.ncl = select_cluster_size(dims->U);
-  p.nbufs = nbufs;
-  p.buf_bytes = buf_bytes;
+  const int v = select_prepare(dims, scores, K, V, kpos, L, kept, workspace, &p);
+  if (v != BKV_OK) return v;
   return cuda_rc(bkv::launch_select_compact(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int bkv_round(const bkv_dims* dims, const void* q_new, int64_t step, void* recent_q, void* buf,
+              int32_t* cnt, int32_t* beacon_idx, void* beacons, int32_t* n_beacons,
+              void* K, void* V, int32_t* L, int32_t* kpos, const int32_t* cur_pos,
+              float* scores, int32_t* kept, void* workspace, bkv_stream_t stream) {
+  if (workspace == nullptr) return BKV_EINVAL;
+  if (dims != nullptr && dims->M > 0 && (beacons == nullptr || n_beacons == nullptr))
+    return BKV_EINVAL;
+  bkv::FpsParams fp{};
+  CUtensorMap fmap;
+  bool cluster = false;
+  int v = fps_prepare(dims, q_new, step, recent_q, buf, cnt, 1, beacon_idx, beacons, n_beacons,
+                      workspace, &fp, &fmap, &cluster);
+  if (v != BKV_OK) return v;
+  bkv::ScoreParams sp{};
+  CUtensorMap smap;
+  v = score_prepare(dims, K, L, kpos, recent_q, step, beacons, n_beacons, cur_pos, scores,
+                    workspace, &sp, &smap);
+  if (v != BKV_OK) return v;
+  bkv::SelectParams cp{};
+  v = select_prepare(dims, scores, K, V, kpos, L, kept, workspace, &cp);
+  if (v != BKV_OK) return v;
+  // scoring follows the beacon selection directly on the stream, and the
+  // selection writes none of K, kpos, L or cur_pos: scoring may read them
+  // before it waits for the selection
+  sp.early_reads = 1;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  v = cuda_rc(cluster ? bkv::launch_fps_cluster(fp, fmap, st) : bkv::launch_fps(fp, fmap, st));
+  if (v != BKV_OK) return v;
+  v = cuda_rc(bkv::launch_score(sp, smap, st));
+  if (v != BKV_OK) return v;
+  return cuda_rc(bkv::launch_select_compact(cp, st));
 }
 
 int bkv_score_noalloc(const bkv_dims* dims, const void* K, const int32_t* L,
@@ -333,61 +407,21 @@ int bkv_score_noalloc(const bkv_dims* dims, const void* K, const int32_t* L,
                       float* scores, int32_t* device_status, bkv_stream_t stream) {
   int v = validate(dims);
   if (v != BKV_OK) return v;
-  if (K == nullptr || L == nullptr || kpos == nullptr || cur_pos == nullptr ||
-      scores == nullptr || step < 0)
-    return BKV_EINVAL;
-  if (dims->W > 0 && recent_q == nullptr) return BKV_EINVAL;
-  if (dims->M > 0 && (beacons == nullptr || n_beacons == nullptr)) return BKV_EINVAL;
-  if (!aligned16(K) || (recent_q && !aligned16(recent_q)) || (beacons && !aligned16(beacons)))
-    return BKV_EINVAL;
   const ScoreShape s = score_shape(dims);
-  if (bkv::score_smem_bytes(dims->d, s.NQ16, dims->W, s.fused) > static_cast<size_t>(kMaxSmem))
-    return BKV_EUNSUPPORTED;
   const size_t need = bkv::kWsHeaderBytes +
                       static_cast<size_t>(dims->U) * s.nsplit * s.nrows_part * sizeof(float2);
   if (need > static_cast<size_t>(BKV_NOALLOC_SCRATCH_BYTES)) return BKV_EUNSUPPORTED;
   void* base = nullptr;
   v = noalloc_scratch(&base);
   if (v != BKV_OK) return v;
+  bkv::ScoreParams p{};
+  CUtensorMap map;
+  v = score_prepare(dims, K, L, kpos, recent_q, step, beacons, n_beacons, cur_pos, scores, base,
+                    &p, &map);
+  if (v != BKV_OK) return v;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the previous call's status must not leak into this one
   if (cudaMemsetAsync(base, 0, bkv::kWsHeaderBytes, st) != cudaSuccess) return BKV_ECUDA;
-  bkv::ScoreParams p{};
-  p.L = L;
-  p.kpos = kpos;
-  p.recent_q = static_cast<const uint16_t*>(recent_q);
-  p.beacons = static_cast<const uint16_t*>(beacons);
-  p.n_beacons = n_beacons;
-  p.cur_pos = cur_pos;
-  p.scores = scores;
-  p.part = reinterpret_cast<float2*>(static_cast<uint8_t*>(base) + bkv::kWsHeaderBytes);
-  p.ws = static_cast<WsHeader*>(base);
-  p.step = step;
-  p.U = dims->U;
-  p.G = dims->G;
-  p.d = dims->d;
-  p.W = dims->W;
-  p.M = dims->M;
-  p.L_cap = dims->L_cap;
-  p.NQ = s.NQ;
-  p.NQ16 = s.NQ16;
-  p.nrows_part = s.nrows_part;
-  p.ngrp = s.ngrp;
-  p.nsplit = s.nsplit;
-  p.tiles_per_split = s.tiles_per_split;
-  p.fused = s.fused ? 1 : 0;
-  p.agg = dims->agg;
-  p.causal = dims->causal_recent;
-  p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dims->d)));
-  for (int i = 0; i < dims->d / 2; ++i) {
-    const double f = std::pow(dims->rope_theta, -2.0 * i / static_cast<double>(dims->d));
-    p.freq_hi[i] = static_cast<float>(f);
-    p.freq_lo[i] = static_cast<float>(f - static_cast<double>(p.freq_hi[i]));
-  }
-  CUtensorMap map;
-  v = make_map(&map, K, static_cast<uint64_t>(dims->d), static_cast<uint64_t>(dims->L_cap),
-               static_cast<uint64_t>(dims->U), 128);
-  if (v != BKV_OK) return v;
   v = cuda_rc(bkv::launch_score(p, map, st));
   if (v != BKV_OK) return v;
   if (device_status != nullptr &&

@@ -580,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                ~static_cast<uintptr_t>(1023));
   FpsShared* sh = reinterpret_cast<FpsShared*>(stages + kStages * stage_rows * 128);
   const int u = blockIdx.x, tid = threadIdx.x;
+  pdl_trigger();  // scoring may set up on free SMs; it waits for this grid before reading it
   const int D = p.D;
   uint16_t* buf = p.buf + static_cast<size_t>(u) * p.C * D;
 

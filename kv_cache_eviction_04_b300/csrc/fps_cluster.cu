@@ -425,6 +425,7 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
 __global__ void __launch_bounds__(kCT, 1)
     fps_cluster_kernel(const __grid_constant__ FpsParams p,
                        const __grid_constant__ CUtensorMap bmap) {
+  pdl_trigger();  // scoring may set up on free SMs; it waits for this grid before reading it
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));

@@ -30,6 +30,8 @@ struct ScoreParams {
   int32_t tiles_per_split;  // 128-key tiles per split
   int32_t agg, causal;
   int32_t fused;            // 1: one CTA per unit runs both passes (NQ16 <= 256)
+  int32_t early_reads;      // 1: the previous kernel of the stream is the beacon selection,
+                            // which writes none of K, kpos, L, cur_pos (read before waiting)
   float qscale;             // log2(e) / sqrt(d)
   float freq_hi[64];        // theta^(-2i/d) = freq_hi + freq_lo
   float freq_lo[64];

@@ -50,6 +50,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// Programmatic dependent launch: let the next kernel of the stream launch
+// now (its griddepcontrol.wait still waits for this whole grid), and wait
+// until the previous kernel of the stream has completed and its memory is
+// visible (no effect when this kernel was launched without the dependency).
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Non-blocking test of a phase (returns at once).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;

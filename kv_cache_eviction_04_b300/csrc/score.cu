@@ -135,11 +135,11 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
   constexpr int kBatch = 4;
   const int total = nrows * kGroups;
   uint4 va[kBatch], vb[kBatch];
-  load_query_batch<D, kBatch>(p, u, row0, total, tid, nthr, va, vb);
+  // cos/sin of every (age, frequency); age 0 is the current position.  The
+  // positions are not written by the beacon selection, so this runs before
+  // waiting for it.
   const int32_t cur = p.cur_pos[u];
-  const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
   const int nage = max(p.W, 1);
-  // cos/sin of every (age, frequency); age 0 is the current position
   for (int idx = tid; idx < nage * H; idx += nthr) {
     const int age = idx / H, i = idx % H;
     const float a = reduce_angle(static_cast<float>(cur - age), p.freq_hi[i], p.freq_lo[i]);
@@ -147,6 +147,11 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
     sincosf(a, &s, &c);
     cs[idx] = make_float2(c, s);
   }
+  // the recent queries, beacons and beacon counts come from the previous
+  // call (the beacon selection)
+  pdl_wait();
+  load_query_batch<D, kBatch>(p, u, row0, total, tid, nthr, va, vb);
+  const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
   for (int r = tid; r < nrows; r += nthr) row_pos[r] = row_position(p, u, row0 + r, nb, cur);
   named_sync(bar, nthr);
   for (int idx0 = tid; idx0 < total; idx0 += kBatch * nthr) {
@@ -834,6 +839,12 @@ template <int D, int NS, int NR>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     score_fused_kernel(const __grid_constant__ ScoreParams p,
                        const __grid_constant__ CUtensorMap kmap) {
+  pdl_trigger();  // select + compact may set up; it waits for this grid before reading it
+  // Launched as a programmatic dependent: wait for the previous kernel before
+  // reading anything, unless that kernel is known to be the beacon selection
+  // (then only its outputs -- beacons, their counts, the recent ring -- wait,
+  // in the query build).
+  if (!p.early_reads) pdl_wait();
   constexpr int kRows = NR * 128;
   constexpr uint32_t kQBytes = kRows * D * 2;  // one query image (hi or lo)
   constexpr uint32_t kStageBytes = kTileKeys * D * 2;
@@ -1050,12 +1061,26 @@ size_t final_smem(int W) {
          256 * 4 + static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
 }
 
+// pdl: launched as a programmatic dependent of the previous kernel of the
+// stream (its setup overlaps that kernel's tail; the kernel waits for it
+// before reading what it wrote).
 template <typename Kern>
 cudaError_t launch(Kern kernel, dim3 grid, size_t smem, cudaStream_t st, const ScoreParams& p,
-                   const CUtensorMap& map, int threads = kThreads) {
+                   const CUtensorMap& map, int threads = kThreads, bool pdl = false) {
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, threads, smem, st>>>(p, map);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kernel, p, map);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1085,12 +1110,13 @@ cudaError_t launch_score(const ScoreParams& p, const CUtensorMap& kmap, cudaStre
     const int T = kFusedThreads;
     if (p.d == 128)
       return one ? launch(score_fused_kernel<128, 4, 1>, g, fused_smem<128, 4, 1>(p.W), st, p,
-                          kmap, T)
+                          kmap, T, true)
                  : launch(score_fused_kernel<128, 2, 2>, g, fused_smem<128, 2, 2>(p.W), st, p,
-                          kmap, T);
-    return one ? launch(score_fused_kernel<64, 4, 1>, g, fused_smem<64, 4, 1>(p.W), st, p, kmap, T)
+                          kmap, T, true);
+    return one ? launch(score_fused_kernel<64, 4, 1>, g, fused_smem<64, 4, 1>(p.W), st, p, kmap, T,
+                        true)
                : launch(score_fused_kernel<64, 4, 2>, g, fused_smem<64, 4, 2>(p.W), st, p, kmap,
-                        T);
+                        T, true);
   }
   const dim3 g1(p.nsplit, p.nrows_part / 128, p.U);
   const dim3 g2(p.nsplit, p.ngrp, p.U);

@@ -214,6 +214,9 @@ __global__ void __launch_bounds__(kThreads)
   const int u = blockIdx.x / ncl;
   const int tid = threadIdx.x;
   const float* sc = p.scores + static_cast<size_t>(u) * p.L_cap;
+  // the scores, and the K rows that scoring reads, belong to the previous
+  // kernel of the stream until it completes
+  pdl_wait();
 
   int L = p.L[u];
   const bool valid = L >= 0 && L <= p.L_cap;
@@ -379,13 +382,17 @@ cudaError_t launch_select_compact(const SelectParams& p, cudaStream_t st) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(p.ncl);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // a programmatic dependent of the scoring kernel: it launches while that
+  // kernel finishes and waits for it before touching any of its data
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, select_compact_kernel, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

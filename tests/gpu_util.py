@@ -83,6 +83,12 @@ class DeviceState:
         bkv.score(self.dims, self.K, self.L, self.kpos, self.ring, self.step, self.beac, self.nb,
                   self.cur, self.scores, self.ws)
 
+    def round(self, with_append=True):
+        """The whole round through the one call (bkv_round)."""
+        bkv.round(self.dims, self.q_new if with_append else None, self.step, self.ring, self.buf,
+                  self.cnt, self.bidx, self.beac, self.nb, self.K, self.V, self.L, self.kpos,
+                  self.cur, self.scores, self.kept, self.ws)
+
     def select_compact(self):
         bkv.select_compact(self.dims, self.scores, self.K, self.V, self.kpos, self.L, self.kept,
                            self.ws)

@@ -109,6 +109,25 @@ def test_null_and_misaligned_pointers_rejected():
     assert bkv.raw("bkv_get_status")(None, None, ctypes.byref(st)) == bkv.EINVAL
 
 
+def test_round_validates_before_enqueuing():
+    """bkv_round rejects bad arguments before any CUDA call (no GPU needed)."""
+    d = _dims()
+    f = bkv.raw("bkv_round")
+    fake = 1 << 20  # never dereferenced: validation fails first
+    # dims q_new step recent_q buf cnt bidx beacons nb K V L kpos cur scores kept ws stream
+    args = [ctypes.byref(d), None, 5, fake, fake, fake, None, fake, fake, fake, fake, fake, fake,
+            fake, fake, None, fake, None]
+    for i, bad in ((16, None), (4, None), (5, None), (2, -1), (4, fake + 8), (7, None),
+                   (8, None)):
+        a = list(args)
+        a[i] = bad
+        assert f(*a) == bkv.EINVAL, i
+    bad_dims = _dims(G=0)
+    a = list(args)
+    a[0] = ctypes.byref(bad_dims)
+    assert f(*a) == bkv.EINVAL
+
+
 def test_binding_raises_on_error_codes():
     with pytest.raises(bkv.BkvError) as e:
         bkv.workspace_size(_dims(U=0))

@@ -287,11 +287,15 @@ def test_fps_exact_ties_and_zero_vectors(cid):
 # ------------------------------------------------------------ whole round
 
 
-def _round_parity(cfg, units, st, append=True):
-    st.fps(with_append=append)
-    st.score()
+def _round_parity(cfg, units, st, append=True, one_call=False):
+    if one_call:
+        st.round(with_append=append)
+    else:
+        st.fps(with_append=append)
+        st.score()
     sg = st.scores.cpu().numpy().astype(np.float64)
-    st.select_compact()
+    if not one_call:
+        st.select_compact()
     assert st.status() == 0
     worst = -1.0
     for u in range(st.U):
@@ -343,6 +347,36 @@ def test_round_parity_bench_round_full():
     units = wl.make_units(cfg, range(cfg.U))
     units["ring"][:, int(units["step"]) % cfg.W] = units["q_new"]
     _round_parity(cfg, units, DeviceState(units, cfg), append=False)
+
+
+def test_round_call_parity_bench_round_full():
+    """The benchmark's round through the one call (bkv_round), every unit
+    checked against the oracle."""
+    cfg = wl.CONFIGS[2]
+    units = wl.make_units(cfg, range(cfg.U))
+    units["ring"][:, int(units["step"]) % cfg.W] = units["q_new"]
+    _round_parity(cfg, units, DeviceState(units, cfg), append=False, one_call=True)
+
+
+@pytest.mark.parametrize("cid,nunits,append", [(1, None, True), (2, None, False), (2, 16, True),
+                                               (5, 1, True)])
+def test_round_call_equals_the_three_calls(cid, nunits, append):
+    """bkv_round and bkv_fps_update + bkv_score + bkv_select_compact give
+    bit-identical outputs (buffers, beacons, scores, cache)."""
+    cfg = wl.CONFIGS[cid]
+    units = wl.make_units(cfg, range(cfg.U if nunits is None else nunits))
+    if not append:
+        units["ring"][:, int(units["step"]) % cfg.W] = units["q_new"]
+    a, b = DeviceState(units, cfg), DeviceState(units, cfg)
+    a.fps(with_append=append)
+    a.score()
+    a.select_compact()
+    b.round(with_append=append)
+    assert a.status() == 0 and b.status() == 0
+    for name in ("ring", "buf", "cnt", "bidx", "beac", "nb", "scores", "K", "V", "kpos", "L",
+                 "kept"):
+        x, y = getattr(a, name), getattr(b, name)
+        assert torch.equal(x, y), name
 
 
 def test_round_parity_32k_cache_one_unit():
