@@ -11,12 +11,13 @@
 // shared memory (it reuses the copy ring, which is idle until then); longer
 // caches than the ring holds read the keys from global memory instead.
 //   * radix select on the keys in three passes of 11, 11 and 10 bits from
-//     the top: a 2048-bin shared-memory histogram with warp-aggregated
-//     increments (match.any), then a block scan finds the bin holding the
-//     k-th largest;
-//   * the ascending kept list by block prefix sums (equal scores: the lower
-//     slots first; when every key equal to the threshold is kept, one
-//     comparison per slot decides).
+//     the top: a 2048-bin shared-memory histogram filled with shared-memory
+//     atomics (cheaper here than aggregating lanes with match.any first),
+//     then a block scan finds the bin holding the k-th largest;
+//   * the ascending kept list: each warp scans its own span of slots, lanes
+//     taking interleaved slots (conflict-free), with a ballot per step for
+//     the order and a scan over the warps for the offsets (equal scores:
+//     the lower slots first).
 // The unit's old key positions are staged in the ring's last two buffers
 // and gathered for the moved rows while the first waves' loads fly.
 // Compaction (row i <- row kept[i], kept[i] >= i) runs in waves over the
@@ -65,8 +66,8 @@ __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot) {
 
 struct __align__(16) Smem {
   int32_t hist[2048];
-  int32_t eq_total;  // candidates equal to the threshold key
   int32_t warp_tot[kWarps];
+  int32_t warp_eq[kWarps];
   uint32_t prefix;
   int32_t krem;
   int32_t first;
@@ -103,7 +104,6 @@ __device__ int select_kept(const SelectParams& p, const float* sc, const uint32_
   const int k = p.B - p.R;
   uint32_t prefix = 0;
   int krem = k;
-  if (tid == 0) sm->eq_total = 0;
   if (k > 0) {
     constexpr int kShift[3] = {21, 10, 0};
     constexpr uint32_t kDigit[3] = {2047u, 2047u, 1023u};
@@ -115,16 +115,19 @@ __device__ int select_kept(const SelectParams& p, const float* sc, const uint32_
 #pragma unroll
       for (int b8 = 0; b8 < 8; ++b8) sm->hist[tid * 8 + b8] = 0;
       __syncthreads();
-      for (int j0 = 0; j0 < ncand; j0 += kThreads) {
-        const int j = j0 + tid;
-        const bool in = j < ncand;
-        const uint32_t key = in ? key_at(j) : 0u;
-        const bool hit = in && (key & hmask) == prefix;
-        const uint32_t bin = (key >> shift) & dmask;
-        const uint32_t active = __ballot_sync(0xffffffffu, hit);
-        if (hit) {
-          const uint32_t same = __match_any_sync(active, bin);
-          if ((__ffs(same) - 1) == lane) atomicAdd(&sm->hist[bin], __popc(same));
+      // four slots per thread per step, loaded before any is used (indices
+      // clamped into range; slots past ncand are discarded)
+      for (int j0 = 0; j0 < ncand; j0 += 4 * kThreads) {
+        uint32_t kv[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) kv[q4] = key_at(min(j0 + q4 * kThreads + tid, ncand - 1));
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const bool in = j0 + q4 * kThreads + tid < ncand;
+          const uint32_t key = kv[q4];
+          const bool hit = in && (key & hmask) == prefix;
+          const uint32_t bin = (key >> shift) & dmask;
+          if (hit) atomicAdd(&sm->hist[bin], 1);
         }
       }
       __syncthreads();
@@ -142,7 +145,6 @@ __device__ int select_kept(const SelectParams& p, const float* sc, const uint32_
           if (above < krem && above + c[b8] >= krem) {
             sm->prefix = prefix | (static_cast<uint32_t>(2047 - tid * 8 - b8) << shift);
             sm->krem = krem - above;
-            if (pass == 2) sm->eq_total = c[b8];
           }
           above += c[b8];
         }
@@ -157,44 +159,77 @@ __device__ int select_kept(const SelectParams& p, const float* sc, const uint32_
   }
   const uint32_t T = prefix;
   const int need_eq = krem;  // candidates equal to T kept, lowest slots first
-  // ---------------- ascending kept list: contiguous segment per thread
-  const int seg = (L + kThreads - 1) / kThreads;
-  const int j0 = min(tid * seg, L), j1 = min(j0 + seg, L);
-  if (k > 0 && sm->eq_total == need_eq) {
-    // every candidate equal to T is kept: keep = key >= T
-    int cnt = 0;
-    for (int j = j0; j < j1; ++j) cnt += (j >= ncand || key_at(j) >= T);
-    int pos = block_incl_scan(cnt, sm->warp_tot) - cnt;
-    for (int j = j0; j < j1; ++j)
-      if (j >= ncand || key_at(j) >= T) kept_s[pos++] = j;
-    __syncthreads();
-    return n_kept;
-  }
-  int eq_local = 0;
-  for (int j = j0; j < j1 && j < ncand; ++j) eq_local += key_at(j) == T;
-  const int eq_before = block_incl_scan(eq_local, sm->warp_tot) - eq_local;
-  int kept_local = 0;
-  {
-    int e = eq_before;
-    for (int j = j0; j < j1; ++j) {
-      bool keep = j >= ncand;
-      if (!keep) {
-        const uint32_t key = key_at(j);
-        keep = key > T || (key == T && e++ < need_eq);
-      }
-      kept_local += keep;
+  // ---------------- ascending kept list.  Warp w takes slots
+  // [w s, w s + s) (s a multiple of 32), lane l the slot w s + 32 i + l in
+  // step i: shared-memory reads are conflict-free and a ballot per step
+  // keeps the slot order.  Pass 1 counts, per warp, the slots kept for sure
+  // (key > T, or in the recent window) and the candidates equal to T; a scan
+  // over the warps gives each warp the equal candidates before it and its
+  // first output index; pass 2 keeps the first need_eq equal candidates in
+  // slot order and writes the list.
+  const int warp = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const int span = ((L + 32 * kWarps - 1) / (32 * kWarps)) * 32;
+  const int jb = min(warp * span, L), je = min(jb + span, L);
+  // keys of four steps are loaded before any is used (indices clamped into
+  // range; slots past the span are discarded)
+  auto load4 = [&](int i0, uint32_t (&kv)[4]) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) kv[q4] = key_at(min(i0 + 32 * q4 + lane, L - 1));
+  };
+  auto classify = [&](int j, uint32_t key, bool& gt, bool& eq) {
+    const bool in = j < je;
+    const bool win = in && j >= ncand;  // the recent window: always kept
+    gt = win || (in && key > T);
+    eq = in && !win && key == T;
+  };
+  int n_gt = 0, n_eq = 0;  // per lane, summed over the warp below
+  for (int i0 = jb; i0 < je; i0 += 128) {
+    uint32_t kv[4];
+    load4(i0, kv);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      bool gt, eq;
+      classify(i0 + 32 * q4 + lane, kv[q4], gt, eq);
+      n_gt += gt;
+      n_eq += eq;
     }
   }
-  int pos = block_incl_scan(kept_local, sm->warp_tot) - kept_local;
-  {
-    int e = eq_before;
-    for (int j = j0; j < j1; ++j) {
-      bool keep = j >= ncand;
-      if (!keep) {
-        const uint32_t key = key_at(j);
-        keep = key > T || (key == T && e++ < need_eq);
+  n_gt = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(n_gt)));
+  n_eq = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(n_eq)));
+  if (lane == 0) {
+    sm->warp_tot[warp] = n_gt;
+    sm->warp_eq[warp] = n_eq;
+  }
+  __syncthreads();
+  int out = 0, e = 0;  // this warp's first output index and equal candidates before it
+  for (int w = 0; w < warp; ++w) {
+    const int eq_w = sm->warp_eq[w];
+    out += sm->warp_tot[w] + min(max(need_eq - e, 0), eq_w);
+    e += eq_w;
+  }
+  // every equal candidate of this warp is kept, or none is, unless the cut
+  // falls inside the warp (warp-uniform); only then are they ranked per step
+  const bool eq_all = e + sm->warp_eq[warp] <= need_eq, eq_none = e >= need_eq;
+  for (int i0 = jb; i0 < je; i0 += 128) {
+    uint32_t kv[4];
+    load4(i0, kv);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int j = i0 + 32 * q4 + lane;
+      bool gt, eq;
+      classify(j, kv[q4], gt, eq);
+      bool keep;
+      if (eq_all || eq_none) {
+        keep = gt || (eq && eq_all);
+      } else {
+        const uint32_t beq = __ballot_sync(0xffffffffu, eq);
+        keep = gt || (eq && e + __popc(beq & lt_mask) < need_eq);
+        e += __popc(beq);
       }
-      if (keep) kept_s[pos++] = j;
+      const uint32_t bk = __ballot_sync(0xffffffffu, keep);
+      if (keep) kept_s[out + __popc(bk & lt_mask)] = j;
+      out += __popc(bk);
     }
   }
   __syncthreads();
@@ -242,8 +277,22 @@ __global__ void __launch_bounds__(kThreads)
           ? reinterpret_cast<uint32_t*>(bufs)
           : nullptr;
   if (keys_s != nullptr) {
+    // 16-byte loads when the unit's scores are aligned (then keys_s + 4i is
+    // too: the ring is 1024-byte aligned)
+    if ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0) {
+      const float4* s4 = reinterpret_cast<const float4*>(sc);
+      const int n4 = L >> 2;
 #pragma unroll 8
-    for (int j = tid; j < L; j += kThreads) keys_s[j] = order_key(sc[j]);
+      for (int i = tid; i < n4; i += kThreads) {
+        const float4 v = s4[i];
+        reinterpret_cast<uint4*>(keys_s)[i] =
+            make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+      }
+      for (int j = 4 * n4 + tid; j < L; j += kThreads) keys_s[j] = order_key(sc[j]);
+    } else {
+#pragma unroll 8
+      for (int j = tid; j < L; j += kThreads) keys_s[j] = order_key(sc[j]);
+    }
   }
   if (kpos_s != nullptr) {
 #pragma unroll 8
