@@ -78,16 +78,26 @@ enum { BKV_AGG_MAX = 0, BKV_AGG_MEAN = 1 };
  *   agg    BKV_AGG_MAX (the method) or BKV_AGG_MEAN
  *   causal_recent  1: a recent query at position p sees keys with kpos <= p;
  *                  0: every row sees every key
+ *   beacon_select  BKV_BEACONS_FPS (0): beacons by farthest-point
+ *                  sampling over the continual buffer, which is FPS-
+ *                  compressed when full (the method);
+ *                  BKV_BEACONS_FIRST (1): the first M buffered queries,
+ *                  the buffer keeping its first M items when it fills (the
+ *                  InitialRecent comparison of the BeaconKV pages: initial
+ *                  queries plus the recent window)
  *   rope_theta     rotary base (rotate-half pairs (i, i + d/2),
  *                  frequency theta^(-2i/d))
  * Limits: (W + M) * G <= 1024 scoring rows; positions < 2^24.
  */
+#define BKV_BEACONS_FPS 0
+#define BKV_BEACONS_FIRST 1
+
 typedef struct bkv_dims {
   int32_t U, G, d, W, M, C, B_KV, R;
   int32_t L_cap;
   int32_t agg;
   int32_t causal_recent;
-  int32_t reserved; /* must be 0 */
+  int32_t beacon_select; /* BKV_BEACONS_FPS (the method) or BKV_BEACONS_FIRST */
   double rope_theta;
 } bkv_dims;
 

@@ -32,7 +32,7 @@ int validate(const bkv_dims* d) {
   if (d->L_cap < d->B_KV || d->L_cap > (1 << 24)) return BKV_EINVAL;
   if (d->agg != BKV_AGG_MAX && d->agg != BKV_AGG_MEAN) return BKV_EINVAL;
   if (d->causal_recent != 0 && d->causal_recent != 1) return BKV_EINVAL;
-  if (d->reserved != 0) return BKV_EINVAL;
+  if (d->beacon_select != BKV_BEACONS_FPS && d->beacon_select != BKV_BEACONS_FIRST) return BKV_EINVAL;
   if (!(d->rope_theta > 1.0) || !std::isfinite(d->rope_theta)) return BKV_EINVAL;
   if (d->W + d->M < 1 || (d->W + d->M) * d->G > 1024) return BKV_EINVAL;
   if (static_cast<int64_t>(d->U) * d->L_cap * d->d >= (int64_t(1) << 40)) return BKV_EINVAL;
@@ -206,6 +206,7 @@ int fps_prepare(const bkv_dims* dims, const void* q_new, int64_t step, void* rec
   p.M = dims->M;
   p.C = dims->C;
   p.want_beacons = want_beacons != 0;
+  p.first_m = dims->beacon_select == BKV_BEACONS_FIRST ? 1 : 0;
   const uint32_t box_rows = static_cast<uint32_t>(std::min(256, (dims->C + 15) & ~15));
   return make_map(map, buf, static_cast<uint64_t>(D), static_cast<uint64_t>(dims->C),
                   static_cast<uint64_t>(dims->U), box_rows);

@@ -449,10 +449,11 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
                           uint8_t* stages, int stage_rows, int u, int n, int m) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (m <= 0) return 0;
-  if (n <= m) {
-    for (int i = tid; i < n; i += kThreads) sh->sel[i] = i;
+  if (n <= m || p.first_m) {  // every item, or the first m (in slot order)
+    const int got = min(n, m);
+    for (int i = tid; i < got; i += kThreads) sh->sel[i] = i;
     __syncthreads();
-    return n;
+    return got;
   }
   const int D = p.D;
   const int N = (n + 15) & ~15;

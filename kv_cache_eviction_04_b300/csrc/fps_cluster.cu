@@ -147,10 +147,11 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
                              uint8_t* stages, int u, int n, int m, int rank, int R, int& xc) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (m <= 0) return 0;
-  if (n <= m) {
-    for (int i = tid; i < n; i += kCT) sh->sel[i] = i;
+  if (n <= m || p.first_m) {  // every item, or the first m (in slot order)
+    const int got = min(n, m);
+    for (int i = tid; i < got; i += kCT) sh->sel[i] = i;
     __syncthreads();
-    return n;
+    return got;
   }
   const int D = p.D;
   const float tauc = tau_cos(D), taum = tau_mean(D);

@@ -70,6 +70,7 @@ struct FpsParams {
   int64_t step;
   int32_t U, D, W, M, C;
   int32_t want_beacons;
+  int32_t first_m;        // 1: the first M items instead of FPS (compress keeps them)
 };
 
 cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, cudaStream_t st);

@@ -90,24 +90,42 @@ def fps(X, m: int, with_radius: bool = False):
 
 class ContinualBuffer:
     """Per-KV-head continual FPS buffer (wzjinhao.cn explainer, section on
-    continual FPS: a bounded buffer that is FPS-compressed when full)."""
+    continual FPS: a bounded buffer that is FPS-compressed when full).
 
-    def __init__(self, C: int, M: int, D: int):
+    ``first_m``: the InitialRecent control of the same explainer (its
+    results section: the earliest generated queries kept fixed, plus the
+    recent ones) -- the beacons are the first M buffered queries, and a full
+    buffer keeps its first M items instead of an FPS selection."""
+
+    def __init__(self, C: int, M: int, D: int, first_m: bool = False):
         self.C, self.M, self.D = C, M, D
+        self.first_m = first_m
         self.buf = np.zeros((C, D), dtype=np.uint16)
         self.cnt = np.zeros(1, dtype=np.int32)
         self.compressions = 0
 
     @classmethod
-    def from_state(cls, buf, cnt: int, M: int):
+    def from_state(cls, buf, cnt: int, M: int, first_m: bool = False):
         buf = _u16(buf)
         C = buf.shape[0]
-        b = cls(C, M, int(np.prod(buf.shape[1:])))
+        b = cls(C, M, int(np.prod(buf.shape[1:])), first_m)
         b.buf[:] = buf.reshape(C, -1)
         b.cnt[0] = cnt
         return b
 
     def push(self, x) -> bool:
+        if self.first_m:
+            c = int(self.cnt[0])
+            if not 0 <= c < self.C:
+                raise ValueError("continual buffer in a bad state")
+            self.buf[c] = _u16(x).reshape(-1)
+            c += 1
+            full = c == self.C
+            if full:  # keep the first M items, in slot order
+                c = self.M
+                self.compressions += 1
+            self.cnt[0] = c
+            return full
         r = _load().ora_buffer_push(self.buf, self.cnt, _u16(x).reshape(-1), self.D, self.C,
                                     self.M)
         if r < 0:
@@ -120,8 +138,12 @@ class ContinualBuffer:
         return self.buf[: int(self.cnt[0])]
 
     def beacons(self):
-        """(selection-order indices, vectors) of FPS_M over the buffer."""
-        idx = fps(self.items, self.M)
+        """(selection-order indices, vectors) of FPS_M over the buffer (the
+        first min(cnt, M) items with ``first_m``)."""
+        if self.first_m:
+            idx = np.arange(min(int(self.cnt[0]), self.M), dtype=np.int32)
+        else:
+            idx = fps(self.items, self.M)
         return idx, self.items[idx]
 
 
@@ -188,16 +210,17 @@ def compact(rows, kept):
 
 
 def round_unit(unit: dict, W: int, M: int, B: int, R: int, theta: float,
-               agg: str = "max", causal: bool = True, append: bool = True):
+               agg: str = "max", causal: bool = True, append: bool = True,
+               first_m: bool = False):
     """One full eviction round of one unit: (if ``append``) append the new
     query to the ring and the buffer, compressing a full buffer; take the
-    beacons, score, select and compact.  ``unit`` is one unit of
-    ``workload.make_unit``.  Returns dict(beacon_idx, scores, kept, K, V,
+    beacons (FPS, or the first M buffered queries with ``first_m``), score,
+    select and compact.  ``unit`` is one unit of ``workload.make_unit``.  Returns dict(beacon_idx, scores, kept, K, V,
     kpos, buf, cnt)."""
     G, d = unit["ring"].shape[1], unit["ring"].shape[2]
     ring = unit["ring"].copy()
     step = int(unit["step"])
-    cb = ContinualBuffer.from_state(unit["buf"], int(unit["cnt"]), M)
+    cb = ContinualBuffer.from_state(unit["buf"], int(unit["cnt"]), M, first_m)
     if append:
         ring[step % W] = unit["q_new"]
         cb.push(unit["q_new"])

@@ -60,11 +60,12 @@ def test_bad_dims_rejected(bad):
     assert rc == bkv.EINVAL
 
 
-def test_reserved_must_be_zero():
-    d = _dims()
-    d.reserved = 1
+def test_beacon_select_must_be_known():
     n = ctypes.c_size_t(0)
-    assert bkv.raw("bkv_workspace_size")(ctypes.byref(d), ctypes.byref(n)) == bkv.EINVAL
+    for v, rc in ((0, bkv.OK), (1, bkv.OK), (2, bkv.EINVAL), (-1, bkv.EINVAL)):
+        d = _dims()
+        d.beacon_select = v
+        assert bkv.raw("bkv_workspace_size")(ctypes.byref(d), ctypes.byref(n)) == rc
 
 
 def test_large_buffer_capacity_reported_unsupported():

@@ -287,7 +287,7 @@ def test_fps_exact_ties_and_zero_vectors(cid):
 # ------------------------------------------------------------ whole round
 
 
-def _round_parity(cfg, units, st, append=True, one_call=False):
+def _round_parity(cfg, units, st, append=True, one_call=False, first_m=False):
     if one_call:
         st.round(with_append=append)
     else:
@@ -300,7 +300,8 @@ def _round_parity(cfg, units, st, append=True, one_call=False):
     worst = -1.0
     for u in range(st.U):
         un = _unit(units, u)
-        ref = oracle.round_unit(un, cfg.W, cfg.M, cfg.B_KV, cfg.Rw, cfg.theta, append=append)
+        ref = oracle.round_unit(un, cfg.W, cfg.M, cfg.B_KV, cfg.Rw, cfg.theta, append=append,
+                                first_m=first_m)
         nbr = len(ref["beacon_idx"])
         assert np.array_equal(st.bidx[u].cpu().numpy()[:nbr], ref["beacon_idx"]), u
         # after a compress the beacon slots are trivially 0..M-1: the buffer
@@ -347,6 +348,17 @@ def test_round_parity_bench_round_full():
     units = wl.make_units(cfg, range(cfg.U))
     units["ring"][:, int(units["step"]) % cfg.W] = units["q_new"]
     _round_parity(cfg, units, DeviceState(units, cfg), append=False)
+
+
+@pytest.mark.parametrize("cid,nunits", [(1, None), (2, 24), (5, 1)])
+def test_round_parity_first_m_beacons(cid, nunits):
+    """The InitialRecent control (beacon_select = first M): the append
+    fills the buffer (it keeps its first M items), the beacons are the first
+    M buffered queries; scores, selection and compaction as usual."""
+    cfg = wl.CONFIGS[cid]
+    units = wl.make_units(cfg, range(cfg.U if nunits is None else nunits))
+    st = DeviceState(units, cfg, beacon_select=bkv.BEACONS_FIRST)
+    _round_parity(cfg, units, st, first_m=True)
 
 
 def test_round_call_parity_bench_round_full():

@@ -167,6 +167,33 @@ def test_continual_compress_keeps_fps_survivors_in_arrival_order():
     assert cb.compressions == 4  # fills at 12, then every 8 pushes
 
 
+def test_first_m_beacons_are_the_earliest_queries():
+    """The InitialRecent control: with ``first_m`` the beacons are always
+    the earliest min(t, M) queries of the stream, whatever was appended
+    since, and a full buffer falls back to those M (fills at C, then every
+    C - M pushes); up to M items the beacons equal FPS's (which then takes
+    every item)."""
+    rng = np.random.default_rng(21)
+    C, M, D = 10, 3, 5
+    stream = _bits(rng.standard_normal((47, D)))
+    cb = oracle.ContinualBuffer(C, M, D, first_m=True)
+    for t, x in enumerate(stream, start=1):
+        cb.push(x)
+        idx, vec = cb.beacons()
+        k = min(t, M)
+        assert list(idx) == list(range(k))
+        assert np.array_equal(vec, stream[:k])
+        # the buffer: the first M queries, then those since the last fill
+        c = t if t < C else M + (t - C) % (C - M)
+        assert int(cb.cnt[0]) == c
+        if t >= C:
+            assert np.array_equal(cb.items[:M], stream[:M])
+            assert np.array_equal(cb.items[M:], stream[t - (c - M):t])
+        if t <= M:
+            assert list(idx) == list(oracle.fps(stream[:t], M))
+    assert cb.compressions == 1 + (len(stream) - C) // (C - M)
+
+
 def test_rope_relative_offset_invariance_and_identity():
     rng = np.random.default_rng(1)
     for d, theta in ((64, 1e4), (128, 1e6)):
