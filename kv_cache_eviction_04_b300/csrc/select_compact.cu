@@ -64,7 +64,21 @@ __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot) {
   return v + add;
 }
 
+// Block-wide sum of one int per thread (every thread gets it).
+__device__ __forceinline__ int block_sum(int v, int* warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = __reduce_add_sync(0xffffffffu, v);
+  __syncthreads();  // earlier readers of warp_tot are done
+  if (lane == 0) warp_tot[warp] = v;
+  __syncthreads();
+  int t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += warp_tot[w];
+  return t;
+}
+
 struct __align__(16) Smem {
+  uint64_t wbar[kMaxBufs];  // per ring buffer: a wave's gathered bytes have landed
   int32_t hist[2048];
   int32_t warp_tot[kWarps];
   int32_t warp_eq[kWarps];
@@ -259,7 +273,11 @@ __global__ void __launch_bounds__(kThreads)
     if (tid == 0 && rank == 0) record_error(p.ws, BKV_EDEVICE, kSiteSelectState);
     L = 0;
   }
-  if (tid == 0) sm->first = 0x7fffffff;
+  if (tid == 0) {
+    sm->first = 0x7fffffff;
+    for (int b = 0; b < nbufs; ++b) mbar_init(&sm->wbar[b], 1);
+    fence_mbar_init();
+  }
   const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
   const size_t ubase = static_cast<size_t>(u) * p.L_cap;
   int32_t* kp = p.kpos + ubase;
@@ -322,11 +340,22 @@ __global__ void __launch_bounds__(kThreads)
     r0 = first + (w * ncl + rank) * RS;
     cnt = max(0, min(RS, n_kept - r0));
   };
-  // All threads gather a wave's source rows of K and V into one ring buffer
-  // with 16-byte cp.async copies (K rows first, then V rows); thread 0 then
-  // writes the wave's contiguous destination rows back with two bulk stores.
+  // A wave's source rows of K and V are gathered into one ring buffer (K
+  // rows first, then V rows), and thread 0 then writes the wave's
+  // contiguous destination rows back with two bulk stores.  The gather:
+  //  * sources in runs of at least four consecutive rows on average (a
+  //    block-uniform choice per unit): warp 0 issues one TMA bulk copy per
+  //    run (runs cut at every 32 rows) and matrix, completion counted in
+  //    bytes on the buffer's mbarrier;
+  //  * scattered sources: every thread issues 16-byte cp.async copies, one
+  //    commit group per wave.
+  const int warp = tid >> 5, lane = tid & 31;
+  int nruns = 0;
+  for (int i = first + tid; i < n_kept; i += kThreads)
+    nruns += (i == first || kept_s[i - 1] + 1 != kept_s[i]) ? 1 : 0;
+  const bool use_tma = 4 * block_sum(nruns, sm->warp_tot) <= n_kept - first;
   const int ppr = static_cast<int>(rb / 16);  // 16-byte pieces per row
-  auto issue = [&](int w) {
+  auto issue_cp = [&](int w) {  // every thread
     int r0, cnt;
     slice(w, r0, cnt);
     uint8_t* buf = bufs + (w % nbufs) * bufb;
@@ -338,17 +367,45 @@ __global__ void __launch_bounds__(kThreads)
       cp_async16(buf + (is_v ? RS + row : row) * rb + pc * 16, (is_v ? Vb : Kb) + src);
     }
   };
+  auto issue = [&](int w) {  // warp 0
+    int r0, cnt;
+    slice(w, r0, cnt);
+    const int b = w % nbufs;
+    uint8_t* buf = bufs + b * bufb;
+    if (lane == 0) mbar_arrive_expect_tx(&sm->wbar[b], 2u * static_cast<uint32_t>(cnt) * rb);
+    __syncwarp();
+    for (int t0 = 0; t0 < cnt; t0 += 32) {
+      const int t = t0 + lane;
+      const bool live = t < cnt;
+      const int src = live ? kept_s[r0 + t] : 0;
+      const bool start = live && (lane == 0 || kept_s[r0 + t - 1] + 1 != src);
+      const uint32_t starts = __ballot_sync(0xffffffffu, start);
+      if (start) {
+        const uint32_t above = starts & ~((2u << lane) - 1u);  // later run starts
+        const int end = above != 0u ? __ffs(above) - 1 : min(32, cnt - t0);
+        const uint32_t bytes = static_cast<uint32_t>(end - lane) * rb;
+        const size_t off = static_cast<size_t>(src) * rb;
+        bulk_load(buf + static_cast<size_t>(t) * rb, Kb + off, bytes, &sm->wbar[b]);
+        bulk_load(buf + static_cast<size_t>(RS + t) * rb, Vb + off, bytes, &sm->wbar[b]);
+      }
+    }
+  };
   // Waves w + 1 .. w + kAhead are in flight while wave w is stored.  Wave
   // w + kAhead reuses the buffer of wave w + kAhead - nbufs = w - 2, whose
   // store is the older of the two outstanding ones (waves w - 2 and w - 1).
-  // Every thread commits one cp.async group per wave slot (empty past the
-  // last wave), so "wave w landed" is "at most kAhead groups pending".
-  // The first kAhead waves use buffers 0 .. nbufs - 3 only.
+  // Wave w is the (w / nbufs)-th use of its buffer: its mbarrier phase has
+  // that parity.  The first kAhead waves use buffers 0 .. nbufs - 3 only.
   const int kAhead = nbufs - 2;
-  for (int w = 0; w < kAhead; ++w) {
-    if (w < nw) issue(w);
-    cp_async_commit();
+  if (use_tma) {
+    if (warp == 0)
+      for (int w = 0; w < min(kAhead, nw); ++w) issue(w);
+  } else {
+    for (int w = 0; w < kAhead; ++w) {  // one group per wave slot, empty past the last wave
+      if (w < nw) issue_cp(w);
+      cp_async_commit();
+    }
   }
+  bool failed = false;  // block-uniform
   // New kpos of every row this CTA writes, gathered while those gathers fly
   // and before the first wave's barrier (no CTA writes kpos before it);
   // entry w * RS + t = wave w, row t.
@@ -365,19 +422,31 @@ __global__ void __launch_bounds__(kThreads)
   for (int w = 0; w < nw; ++w) {
     if (tid == 0) bulk_wait_read<1>();  // all stores but wave w - 1's have read smem
     __syncthreads();
-    if (w + kAhead < nw) issue(w + kAhead);
-    cp_async_commit();
-    cp_async_wait_dyn(kAhead);
-    fence_proxy_async_shared();  // this thread's smem writes -> the bulk stores
-    __syncthreads();
+    bool here = true;
+    if (use_tma) {
+      if (warp == 0 && w + kAhead < nw && !failed) issue(w + kAhead);
+      here = !failed && wait_bar(&sm->wbar[w % nbufs], (w / nbufs) & 1);
+    } else {
+      // "wave w landed" is "at most kAhead groups pending"
+      if (w + kAhead < nw) issue_cp(w + kAhead);
+      cp_async_commit();
+      cp_async_wait_dyn(kAhead);
+      fence_proxy_async_shared();  // this thread's smem writes -> the bulk stores
+    }
+    // A wave that never lands stops the copies but not the loop: every CTA
+    // of the cluster still meets at each of its barriers.
+    const bool landed = __syncthreads_and(here);
+    if (!landed && !failed && tid == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteSelectWait);
+    failed = failed || !landed;
     int r0, cnt;
     slice(w, r0, cnt);
     // Every CTA's sources of wave w are in its shared memory, so only
     // execution order matters here; a one-CTA cluster needs nothing more.
     if (ncl > 1) cluster_sync_relaxed();
-    if (cnt > 0) {
+    if (cnt > 0 && !failed) {
       if (tid == 0) {
         const uint8_t* buf = bufs + (w % nbufs) * bufb;
+        fence_proxy_async_shared();
         bulk_store(Kb + static_cast<size_t>(r0) * rb, buf, cnt * rb);
         bulk_store(Vb + static_cast<size_t>(r0) * rb, buf + RS * rb, cnt * rb);
         bulk_commit();
