@@ -219,8 +219,6 @@ static_assert(sizeof(Barriers) % 16 == 0, "arrays after the barriers need 16-byt
 // kTmaxTiles tiles in shared memory: a tile whose largest position is within
 // every row's limit needs no causal mask and no per-key positions.
 constexpr int kTmaxTiles = 512;
-// Tiles pulled into L2 ahead of the TMA loads (iterations of both passes).
-constexpr int kPrefetchAhead = 8;
 
 // Key tile range of split `s` for unit u.
 __device__ __forceinline__ void split_tiles(const ScoreParams& p, int u, int s, int& t0, int& t1,
@@ -898,9 +896,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer: every tile twice (pass 1, then pass 2).
-    // Iteration i loads tile i % nt; iteration i + kPrefetchAhead is pulled
-    // into L2 when iteration i is loaded, so HBM latency is covered beyond
-    // the NS stages of shared memory.
+    // Iteration i loads tile i % nt.  (An L2 run-ahead of bulk prefetches
+    // measured slower and, on long caches, re-read tiles from HBM.)
     const int niter = 2 * nt;
     auto issue = [&](int i) {  // stage i % NS is free
       const int st = i % NS;
@@ -909,11 +906,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 #pragma unroll
       for (int a = 0; a < D / 64; ++a)
         tma_load_3d(stages + st * kStageBytes + a * 16384, &kmap, &bars->full[st], 64 * a, j0, u);
-    };
-    auto prefetch = [&](int i) {
-      if (i < niter)
-#pragma unroll
-        for (int a = 0; a < D / 64; ++a) tma_prefetch_l2_3d(&kmap, 64 * a, (i % nt) * kTileKeys, u);
     };
     const int first = min(NS, niter);
     if (lane == 0) prefetch_tmap(&kmap);
@@ -957,8 +949,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       if (lane == 0) mbar_arrive(&bars->tmax_ready);
     }
     // The small loads above and the query build's go first; the first tiles
-    // and the L2 run-ahead follow (the run-ahead starts once the pipeline
-    // turns, after the first tile's MMAs).
+    // follow.
     if (lane == 0) {
       for (int i = 0; i < first; ++i) issue(i);
       for (int i = first; i < niter; ++i) {
@@ -970,10 +961,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           break;
         }
         issue(i);
-        if (i == first)
-          for (int k = 1; k <= kPrefetchAhead; ++k) prefetch(i + k);
-        else
-          prefetch(i + kPrefetchAhead);
       }
     }
     __syncwarp();
