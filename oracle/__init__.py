@@ -209,13 +209,37 @@ def compact(rows, kept):
     return a
 
 
+def fill_order(kept):
+    """Source slot of each row for the order-free (hole-filling) compaction.
+
+    With n = len(kept) slots kept (``kept`` ascending, as ``select`` returns
+    it), a kept slot i < n keeps its row; the slots below n that are not kept
+    (the holes), taken in ascending order, receive the kept slots at or past
+    n, also in ascending order.  Every kept row stays or moves once, and at
+    most L - n rows move.  The BeaconKV pages fix the kept set (inkeast.github.io
+    reading, section 三: I = TopK(score, B_KV)) but not where the kept entries
+    sit; this is the layout when row order is not required.  Index
+    bookkeeping only, so it is plain numpy."""
+    kept = np.asarray(kept, dtype=np.int64)
+    n = kept.size
+    is_kept = np.zeros(n, dtype=bool)
+    is_kept[kept[kept < n]] = True
+    holes = np.flatnonzero(~is_kept)
+    movers = kept[kept >= n]
+    order = np.arange(n, dtype=np.int32)
+    order[holes] = movers
+    return order
+
+
 def round_unit(unit: dict, W: int, M: int, B: int, R: int, theta: float,
                agg: str = "max", causal: bool = True, append: bool = True,
-               first_m: bool = False):
+               first_m: bool = False, fill: bool = False):
     """One full eviction round of one unit: (if ``append``) append the new
     query to the ring and the buffer, compressing a full buffer; take the
     beacons (FPS, or the first M buffered queries with ``first_m``), score,
-    select and compact.  ``unit`` is one unit of ``workload.make_unit``.  Returns dict(beacon_idx, scores, kept, K, V,
+    select and compact (order-preserving, or hole-filling with ``fill``, where
+    ``kept`` then holds each row's source slot).  ``unit`` is one unit of
+    ``workload.make_unit``.  Returns dict(beacon_idx, scores, kept, K, V,
     kpos, buf, cnt)."""
     G, d = unit["ring"].shape[1], unit["ring"].shape[2]
     ring = unit["ring"].copy()
@@ -228,6 +252,8 @@ def round_unit(unit: dict, W: int, M: int, B: int, R: int, theta: float,
     sc = score(unit["K"], unit["kpos"], ring, step, bvec.reshape(-1, G, d),
                int(unit["cur_pos"]), theta, agg, causal, L=int(unit["L"]))
     kept = select(sc, B, R)
+    if fill:
+        kept = fill_order(kept)
     K = compact(unit["K"].copy(), kept)[: kept.size]
     V = compact(unit["V"].copy(), kept)[: kept.size]
     kpos = compact(unit["kpos"].copy(), kept)[: kept.size]

@@ -365,6 +365,59 @@ def test_compact_is_a_gather():
     assert np.array_equal(out[:17], ref)
 
 
+def test_fill_order_is_the_unique_monotone_hole_matching():
+    """Three properties fix the hole-filling layout uniquely: the rows are
+    the kept set; a kept slot below n keeps its row; the holes take their
+    sources in increasing order.  Checked on random kept sets, with the
+    moved count against L - n."""
+    rng = np.random.default_rng(21)
+    for t in range(300):
+        L = int(rng.integers(1, 90))
+        n = int(rng.integers(1, L + 1))
+        kept = np.sort(rng.choice(L, n, replace=False)).astype(np.int32)
+        if t % 5 == 0:
+            kept = np.arange(n, dtype=np.int32)                # nothing evicted below n
+        elif t % 5 == 1:
+            kept = np.arange(L - n, L, dtype=np.int32)         # the tail only
+        order = oracle.fill_order(kept)
+        assert order.size == n
+        assert sorted(order.tolist()) == kept.tolist()
+        low = kept[kept < n]
+        assert np.array_equal(order[low], low)
+        holes = np.setdiff1d(np.arange(n), low)
+        assert np.all(np.diff(order[holes]) > 0)
+        assert np.all(order[holes] >= n)
+        moved = int(np.count_nonzero(order != np.arange(n)))
+        assert moved == holes.size <= L - n
+
+
+def test_fill_compaction_holds_the_ordered_rows_in_another_order():
+    """Both compactions keep the same rows: sorting the filled result by
+    source slot gives the order-preserving result.  The prefix below the
+    first eviction is untouched by both."""
+    rng = np.random.default_rng(22)
+    for _ in range(50):
+        L = int(rng.integers(2, 70))
+        B = int(rng.integers(1, L))
+        s = rng.random(L)
+        kept = oracle.select(s, B, min(B, 4))
+        rows = rng.integers(0, 2 ** 16, size=(L, 6), dtype=np.uint16)
+        ordered = oracle.compact(rows.copy(), kept)[: kept.size]
+        order = oracle.fill_order(kept)
+        filled = oracle.compact(rows.copy(), order)[: kept.size]
+        assert np.array_equal(filled, rows[order])
+        assert np.array_equal(filled[np.argsort(order, kind="stable")], ordered)
+        first = int(np.argmax(kept != np.arange(kept.size))) if np.any(kept != np.arange(kept.size)) \
+            else kept.size
+        assert np.array_equal(filled[:first], rows[:first])
+
+
+def test_fill_order_within_budget_is_identity():
+    s = np.random.default_rng(23).random(40)
+    kept = oracle.select(s, 64, 16)
+    assert np.array_equal(oracle.fill_order(kept), np.arange(40))
+
+
 def test_round_unit_tiny_workload_is_consistent():
     """A whole round on one unit of the tiny workload: the kept set holds
     the window, the compacted cache is the gather of the kept rows."""
