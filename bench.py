@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--e2e-max-gb", type=float, default=12.0,
                     help="largest host staging for the end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--compact", choices=["ordered", "fill"], default="ordered",
+                    help="compaction layout: slot order kept (the default) or hole-filling")
     return ap.parse_args()
 
 
@@ -86,7 +88,7 @@ def round_units(cfg, units_idx, seed=wl.SEED):
     return units
 
 
-def workload_desc(cfg, world):
+def workload_desc(cfg, world, compact="ordered"):
     return {
         "workload": f"{cfg.name}: {cfg.layers} layer(s) x {cfg.batch} seq x {cfg.kv_heads} KV "
                     f"heads per GPU, GQA {cfg.G}, d {cfg.d}, L {cfg.L} -> B_KV {cfg.B_KV}, "
@@ -95,18 +97,19 @@ def workload_desc(cfg, world):
         "parallelism": f"units sharded over {world} GPU(s)",
         "l2": "flushed (256 MiB write) and state restored before every timed step",
         "step": "bkv_round: fps_update (beacon select over C-1 items) + score + select_compact",
+        "compaction": compact,
     }
 
 
 # ------------------------------------------------------------ CPU oracle
 
 
-def oracle_round_time(cfg, units, n):
+def oracle_round_time(cfg, units, n, fill=False):
     import oracle
     t0 = time.perf_counter()
     for u in range(n):
         un = {k: (v[u] if getattr(v, "ndim", 0) else v) for k, v in units.items()}
-        oracle.round_unit(un, cfg.W, cfg.M, cfg.B_KV, cfg.Rw, cfg.theta, append=False)
+        oracle.round_unit(un, cfg.W, cfg.M, cfg.B_KV, cfg.Rw, cfg.theta, append=False, fill=fill)
     return time.perf_counter() - t0
 
 
@@ -118,19 +121,20 @@ def run_reference(args, rank, world):
         return
     cfg = cfg_of(args.config, args.M)
     units = round_units(cfg, range(8))
-    t1 = oracle_round_time(cfg, units, 1)  # also builds / loads the oracle
+    fill = args.compact == "fill"
+    t1 = oracle_round_time(cfg, units, 1, fill)  # also builds / loads the oracle
     budget = 120.0 / max(1, args.steps + args.warmup)
     n = int(max(1, min(8, budget // max(t1, 1e-3))))
     for _ in range(args.warmup):
-        oracle_round_time(cfg, units, 1)
-    times = [oracle_round_time(cfg, units, n) for _ in range(args.steps)]
+        oracle_round_time(cfg, units, 1, fill)
+    times = [oracle_round_time(cfg, units, n, fill) for _ in range(args.steps)]
     per_round = (sum(times) / len(times)) / n * cfg.U
     val = 1.0 / per_round
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_round * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded generator)", "config": workload_desc(cfg, 1),
+        "data": "synthetic (seeded generator)", "config": workload_desc(cfg, 1, args.compact),
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{n} of {cfg.U} units per step, single thread, scaled by unit count"},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -236,9 +240,10 @@ class ClockSampler:
 # ------------------------------------------------------------------ ours
 
 
-def workload_key(cfg):
-    """Name of a workload as run: its shape name, beacon count and unit count."""
-    return f"{cfg.name}:M{cfg.M}:U{cfg.U}"
+def workload_key(cfg, compact="ordered"):
+    """Name of a workload as run: its shape name, beacon count and unit count
+    (and ":fill" for the hole-filling compaction)."""
+    return f"{cfg.name}:M{cfg.M}:U{cfg.U}" + (":fill" if compact == "fill" else "")
 
 
 def kernel_source_sha(kernel_file):
@@ -311,7 +316,8 @@ def run_ours(args, rank, world):
     nb = torch.zeros(U, dtype=torch.int32, device=dev)
     scores = torch.zeros((U, cfg.L), dtype=torch.float32, device=dev)
     kept = torch.zeros((U, B), dtype=torch.int32, device=dev)
-    dims = bkv.Dims.from_config(cfg)
+    dims = bkv.Dims.from_config(cfg, compact=bkv.COMPACT_FILL if args.compact == "fill"
+                                else bkv.COMPACT_ORDERED)
     stream = torch.cuda.current_stream(dev)
     ws = bkv.make_workspace(dims, dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -451,7 +457,7 @@ def run_ours(args, rank, world):
     # split, the second pass and row padding are executed work, not counted)
     score_flops = U * 2.0 * (cfg.W + M) * cfg.G * Lr * d
     ridge = tfl * 1e12 / (hbm * 1e9)  # FLOP per byte where the two roofs meet
-    wkey = workload_key(cfg)
+    wkey = workload_key(cfg, args.compact)
     roofs = {}
     for k, n in enumerate(names):
         t = mean_ms[k] * 1e-3
@@ -475,7 +481,7 @@ def run_ours(args, rank, world):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded generator; stands in for Qwen3-4B AIME24/LiveCodeBench traces)",
-        "config": workload_desc(cfg, world),
+        "config": workload_desc(cfg, world, args.compact),
         "kv_gbs": world * kv_bytes * args.steps / (total_ms * 1e-3) / 1e9,
         "kernel_ms": {n: float(m) for n, m in zip(names, mean_ms)},
         "roofline": roofs[names[dom]],
@@ -492,9 +498,9 @@ def run_ours(args, rank, world):
         line["decode_cycle"] = cycle
     if not args.no_cpu_baseline and world == 1:
         # the oracle on a bounded sample of the same units (about 20 s), scaled
-        t1 = oracle_round_time(cfg, host_units, 1)
+        t1 = oracle_round_time(cfg, host_units, 1, args.compact == "fill")
         n = int(max(1, min(pool, U, round(20.0 / max(t1, 1e-3)))))
-        secs = oracle_round_time(cfg, host_units, n)
+        secs = oracle_round_time(cfg, host_units, n, args.compact == "fill")
         line["cpu_baseline"] = {"value": 1.0 / (secs / n * U), "unit": UNIT, "cores": 1,
                                 "kind": "oracle",
                                 "sample": f"{n} of {U} units, single thread, scaled by unit count"}

@@ -85,12 +85,19 @@ enum { BKV_AGG_MAX = 0, BKV_AGG_MEAN = 1 };
  *                  the buffer keeping its first M items when it fills (the
  *                  InitialRecent comparison of the BeaconKV pages: initial
  *                  queries plus the recent window)
+ *   compact        BKV_COMPACT_ORDERED (0): the kept rows in slot order;
+ *                  BKV_COMPACT_FILL (1): order-free, kept rows below the
+ *                  new length stay and the holes there take the kept rows
+ *                  past it (moves at most L - B_KV rows; see
+ *                  bkv_select_compact)
  *   rope_theta     rotary base (rotate-half pairs (i, i + d/2),
  *                  frequency theta^(-2i/d))
  * Limits: (W + M) * G <= 1024 scoring rows; positions < 2^24.
  */
 #define BKV_BEACONS_FPS 0
 #define BKV_BEACONS_FIRST 1
+#define BKV_COMPACT_ORDERED 0
+#define BKV_COMPACT_FILL 1
 
 typedef struct bkv_dims {
   int32_t U, G, d, W, M, C, B_KV, R;
@@ -98,6 +105,7 @@ typedef struct bkv_dims {
   int32_t agg;
   int32_t causal_recent;
   int32_t beacon_select; /* BKV_BEACONS_FPS (the method) or BKV_BEACONS_FIRST */
+  int32_t compact;       /* BKV_COMPACT_ORDERED (default) or BKV_COMPACT_FILL */
   double rope_theta;
 } bkv_dims;
 
@@ -175,14 +183,24 @@ int bkv_score(const bkv_dims* dims, const void* K, const int32_t* L, const int32
  *   K, V       [U][L_cap][d] bf16, compacted in place
  *   kpos       [U][L_cap] int32, compacted in place
  *   L          [U] int32 in: lengths; out: min(L, B_KV)
- *   kept       [U][B_KV] int32 or NULL: kept slots in ascending order,
- *              -1 past the new length
+ *   kept       [U][B_KV] int32 or NULL: the source slot of each row after
+ *              compaction (BKV_COMPACT_ORDERED: the kept slots in ascending
+ *              order), -1 past the new length
  *
  * If L <= B_KV nothing moves.  Else the last R slots are kept, plus the
  * B_KV - R highest-scoring of the other L - R slots (equal scores: the lower
- * slot wins; -0.0 counts as +0.0; scores must not be NaN); slot order is
- * preserved, so row i takes the row of the i-th kept slot, for K, V and
- * kpos alike.
+ * slot wins; -0.0 counts as +0.0; scores must not be NaN).  Rows of K, V and
+ * kpos move alike; with n = B_KV kept:
+ *   BKV_COMPACT_ORDERED  slot order is preserved: row i takes the row of the
+ *                        i-th kept slot;
+ *   BKV_COMPACT_FILL     a kept slot below n keeps its row, and the slots
+ *                        below n that are not kept, in ascending order, take
+ *                        the kept slots at or past n, in ascending order.  At
+ *                        most L - n rows move.  Attention over the cache is
+ *                        order-free (kpos carries each row's position), so
+ *                        the row order is a layout choice; the BeaconKV pages
+ *                        fix only the kept set (inkeast.github.io reading,
+ *                        section 三).
  */
 int bkv_select_compact(const bkv_dims* dims, const float* scores, void* K, void* V,
                        int32_t* kpos, int32_t* L, int32_t* kept, void* workspace,

@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libbkv.so")
 OK, EINVAL, ECUDA, ETIMEOUT, EDEVICE, EUNSUPPORTED = 0, -1, -2, -3, -4, -5
 AGG_MAX, AGG_MEAN = 0, 1
 BEACONS_FPS, BEACONS_FIRST = 0, 1
+COMPACT_ORDERED, COMPACT_FILL = 0, 1
 
 
 class BkvError(RuntimeError):
@@ -29,18 +30,18 @@ class Dims(ctypes.Structure):
 
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("U", "G", "d", "W", "M", "C", "B_KV", "R", "L_cap", "agg",
-                 "causal_recent", "beacon_select")] + [("rope_theta", ctypes.c_double)]
+                 "causal_recent", "beacon_select", "compact")] + [("rope_theta", ctypes.c_double)]
 
     @classmethod
     def make(cls, U, G, d, W, M, C, B_KV, R, L_cap, rope_theta, agg=AGG_MAX, causal_recent=1,
-             beacon_select=0):
-        return cls(U, G, d, W, M, C, B_KV, R, L_cap, agg, causal_recent, beacon_select,
+             beacon_select=0, compact=COMPACT_ORDERED):
+        return cls(U, G, d, W, M, C, B_KV, R, L_cap, agg, causal_recent, beacon_select, compact,
                    float(rope_theta))
 
     @classmethod
-    def from_config(cls, cfg, U=None, agg=AGG_MAX, beacon_select=0):
+    def from_config(cls, cfg, U=None, agg=AGG_MAX, beacon_select=0, compact=COMPACT_ORDERED):
         return cls.make(cfg.U if U is None else U, cfg.G, cfg.d, cfg.W, cfg.M, cfg.C, cfg.B_KV,
-                        cfg.Rw, cfg.L, cfg.theta, agg, 1, beacon_select)
+                        cfg.Rw, cfg.L, cfg.theta, agg, 1, beacon_select, compact)
 
 
 if not os.path.exists(LIB_PATH):

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -19,6 +20,10 @@ namespace {
 
 using bkv::WsHeader;
 
+// The binding mirrors this layout (13 int32 fields, then the double).
+static_assert(offsetof(bkv_dims, rope_theta) == 56 && sizeof(bkv_dims) == 64,
+              "bkv_dims layout");
+
 constexpr int kMaxSmem = 232448;  // bytes of shared memory a CTA may opt into on sm_103
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -33,6 +38,7 @@ int validate(const bkv_dims* d) {
   if (d->agg != BKV_AGG_MAX && d->agg != BKV_AGG_MEAN) return BKV_EINVAL;
   if (d->causal_recent != 0 && d->causal_recent != 1) return BKV_EINVAL;
   if (d->beacon_select != BKV_BEACONS_FPS && d->beacon_select != BKV_BEACONS_FIRST) return BKV_EINVAL;
+  if (d->compact != BKV_COMPACT_ORDERED && d->compact != BKV_COMPACT_FILL) return BKV_EINVAL;
   if (!(d->rope_theta > 1.0) || !std::isfinite(d->rope_theta)) return BKV_EINVAL;
   if (d->W + d->M < 1 || (d->W + d->M) * d->G > 1024) return BKV_EINVAL;
   if (static_cast<int64_t>(d->U) * d->L_cap * d->d >= (int64_t(1) << 40)) return BKV_EINVAL;
@@ -300,6 +306,7 @@ int select_prepare(const bkv_dims* dims, const float* scores, void* K, void* V, 
   p.ncl = select_cluster_size(dims->U);
   p.nbufs = nbufs;
   p.buf_bytes = buf_bytes;
+  p.fill = dims->compact == BKV_COMPACT_FILL ? 1 : 0;
   return BKV_OK;
 }
 

@@ -53,6 +53,7 @@ struct SelectParams {
   int32_t ncl;    // CTAs (one cluster) per unit, 1..8
   int32_t nbufs;      // wave buffers in the ring, 3..8
   int32_t buf_bytes;  // bytes of one wave buffer (32768 or 16384)
+  int32_t fill;       // 1: hole-filling (order-free) compaction
 };
 
 cudaError_t launch_select_compact(const SelectParams& p, cudaStream_t st);

@@ -250,6 +250,79 @@ __device__ int select_kept(const SelectParams& p, const float* sc, const uint32_
   return n_kept;
 }
 
+// Hole-filling (order-free) compaction of unit u, whose n = n_kept kept
+// slots are kept_s[0, n) in ascending order: a kept slot below n keeps its
+// row, and the slots below n that are not kept (the holes), ascending, take
+// the kept slots at or past n, ascending.  Sources lie at or past n and
+// destinations below it, so the copies need no order among themselves and
+// no staging: every CTA of the cluster copies its share of the (hole,
+// source) pairs with 16-byte loads and stores, four per thread in flight.
+// `hole` holds up to n entries, `bits` up to n bits.
+__device__ void fill_compact(const SelectParams& p, int u, int rank, int ncl, int n,
+                             const int32_t* kept_s, int32_t* hole, uint32_t* bits, Smem* sm,
+                             int32_t* kp, uint8_t* Kb, uint8_t* Vb, uint32_t rb) {
+  const int tid = threadIdx.x;
+  const int nwords = (n + 31) >> 5;
+  for (int w = tid; w < nwords; w += kThreads) bits[w] = 0u;
+  int below = 0;  // kept slots below n: a prefix of the ascending list
+  for (int j = tid; j < n; j += kThreads) below += kept_s[j] < n ? 1 : 0;
+  const int c = block_sum(below, sm->warp_tot);  // its barriers also publish the zeroed bits
+  for (int j = tid; j < c; j += kThreads) atomicOr(&bits[kept_s[j] >> 5], 1u << (kept_s[j] & 31));
+  __syncthreads();
+  // ascending hole list: thread t takes words [t wpt, (t + 1) wpt) of the map
+  auto hole_bits = [&](int w) {
+    uint32_t m = ~bits[w];
+    const int valid = n - 32 * w;  // slots of this word below n
+    return valid < 32 ? m & ((1u << valid) - 1u) : m;
+  };
+  const int wpt = (nwords + kThreads - 1) / kThreads;
+  const int w0 = min(nwords, tid * wpt), w1 = min(nwords, w0 + wpt);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(hole_bits(w));
+  int pos = block_incl_scan(cnt, sm->warp_tot) - cnt;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t m = hole_bits(w);
+    while (m != 0u) {
+      hole[pos++] = 32 * w + __ffs(m) - 1;
+      m &= m - 1u;
+    }
+  }
+  __syncthreads();
+  const int h = n - c;  // holes = kept slots at or past n
+  if (rank == 0 && p.kept != nullptr) {  // the source slot of every row
+    int32_t* ko = p.kept + static_cast<size_t>(u) * p.B;
+    for (int i = tid; i < p.B; i += kThreads) ko[i] = i < n ? i : -1;
+    __syncthreads();
+    for (int k = tid; k < h; k += kThreads) ko[hole[k]] = kept_s[c + k];
+  }
+  const int k0 = static_cast<int>(static_cast<int64_t>(h) * rank / ncl);
+  const int k1 = static_cast<int>(static_cast<int64_t>(h) * (rank + 1) / ncl);
+  for (int k = k0 + tid; k < k1; k += kThreads) kp[hole[k]] = kp[kept_s[c + k]];
+  // element e of this CTA's pairs: pair k0 + e / per_pair, 16-byte piece
+  // e % per_pair (K pieces first, then V)
+  const int ppr = static_cast<int>(rb / 16);
+  const int per_pair = 2 * ppr;
+  const int total = (k1 - k0) * per_pair;
+  for (int e0 = tid; e0 < total; e0 += 4 * kThreads) {
+    uint4 v[4];
+    uint8_t* dst[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = e0 + q * kThreads;
+      const int ec = e < total ? e : total - 1;  // clamped: a valid address, store skipped
+      const int k = k0 + ec / per_pair, pc = ec % per_pair;
+      const bool is_v = pc >= ppr;
+      const size_t off = static_cast<size_t>(is_v ? pc - ppr : pc) * 16;
+      uint8_t* base = is_v ? Vb : Kb;
+      v[q] = *reinterpret_cast<const uint4*>(base + static_cast<size_t>(kept_s[c + k]) * rb + off);
+      dst[q] = e < total ? base + static_cast<size_t>(hole[k]) * rb + off : nullptr;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (dst[q] != nullptr) *reinterpret_cast<uint4*>(dst[q]) = v[q];
+  }
+}
+
 __global__ void __launch_bounds__(kThreads)
     select_compact_kernel(const __grid_constant__ SelectParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -323,6 +396,14 @@ __global__ void __launch_bounds__(kThreads)
     if (kept_s[i] != i) atomicMin(&sm->first, i);
   __syncthreads();  // the keys in the ring are dead from here on
   const int first = min(sm->first, n_kept);
+
+  if (p.fill) {
+    fill_compact(p, u, rank, ncl, n_kept, kept_s, kpn, reinterpret_cast<uint32_t*>(bufs), sm, kp,
+                 p.K + ubase * rb, p.V + ubase * rb, rb);
+    cluster_sync();  // every CTA of the unit has read L and finished its copies
+    if (rank == 0 && tid == 0 && valid) p.L[u] = n_kept;
+    return;
+  }
 
   if (rank == 0 && p.kept != nullptr)
     for (int i = tid; i < p.B; i += kThreads)

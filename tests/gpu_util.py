@@ -47,7 +47,8 @@ def kept_sets_agree(kept_gpu, scores_ref, B, R, L):
 class DeviceState:
     """Device copies of a stack of units (as made by workload.make_units)."""
 
-    def __init__(self, units, cfg, L_cap=None, agg=bkv.AGG_MAX, causal=1, beacon_select=0):
+    def __init__(self, units, cfg, L_cap=None, agg=bkv.AGG_MAX, causal=1, beacon_select=0,
+                 compact=0):
         self.cfg = cfg
         U = units["K"].shape[0]
         self.U = U
@@ -72,7 +73,7 @@ class DeviceState:
         self.scores = torch.full((U, self.L_cap), -1.0, dtype=torch.float32, device=DEV)
         self.kept = torch.zeros((U, cfg.B_KV), dtype=torch.int32, device=DEV)
         self.dims = bkv.Dims.make(U, G, d, cfg.W, M, cfg.C, cfg.B_KV, cfg.Rw, self.L_cap,
-                                  cfg.theta, agg, causal, beacon_select)
+                                  cfg.theta, agg, causal, beacon_select, compact)
         self.ws = bkv.make_workspace(self.dims, DEV)
 
     def fps(self, with_append=True, want_beacons=True):

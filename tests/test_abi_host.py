@@ -68,6 +68,21 @@ def test_beacon_select_must_be_known():
         assert bkv.raw("bkv_workspace_size")(ctypes.byref(d), ctypes.byref(n)) == rc
 
 
+def test_compact_mode_must_be_known():
+    n = ctypes.c_size_t(0)
+    for v, rc in ((0, bkv.OK), (1, bkv.OK), (2, bkv.EINVAL), (-1, bkv.EINVAL)):
+        d = _dims()
+        d.compact = v
+        assert bkv.raw("bkv_workspace_size")(ctypes.byref(d), ctypes.byref(n)) == rc
+
+
+def test_dims_mirror_matches_the_header_layout():
+    """The ctypes mirror puts rope_theta after the 13 int32 fields, at the
+    8-byte boundary the C struct uses."""
+    assert bkv.Dims.rope_theta.offset == 56
+    assert ctypes.sizeof(bkv.Dims) == 64
+
+
 def test_large_buffer_capacity_reported_unsupported():
     d = _dims(C=513)
     n = ctypes.c_size_t(0)

@@ -73,6 +73,38 @@ def test_select_compact_bit_exact(d, L_cap, B, R):
         assert np.array_equal(pg[u, :n], kpos[u][ref])
 
 
+@pytest.mark.parametrize("d,L_cap,B,R", [(128, 2176, 2048, 16), (64, 512, 128, 16),
+                                         (128, 1000, 300, 0), (128, 700, 64, 64),
+                                         (128, 33000, 2048, 16), (128, 16500, 16384, 16)])
+def test_select_compact_fill_bit_exact(d, L_cap, B, R):
+    """Hole-filling compaction: every row, kpos entry and source slot as the
+    oracle's fill order gives them, rows past the new length untouched."""
+    rng = np.random.default_rng(7 * d + L_cap + B + R)
+    U = 9
+    Ls = [L_cap, B, B + 1, max(0, B - 5), 0, L_cap - 1, min(L_cap, B + 129), R, L_cap]
+    scores, K, V, kpos, L = _select_case(rng, U, d, L_cap, B, R, Ls)
+    dims = bkv.Dims.make(U, 1, d, 16, 16, 64, B, R, L_cap, 1e4, compact=bkv.COMPACT_FILL)
+    ws = bkv.make_workspace(dims)
+    tK, tV, tp, tL, ts = dev(K), dev(V), dev(kpos), dev(L), dev(scores)
+    kept = torch.zeros((U, B), dtype=torch.int32, device="cuda")
+    bkv.select_compact(dims, ts, tK, tV, tp, tL, kept, ws)
+    assert bkv.get_status(ws) == 0
+    Kg, Vg, pg, Lg, kg = host_u16(tK), host_u16(tV), tp.cpu().numpy(), tL.cpu().numpy(), \
+        kept.cpu().numpy()
+    for u in range(U):
+        order = oracle.fill_order(oracle.select(scores[u].astype(np.float64), B, R, int(L[u])))
+        n = order.size
+        assert Lg[u] == n
+        assert np.array_equal(kg[u, :n], order)
+        assert np.all(kg[u, n:] == -1)
+        ref_K = oracle.compact(K[u].copy(), order)
+        ref_V = oracle.compact(V[u].copy(), order)
+        ref_p = oracle.compact(kpos[u].copy(), order)
+        assert np.array_equal(Kg[u], ref_K)   # rows past n keep what they held
+        assert np.array_equal(Vg[u], ref_V)
+        assert np.array_equal(pg[u], ref_p)
+
+
 def test_select_compact_dense_eviction_and_repeat():
     """Keep a small fraction of a long cache (most rows move far), twice in
     a row on the same workspace."""
@@ -287,7 +319,7 @@ def test_fps_exact_ties_and_zero_vectors(cid):
 # ------------------------------------------------------------ whole round
 
 
-def _round_parity(cfg, units, st, append=True, one_call=False, first_m=False):
+def _round_parity(cfg, units, st, append=True, one_call=False, first_m=False, fill=False):
     if one_call:
         st.round(with_append=append)
     else:
@@ -301,7 +333,7 @@ def _round_parity(cfg, units, st, append=True, one_call=False, first_m=False):
     for u in range(st.U):
         un = _unit(units, u)
         ref = oracle.round_unit(un, cfg.W, cfg.M, cfg.B_KV, cfg.Rw, cfg.theta, append=append,
-                                first_m=first_m)
+                                first_m=first_m, fill=fill)
         nbr = len(ref["beacon_idx"])
         assert np.array_equal(st.bidx[u].cpu().numpy()[:nbr], ref["beacon_idx"]), u
         # after a compress the beacon slots are trivially 0..M-1: the buffer
@@ -317,8 +349,9 @@ def _round_parity(cfg, units, st, append=True, one_call=False, first_m=False):
         worst = max(worst, score_tol_excess(sg[u, :L0], ref["scores"]))
         kept = st.kept[u].cpu().numpy()
         n = min(L0, cfg.B_KV)
-        assert np.array_equal(kept[:n], oracle.select(sg[u, :L0], cfg.B_KV, cfg.Rw))
-        assert kept_sets_agree(kept[:n], ref["scores"], cfg.B_KV, cfg.Rw, L0)
+        sel = oracle.select(sg[u, :L0], cfg.B_KV, cfg.Rw)
+        assert np.array_equal(kept[:n], oracle.fill_order(sel) if fill else sel)
+        assert kept_sets_agree(np.sort(kept[:n]), ref["scores"], cfg.B_KV, cfg.Rw, L0)
         assert np.array_equal(host_u16(st.K[u])[:n], un["K"][kept[:n]])
         assert np.array_equal(host_u16(st.V[u])[:n], un["V"][kept[:n]])
         assert np.array_equal(st.kpos[u].cpu().numpy()[:n], un["kpos"][kept[:n]])
@@ -359,6 +392,16 @@ def test_round_parity_first_m_beacons(cid, nunits):
     units = wl.make_units(cfg, range(cfg.U if nunits is None else nunits))
     st = DeviceState(units, cfg, beacon_select=bkv.BEACONS_FIRST)
     _round_parity(cfg, units, st, first_m=True)
+
+
+@pytest.mark.parametrize("cid,nunits", [(1, None), (2, None), (5, 2)])
+def test_round_parity_fill_compaction(cid, nunits):
+    """A whole round with hole-filling compaction (bkv_round), against the
+    oracle's round with the same layout."""
+    cfg = wl.CONFIGS[cid]
+    units = wl.make_units(cfg, range(cfg.U if nunits is None else nunits))
+    st = DeviceState(units, cfg, compact=bkv.COMPACT_FILL)
+    _round_parity(cfg, units, st, one_call=True, fill=True)
 
 
 def test_round_call_parity_bench_round_full():
