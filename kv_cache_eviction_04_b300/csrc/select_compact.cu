@@ -41,6 +41,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxBufs = 8;             // ring of wave buffers (count set by the host)
 constexpr uint32_t kBufBig = 32768;     // bytes of one wave of one CTA (RS rows of K and V)
 constexpr uint32_t kBufSmall = 16384;   // the same when a very large B_KV leaves less room
+constexpr int kFillAhead = 16;          // 16-byte loads per thread in flight (hole-filling copy)
 
 __device__ __forceinline__ uint32_t order_key(float s) {
   uint32_t u = __float_as_uint(s);
@@ -256,7 +257,8 @@ __device__ int select_kept(const SelectParams& p, const float* sc, const uint32_
 // the kept slots at or past n, ascending.  Sources lie at or past n and
 // destinations below it, so the copies need no order among themselves and
 // no staging: every CTA of the cluster copies its share of the (hole,
-// source) pairs with 16-byte loads and stores, four per thread in flight.
+// source) pairs with 16-byte loads and stores, kFillAhead per thread in
+// flight (the copy is bound by the bytes each SM keeps in flight).
 // `hole` holds up to n entries, `bits` up to n bits.
 __device__ void fill_compact(const SelectParams& p, int u, int rank, int ncl, int n,
                              const int32_t* kept_s, int32_t* hole, uint32_t* bits, Smem* sm,
@@ -303,11 +305,11 @@ __device__ void fill_compact(const SelectParams& p, int u, int rank, int ncl, in
   const int ppr = static_cast<int>(rb / 16);
   const int per_pair = 2 * ppr;
   const int total = (k1 - k0) * per_pair;
-  for (int e0 = tid; e0 < total; e0 += 4 * kThreads) {
-    uint4 v[4];
-    uint8_t* dst[4];
+  for (int e0 = tid; e0 < total; e0 += kFillAhead * kThreads) {
+    uint4 v[kFillAhead];
+    uint8_t* dst[kFillAhead];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kFillAhead; ++q) {
       const int e = e0 + q * kThreads;
       const int ec = e < total ? e : total - 1;  // clamped: a valid address, store skipped
       const int k = k0 + ec / per_pair, pc = ec % per_pair;
@@ -318,11 +320,15 @@ __device__ void fill_compact(const SelectParams& p, int u, int rank, int ncl, in
       dst[q] = e < total ? base + static_cast<size_t>(hole[k]) * rb + off : nullptr;
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < kFillAhead; ++q)
       if (dst[q] != nullptr) *reinterpret_cast<uint4*>(dst[q]) = v[q];
   }
 }
 
+// kFill: the hole-filling compaction (p.fill), a separate instantiation so
+// that its copy loop's registers do not lower the occupancy of the
+// order-preserving one.
+template <bool kFill>
 __global__ void __launch_bounds__(kThreads)
     select_compact_kernel(const __grid_constant__ SelectParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -397,7 +403,7 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();  // the keys in the ring are dead from here on
   const int first = min(sm->first, n_kept);
 
-  if (p.fill) {
+  if constexpr (kFill) {
     fill_compact(p, u, rank, ncl, n_kept, kept_s, kpn, reinterpret_cast<uint32_t*>(bufs), sm, kp,
                  p.K + ubase * rb, p.V + ubase * rb, rb);
     cluster_sync();  // every CTA of the unit has read L and finished its copies
@@ -574,7 +580,8 @@ size_t select_smem_bytes(int B, int nbufs, int buf_bytes) {
 
 cudaError_t launch_select_compact(const SelectParams& p, cudaStream_t st) {
   const size_t smem = select_smem_bytes(p.B, p.nbufs, p.buf_bytes);
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(select_compact_kernel), smem);
+  auto* kernel = p.fill ? select_compact_kernel<true> : select_compact_kernel<false>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(p.U * p.ncl));
@@ -592,7 +599,7 @@ cudaError_t launch_select_compact(const SelectParams& p, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, select_compact_kernel, p);
+  e = cudaLaunchKernelEx(&cfg, kernel, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
