@@ -23,13 +23,18 @@
 // Compaction (row i <- row kept[i], kept[i] >= i) runs in waves over the
 // rows that move, [first, n_kept): wave w covers ncl consecutive slices of
 // RS rows, one per CTA.  Each CTA gathers its slice's source rows of K and V
-// into a shared-memory ring with 16-byte cp.async copies spread over all its
-// threads, the cluster meets at a hardware barrier once every CTA's copies
-// of the wave have landed, and only then is each slice stored back (two TMA
-// bulk stores of contiguous rows).  Sources of a wave lie at or above its
-// first row, so stores of earlier waves never touch them, and a wave's
-// stores wait for all of its loads: in-place compaction needs no second
-// buffer and no spin-wait between CTAs.  Loads run nbufs - 2 waves ahead.
+// into a shared-memory ring (TMA bulk copies per run of consecutive source
+// rows when the unit's sources are dense, else 16-byte cp.async copies
+// spread over all its threads), the cluster meets at a hardware barrier
+// once every CTA's copies of the wave have landed, and only then is each
+// slice stored back (two TMA bulk stores of contiguous rows).  Sources of a
+// wave lie at or above its first row, so stores of earlier waves never
+// touch them, and a wave's stores wait for all of its loads: in-place
+// compaction needs no second buffer and no spin-wait between CTAs.  Loads
+// run nbufs - 2 waves ahead.
+// The hole-filling mode (an order-free layout: the holes below the new
+// length take the kept rows past it) replaces the waves with direct copies
+// of (hole, source) pairs; see fill_compact.
 #include "common.cuh"
 #include "kernels.h"
 
