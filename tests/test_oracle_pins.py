@@ -412,6 +412,14 @@ def test_fill_compaction_holds_the_ordered_rows_in_another_order():
         assert np.array_equal(filled[:first], rows[:first])
 
 
+def test_fill_order_golden_hand_example():
+    lines = [l for l in open(os.path.join(GOLDEN, "fill_order_hand_example.txt"))
+             if not l.startswith("#") and l.strip()]
+    kept = np.array(lines[0].split(":")[1].split(), dtype=np.int32)
+    want = [int(v) for v in lines[1].split(":")[1].split()]
+    assert oracle.fill_order(kept).tolist() == want
+
+
 def test_fill_order_within_budget_is_identity():
     s = np.random.default_rng(23).random(40)
     kept = oracle.select(s, 64, 16)
