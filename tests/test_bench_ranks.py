@@ -55,3 +55,19 @@ def test_reference_arm_under_torchrun_two_ranks():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_names_the_compaction_layout():
+    """--compact fill times the oracle's hole-filling round and says so in
+    the line's config; the default line names the order-preserving layout."""
+    for flag, want in ((["--compact", "fill"], "fill"), ([], "ordered")):
+        cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0",
+               "--config", "1"] + flag
+        r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        rec = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+        assert rec["config"]["compaction"] == want and rec["value"] > 0
+    sys.path.insert(0, ROOT)
+    import bench
+    cfg = bench.cfg_of(2, None)
+    assert bench.workload_key(cfg, "fill") == bench.workload_key(cfg) + ":fill"
