@@ -27,8 +27,11 @@
  *
  * Conventions
  *   - All pointers are DEVICE pointers owned by the caller.  The library
- *     keeps no state between calls and allocates no device memory; scratch
- *     lives in a caller-allocated workspace (see bkv_workspace_size).
+ *     allocates no device memory and keeps no state between calls; scratch
+ *     lives in a caller-allocated workspace (see bkv_workspace_size).  The
+ *     one exception is bkv_score_noalloc, whose scratch is a fixed array in
+ *     the library's own device memory: calls sharing that array must be
+ *     ordered (see its declaration below).
  *   - bf16 arrays are raw 16-bit patterns.  Every array is dense, unit-major.
  *   - Every call only enqueues work on `stream` and returns; nothing
  *     synchronises except bkv_get_status.
@@ -143,6 +146,12 @@ int bkv_workspace_init(void* workspace, size_t bytes, bkv_stream_t stream);
  * bf16 inputs with exact products and error-free sums (~2^-44 relative), and
  * identical items tie exactly (lowest slot).  Requires a workspace of
  * bkv_workspace_size(dims) bytes.
+ *
+ * BeaconKV pages: the wzjinhao.cn explainer, section "怎么挑出这几个信标：一种叫
+ * FPS的采样算法" (seed = the query least similar on average to the others,
+ * then the query farthest from the chosen set; a bounded per-head buffer
+ * of pre-RoPE queries, FPS-compressed when it fills), and the aimodeling.com
+ * article, section "用信标 query 预判" (16 beacons by default).
  */
 int bkv_fps_update(const bkv_dims* dims, const void* q_new, int64_t step, void* recent_q,
                    void* buf, int32_t* cnt, int32_t want_beacons, int32_t* beacon_idx,
@@ -170,6 +179,13 @@ int bkv_fps_update(const bkv_dims* dims, const void* q_new, int64_t step, void* 
  * r sees.  score_j = max_r P_r(j) (BKV_AGG_MAX) or the mean over rows.
  * Accuracy: |score - exact| <= 1e-6 + 2e-3 |exact| (fp32 accumulation of
  * bf16 products, queries carried as a two-term bf16 split).
+ *
+ * BeaconKV pages: the wzjinhao.cn explainer, section "信标查询怎么用：位置对齐与
+ * 打分策略" (beacons re-rotated to the current position, recent queries at
+ * their own positions, max over queries beats the mean), and the
+ * inkeast.github.io reading, section 三 (score(K, V) from the union of the
+ * recent and beacon queries).  M = 0 is recent-only scoring, the RPC
+ * comparison on the same pages.
  */
 int bkv_score(const bkv_dims* dims, const void* K, const int32_t* L, const int32_t* kpos,
               const void* recent_q, int64_t step, const void* beacons,

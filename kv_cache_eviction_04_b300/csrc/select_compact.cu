@@ -498,6 +498,7 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
   bool failed = false;  // block-uniform
+  int failed_at = nw;    // first wave whose gather never landed
   // New kpos of every row this CTA writes, gathered while those gathers fly
   // and before the first wave's barrier (no CTA writes kpos before it);
   // entry w * RS + t = wave w, row t.
@@ -528,7 +529,10 @@ __global__ void __launch_bounds__(kThreads)
     // A wave that never lands stops the copies but not the loop: every CTA
     // of the cluster still meets at each of its barriers.
     const bool landed = __syncthreads_and(here);
-    if (!landed && !failed && tid == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteSelectWait);
+    if (!landed && !failed) {
+      if (tid == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteSelectWait);
+      failed_at = w;
+    }
     failed = failed || !landed;
     int r0, cnt;
     slice(w, r0, cnt);
@@ -548,6 +552,14 @@ __global__ void __launch_bounds__(kThreads)
   }
   cp_async_wait<0>();
   if (tid == 0) bulk_wait<0>();
+  // After a gather that never landed no further wave was issued, but waves
+  // failed_at .. failed_at + kAhead may still have bulk loads in flight into
+  // this CTA's shared memory: wait for them (bounded) before the CTA exits.
+  // A wave that still has not landed then is left in flight; its error is
+  // already recorded.
+  if (use_tma && failed && tid == 0)
+    for (int w = failed_at; w < min(nw, failed_at + kAhead + 1); ++w)
+      wait_bar(&sm->wbar[w % nbufs], (w / nbufs) & 1);
   cluster_sync();  // every CTA of the unit has read L and finished its copies
   if (rank == 0 && tid == 0 && valid) p.L[u] = n_kept;
 }
