@@ -52,8 +52,8 @@ def parse():
     ap.add_argument("--units", type=int, default=None,
                     help="run only this many units of the workload (same per-unit shape); "
                          "for small profiling captures of the large workloads")
-    ap.add_argument("--cycle", action="store_true",
-                    help="also time a 128-step decode cycle (appends + compress + round)")
+    ap.add_argument("--no-cycle", action="store_true",
+                    help="skip the 128-step decode cycle (appends + compress + round)")
     ap.add_argument("--e2e-max-gb", type=float, default=12.0,
                     help="largest host staging for the end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -429,7 +429,7 @@ def run_ours(args, rank, world):
                "d2h_bytes_per_step": int(d2h)}
 
     cycle = run_cycle(args, cfg, dims, pristine, work, cur, step, bidx, beac, nb, scores, kept,
-                      ws, stream, restore) if args.cycle else None
+                      ws, stream, restore) if not args.no_cycle else None
 
     if rank != 0:
         return
@@ -519,7 +519,7 @@ def run_cycle(args, cfg, dims, pristine, work, cur, step, bidx, beac, nb, scores
     g = torch.Generator(device=cur.device).manual_seed(0xC1C1E)
     qs = [(torch.randn((cfg.U, cfg.G, cfg.d), device=cur.device, generator=g) * 3.0)
           .to(torch.bfloat16).view(torch.int16) for _ in range(128)]
-    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
 
     def cycle_once():
         restore()
@@ -527,6 +527,8 @@ def run_cycle(args, cfg, dims, pristine, work, cur, step, bidx, beac, nb, scores
         for t in range(128):
             bkv.fps_update(dims, qs[t], step + 1 + t, work["ring"], work["buf"], work["cnt"],
                            False, None, None, None, ws, stream)
+            if t == 0:
+                e[3].record(stream)  # after the append that compresses every buffer
         e[1].record(stream)
         s2 = step + 128
         bkv.fps_update(dims, None, s2, work["ring"], work["buf"], work["cnt"], True, bidx, beac,
@@ -537,7 +539,7 @@ def run_cycle(args, cfg, dims, pristine, work, cur, step, bidx, beac, nb, scores
                            stream)
         e[2].record(stream)
         e[2].synchronize()
-        return e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])
+        return e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[3].elapsed_time(e[1])
 
     cycle_once()
     reps = [cycle_once() for _ in range(max(2, min(args.steps, 5)))]
@@ -545,9 +547,22 @@ def run_cycle(args, cfg, dims, pristine, work, cur, step, bidx, beac, nb, scores
         raise RuntimeError("device status set during the decode cycle")
     app = float(np.median([r[0] for r in reps]))
     rnd = float(np.median([r[1] for r in reps]))
+    steady = float(np.median([r[2] for r in reps])) / 127  # an append that fills no buffer
+    # per-step appends of C <= 256 buffers run as two launches (the append,
+    # then the compress of the buffers it filled); larger buffers as one
+    per_append = 2 if cfg.C <= 256 else 1
     return {"what": "128 appends (first one compresses every buffer) + one eviction round",
             "ms": app + rnd, "appends_ms": app, "round_ms": rnd, "cycles_per_s": 1e3 / (app + rnd),
-            "launches": 128 + 4}
+            "compress_burst_ms": app - 127 * steady, "steady_append_ms": steady,
+            "steady_append_gbs": append_bytes(cfg) / (steady * 1e-3) / 1e9,
+            "launches": 128 * per_append + 3}
+
+
+def append_bytes(cfg):
+    """Algorithmic bytes of one per-step append: the step's query read once
+    and written to the ring and to the buffer, plus the count read and
+    written (2 U G d 2 of copies, 3 U G d 2 with the read)."""
+    return cfg.U * (3 * cfg.D * 2 + 8)
 
 
 def main():

@@ -351,6 +351,10 @@ int bkv_fps_update(const bkv_dims* dims, const void* q_new, int64_t step, void* 
                             beacons, n_beacons, workspace, &p, &map, &cluster);
   if (v != BKV_OK) return v;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // A decode step that selects no beacons appends with a light copy kernel
+  // and compresses only the buffers that step filled.
+  if (q_new != nullptr && want_beacons == 0 && !cluster)
+    return cuda_rc(bkv::launch_fps_append_compress(p, map, sm_count(), st));
   return cuda_rc(cluster ? bkv::launch_fps_cluster(p, map, st) : bkv::launch_fps(p, map, st));
 }
 

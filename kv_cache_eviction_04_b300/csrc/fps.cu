@@ -71,6 +71,8 @@ struct __align__(16) FpsShared {
   double pair64[kMaxPairs];
   int16_t pair_a[kMaxPairs];  // item of a pair's contender
   int16_t pair_s[kMaxPairs];  // its chosen item
+  int32_t ulist[kItems];      // compress pass: full units of the current batch
+  int32_t ucount;
 };
 
 // Barrier of the eight item warps only (the producer warp idles after the
@@ -348,7 +350,10 @@ __device__ void fps_pick(const FpsParams& p, const CUtensorMap* bmap, FpsShared*
       item_sync();
       seed = sh->winner;
     } else if (tid == 0) {
+      // a chunk that never landed: later chunks' copies may still be in
+      // flight, so the CTA takes on no further unit
       record_error(p.ws, BKV_ETIMEOUT, kSiteFpsWait);
+      sh->abort_flag = 1;
     }
   }
 
@@ -572,6 +577,70 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   return m;
 }
 
+// The CTA's mbarriers and abort flag (thread 0).  With `again` the words
+// were initialised before: every wait on them has completed and no copy
+// still signals them (the whole CTA has passed a barrier since).
+__device__ void init_fps_barriers(FpsShared* sh, bool again) {
+  if (again) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_inval(&sh->full[s]);
+      mbar_inval(&sh->empty[s]);
+    }
+    mbar_inval(&sh->done);
+  }
+  for (int s = 0; s < kStages; ++s) {
+    mbar_init(&sh->full[s], 1);
+    mbar_init(&sh->empty[s], kItemWarps + 1);  // every item warp read it + the MMAs ran
+  }
+  mbar_init(&sh->done, 1);
+  sh->abort_flag = 0;
+  fence_mbar_init();
+}
+
+// Compress unit u's full buffer (C items) to its FPS survivors, kept in slot
+// order in buf[0, got); returns got (all threads call, block-uniform).
+__device__ int compress_unit(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
+                             uint8_t* stages, int stage_rows, int u, uint16_t* buf) {
+  const int tid = threadIdx.x, D = p.D;
+  const int got = fps_select(p, bmap, sh, stages, stage_rows, u, p.C, p.M);
+  if (tid == 0) {
+    for (int k = 0; k < got; ++k) sh->surv[k] = sh->sel[k];
+    for (int a = 1; a < got; ++a) {  // insertion sort, got <= 64
+      const int v = sh->surv[a];
+      int b = a - 1;
+      while (b >= 0 && sh->surv[b] > v) {
+        sh->surv[b + 1] = sh->surv[b];
+        --b;
+      }
+      sh->surv[b + 1] = v;
+    }
+  }
+  __syncthreads();
+  // row k <- row surv[k] (surv ascending, surv[k] >= k): batches read into
+  // shared memory first, then written
+  const int row_vec = D / 8;  // uint4 per row
+  const int batch = max(1, static_cast<int>((kStages * stage_rows * 128) / (D * 2)));
+  uint4* tmp = reinterpret_cast<uint4*>(stages);
+  for (int k0 = 0; k0 < got; k0 += batch) {
+    const int k1 = min(got, k0 + batch);
+    for (int e = tid; e < (k1 - k0) * row_vec; e += kThreads) {
+      const int k = k0 + e / row_vec, v = e % row_vec;
+      tmp[e] = reinterpret_cast<const uint4*>(buf + static_cast<size_t>(sh->surv[k]) * D)[v];
+    }
+    __syncthreads();
+    for (int e = tid; e < (k1 - k0) * row_vec; e += kThreads) {
+      const int k = k0 + e / row_vec, v = e % row_vec;
+      reinterpret_cast<uint4*>(buf + static_cast<size_t>(k) * D)[v] = tmp[e];
+    }
+    __syncthreads();
+  }
+  // generic writes (buffer rows, and the staging in shared memory) before
+  // later TMA reads and writes of the same memory
+  fence_proxy_async();
+  __syncthreads();
+  return got;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     fps_update_kernel(const __grid_constant__ FpsParams p,
                       const __grid_constant__ CUtensorMap bmap, int stage_rows) {
@@ -585,15 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int D = p.D;
   uint16_t* buf = p.buf + static_cast<size_t>(u) * p.C * D;
 
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sh->full[s], 1);
-      mbar_init(&sh->empty[s], kItemWarps + 1);  // every item warp read it + the MMAs ran
-    }
-    mbar_init(&sh->done, 1);
-    sh->abort_flag = 0;
-    fence_mbar_init();
-  }
+  if (tid == 0) init_fps_barriers(sh, false);
   int c = p.cnt[u];
   const bool ok_state = c >= 0 && c < p.C;
   if (!ok_state) {
@@ -619,43 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 
   // ---- 2. compress a full buffer to its FPS survivors, in slot order
-  if (ok_state && c == p.C) {
-    const int got = fps_select(p, &bmap, sh, stages, stage_rows, u, c, p.M);
-    if (tid == 0) {
-      for (int k = 0; k < got; ++k) sh->surv[k] = sh->sel[k];
-      for (int a = 1; a < got; ++a) {  // insertion sort, got <= 64
-        const int v = sh->surv[a];
-        int b = a - 1;
-        while (b >= 0 && sh->surv[b] > v) {
-          sh->surv[b + 1] = sh->surv[b];
-          --b;
-        }
-        sh->surv[b + 1] = v;
-      }
-    }
-    __syncthreads();
-    // row k <- row surv[k] (surv ascending, surv[k] >= k): batches read into
-    // shared memory first, then written
-    const int row_vec = D / 8;  // uint4 per row
-    const int batch = max(1, static_cast<int>((kStages * stage_rows * 128) / (D * 2)));
-    uint4* tmp = reinterpret_cast<uint4*>(stages);
-    for (int k0 = 0; k0 < got; k0 += batch) {
-      const int k1 = min(got, k0 + batch);
-      for (int e = tid; e < (k1 - k0) * row_vec; e += kThreads) {
-        const int k = k0 + e / row_vec, v = e % row_vec;
-        tmp[e] = reinterpret_cast<const uint4*>(buf + static_cast<size_t>(sh->surv[k]) * D)[v];
-      }
-      __syncthreads();
-      for (int e = tid; e < (k1 - k0) * row_vec; e += kThreads) {
-        const int k = k0 + e / row_vec, v = e % row_vec;
-        reinterpret_cast<uint4*>(buf + static_cast<size_t>(k) * D)[v] = tmp[e];
-      }
-      __syncthreads();
-    }
-    c = got;
-    fence_proxy_async();
-    __syncthreads();
-  }
+  if (ok_state && c == p.C) c = compress_unit(p, &bmap, sh, stages, stage_rows, u, buf);
 
   // ---- 3. beacons: FPS over the current buffer (read-only)
   if (p.want_beacons) {
@@ -677,6 +702,103 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0 && ok_state) p.cnt[u] = c;
 }
 
+// ---- The per-step append on its own (a1), for steps that select no
+// beacons: one warp per unit copies the step's query (G*d bf16, at most 256
+// 16-byte pieces, at most 8 per lane) into ring slot step % W and buffer
+// slot cnt, then counts it.  Only this warp touches the unit, so reading
+// cnt and writing cnt + 1 need no atomics.  The query's loads are issued
+// before cnt arrives.  A unit whose buffer this fills (cnt == C) is left
+// for fps_compress_kernel, launched right after on the same stream.
+constexpr int kAppendWarps = 8;
+
+__global__ void __launch_bounds__(kAppendWarps * 32)
+    fps_append_kernel(const __grid_constant__ FpsParams p) {
+  pdl_trigger();  // the compress pass may set up; it waits for this grid before reading it
+  const int lane = threadIdx.x & 31;
+  const int64_t u = static_cast<int64_t>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
+  if (u >= p.U) return;
+  const int nv = p.D / 8;  // 16-byte pieces of an item: 8..256
+  const uint4* src = reinterpret_cast<const uint4*>(p.q_new + u * p.D);
+  uint4 v[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (lane + 32 * k < nv) v[k] = src[lane + 32 * k];
+  const int c = p.cnt[u];
+  if (c < 0 || c >= p.C) {  // not a valid buffer state: nothing is written
+    if (lane == 0) record_error(p.ws, BKV_EDEVICE, kSiteFpsState);
+    return;
+  }
+  uint4* ring = p.W > 0 ? reinterpret_cast<uint4*>(
+                              p.recent_q + (u * p.W + static_cast<int64_t>(p.step % p.W)) * p.D)
+                        : nullptr;
+  uint4* dst = reinterpret_cast<uint4*>(p.buf + (u * p.C + c) * p.D);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (lane + 32 * k < nv) {
+      if (ring != nullptr) ring[lane + 32 * k] = v[k];
+      dst[lane + 32 * k] = v[k];
+    }
+  __syncwarp();
+  if (lane == 0) p.cnt[u] = c + 1;
+}
+
+// ---- Compress on demand (a2) after fps_append_kernel: a persistent grid
+// (at most one CTA per SM) finds the units whose buffer is full and
+// compresses each to its FPS survivors, as step 2 of fps_update_kernel
+// does.  CTA b takes units b, b + grid, b + 2 grid, ...: it reads their
+// counts 256 at a time, lists the full ones in shared memory and compresses
+// them one after another, re-initialising its mbarriers between units.  A
+// step that fills no buffer costs one short scan per CTA.
+__global__ void __launch_bounds__(kThreads, 1)
+    fps_compress_kernel(const __grid_constant__ FpsParams p,
+                        const __grid_constant__ CUtensorMap bmap, int stage_rows) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+  FpsShared* sh = reinterpret_cast<FpsShared*>(stages + kStages * stage_rows * 128);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) init_fps_barriers(sh, false);
+  __syncthreads();
+  pdl_wait();  // the counts and buffers come from the append
+  const int64_t grid = gridDim.x;
+  bool again = false;
+  for (int64_t k0 = 0; blockIdx.x + k0 * grid < p.U; k0 += kItems) {
+    bool full = false;
+    int u = -1;
+    if (tid < kItems) {
+      const int64_t uu = blockIdx.x + (k0 + tid) * grid;
+      if (uu < p.U) {
+        u = static_cast<int>(uu);
+        full = p.cnt[u] == p.C;
+      }
+    }
+    if (tid == 0) sh->ucount = 0;
+    __syncthreads();
+    if (warp < kItemWarps) {
+      const uint32_t b = __ballot_sync(0xffffffffu, full);
+      int base = 0;
+      if (lane == 0 && b != 0u) base = atomicAdd(&sh->ucount, __popc(b));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (full) sh->ulist[base + __popc(b & ((1u << lane) - 1u))] = u;
+    }
+    __syncthreads();
+    const int n = sh->ucount;
+    for (int i = 0; i < n; ++i) {
+      const int uu = sh->ulist[i];
+      if (again) {
+        if (tid == 0) init_fps_barriers(sh, true);
+        __syncthreads();
+      }
+      again = true;
+      uint16_t* buf = p.buf + static_cast<size_t>(uu) * p.C * p.D;
+      const int got = compress_unit(p, &bmap, sh, stages, stage_rows, uu, buf);
+      if (tid == 0) p.cnt[uu] = got;
+      if (sh->abort_flag != 0) return;  // a wait timed out (recorded): copies may be in flight
+    }
+    __syncthreads();  // the list is read before the next batch rewrites it
+  }
+}
+
 }  // namespace
 
 // Stage rows cover every row a 128-row MMA band reads (one band up to C =
@@ -696,6 +818,33 @@ cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, cudaStream
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fps_update_kernel), smem);
   if (e != cudaSuccess) return e;
   fps_update_kernel<<<p.U, kThreads, smem, st>>>(p, bufmap, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fps_append_compress(const FpsParams& p, const CUtensorMap& bufmap, int sms,
+                                       cudaStream_t st) {
+  const unsigned blocks = static_cast<unsigned>((p.U + kAppendWarps - 1) / kAppendWarps);
+  fps_append_kernel<<<blocks, kAppendWarps * 32, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int rows = fps_stage_rows(p.C);
+  const size_t smem = fps_smem_bytes(p.C);
+  e = set_smem_once(reinterpret_cast<const void*>(fps_compress_kernel), smem);
+  if (e != cudaSuccess) return e;
+  // a programmatic dependent of the append: it launches while the append
+  // runs and waits for it before reading any count or buffer
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.U < sms ? p.U : sms));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, fps_compress_kernel, p, bufmap, rows);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -75,6 +75,10 @@ struct FpsParams {
 };
 
 cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, cudaStream_t st);
+// The append alone (one warp per unit), then the compress of the buffers it
+// filled (a persistent grid of at most `sms` CTAs); C <= 256, no beacons.
+cudaError_t launch_fps_append_compress(const FpsParams& p, const CUtensorMap& bufmap, int sms,
+                                       cudaStream_t st);
 // Capacities of 257..512: one cluster of ceil(C / 128) CTAs per unit.
 cudaError_t launch_fps_cluster(const FpsParams& p, const CUtensorMap& bufmap, cudaStream_t st);
 size_t fps_cluster_smem_bytes();

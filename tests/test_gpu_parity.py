@@ -441,3 +441,132 @@ def test_round_parity_32k_cache_one_unit():
     cfg = wl.CONFIGS[5]
     units = wl.make_units(cfg, range(1))
     _round_parity(cfg, units, DeviceState(units, cfg))
+
+
+@pytest.mark.parametrize("cid,one_call", [(1, False), (1, True), (2, False), (2, True)])
+def test_round_parity_recent_only_m0(cid, one_call):
+    """RPC's recent-only scoring as M = 0 in bkv_dims (inkeast.github.io
+    reading, section 三: the scores come from the recent queries alone when
+    there are no beacons): no beacon arrays at all (beacons, beacon_idx and
+    n_beacons are NULL), W * G scoring rows, and the append that fills the
+    buffer compresses it to nothing.  Through the three calls and through
+    bkv_round, against the oracle's round with M = 0."""
+    cfg = wl.CONFIGS[cid].with_(M=0)
+    units = wl.make_units(cfg, range(cfg.U))
+    st = DeviceState(units, cfg)
+    if one_call:
+        bkv.round(st.dims, st.q_new, st.step, st.ring, st.buf, st.cnt, None, None, None, st.K,
+                  st.V, st.L, st.kpos, st.cur, st.scores, st.kept, st.ws)
+        sg = None
+    else:
+        bkv.fps_update(st.dims, st.q_new, st.step, st.ring, st.buf, st.cnt, True, None, None,
+                       None, st.ws)
+        bkv.score(st.dims, st.K, st.L, st.kpos, st.ring, st.step, None, None, st.cur, st.scores,
+                  st.ws)
+        sg = st.scores.cpu().numpy().astype(np.float64)
+        bkv.select_compact(st.dims, st.scores, st.K, st.V, st.kpos, st.L, st.kept, st.ws)
+    assert st.status() == 0
+    if sg is None:
+        sg = st.scores.cpu().numpy().astype(np.float64)
+    worst = -1.0
+    for u in range(st.U):
+        un = _unit(units, u)
+        ref = oracle.round_unit(un, cfg.W, 0, cfg.B_KV, cfg.Rw, cfg.theta)
+        assert len(ref["beacon_idx"]) == 0
+        assert int(st.cnt[u]) == ref["cnt"]
+        L0 = int(un["L"])
+        worst = max(worst, score_tol_excess(sg[u, :L0], ref["scores"]))
+        n = min(L0, cfg.B_KV)
+        kept = st.kept[u].cpu().numpy()
+        assert np.array_equal(kept[:n], oracle.select(sg[u, :L0], cfg.B_KV, cfg.Rw))
+        assert kept_sets_agree(kept[:n], ref["scores"], cfg.B_KV, cfg.Rw, L0)
+        assert np.array_equal(host_u16(st.K[u])[:n], un["K"][kept[:n]])
+        assert np.array_equal(host_u16(st.V[u])[:n], un["V"][kept[:n]])
+        assert np.array_equal(st.kpos[u].cpu().numpy()[:n], un["kpos"][kept[:n]])
+        assert int(st.L[u]) == n
+    assert worst <= 0, f"score parity: worst excess {worst:.3g}"
+
+
+def _bf16_normal(rng, shape, scale=1.0):
+    return wl.to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(scale))
+
+
+@pytest.mark.parametrize("U,C,G,d,M,W", [(600, 256, 4, 128, 16, 16), (300, 64, 7, 128, 16, 16),
+                                         (200, 4, 7, 128, 1, 16), (40000, 16, 1, 64, 4, 16),
+                                         (150, 256, 1, 64, 0, 8), (97, 128, 16, 128, 32, 0)])
+def test_fps_append_compress_on_demand(U, C, G, d, M, W):
+    """A decode step that selects no beacons: the append alone, then the
+    compress of exactly the buffers it filled (wzjinhao.cn explainer, FPS
+    section: a bounded per-head buffer, FPS-compressed when it fills).  The
+    units start at assorted counts, a fifth of them one short of full, so
+    that full and non-full units interleave; 40000 units make each CTA of
+    the compress pass scan several batches of counts.  Ring, buffer
+    (survivors in slot order) and counts bit-exact against the oracle's
+    continual buffer."""
+    rng = np.random.default_rng(U + C + G + d + M)
+    D = G * d
+    buf = _bf16_normal(rng, (U, C, D), 2.0)
+    ring = _bf16_normal(rng, (U, max(W, 1), D))[:, :W]
+    q = _bf16_normal(rng, (U, D), 2.0)
+    cnt = rng.integers(0, C - 1, size=U).astype(np.int32)
+    cnt[rng.random(U) < 0.2] = C - 1
+    cnt[:3] = C - 1
+    step = 1234567
+    dims = bkv.Dims.make(U, G, d, W, M, C, 64, 16, 64, 1e4)
+    ws = bkv.make_workspace(dims)
+    t_buf, t_ring, t_cnt, t_q = dev(buf), dev(np.ascontiguousarray(ring)), dev(cnt), dev(q)
+    bkv.fps_update(dims, t_q, step, t_ring, t_buf, t_cnt, False, None, None, None, ws)
+    assert bkv.get_status(ws) == 0
+    g_buf, g_ring, g_cnt = host_u16(t_buf), host_u16(t_ring), t_cnt.cpu().numpy()
+    full = cnt == C - 1
+    assert full.sum() >= 3
+    # units that did not fill: the query lands at slot cnt, nothing else moves
+    nf = np.flatnonzero(~full)
+    exp = buf[nf].copy()
+    exp[np.arange(nf.size), cnt[nf]] = q[nf]
+    assert np.array_equal(g_buf[nf], exp)
+    assert np.array_equal(g_cnt[nf], cnt[nf] + 1)
+    if W > 0:
+        exp_ring = ring.copy()
+        exp_ring[:, step % W] = q
+        assert np.array_equal(g_ring, exp_ring)
+    for u in np.flatnonzero(full):
+        cb = oracle.ContinualBuffer.from_state(buf[u], int(cnt[u]), M)
+        assert cb.push(q[u])
+        assert int(g_cnt[u]) == M, u
+        assert np.array_equal(g_buf[u, :M], cb.items), u
+
+
+def test_fps_decode_cycle_replay():
+    """128 decode steps through the append path on the Qwen3-4B one-layer
+    shape (112 units): the first step fills every buffer, so every unit
+    compresses; the buffers, counts and ring then match the oracle's
+    continual buffers replayed over the same queries, and the beacons of the
+    round that follows match FPS over them."""
+    cfg = wl.CONFIGS[2]
+    units = wl.make_units(cfg, range(cfg.U))
+    st = DeviceState(units, cfg)
+    D = cfg.G * cfg.d
+    rng = np.random.default_rng(77)
+    qs = _bf16_normal(rng, (128, cfg.U, D), 3.0)
+    refs = [oracle.ContinualBuffer.from_state(units["buf"][u], int(units["cnt"][u]), cfg.M)
+            for u in range(cfg.U)]
+    for t in range(128):
+        bkv.fps_update(st.dims, dev(qs[t]), st.step + 1 + t, st.ring, st.buf, st.cnt, False,
+                       None, None, None, st.ws)
+        for u in range(cfg.U):
+            refs[u].push(qs[t, u])
+    st.step += 128
+    st.fps(with_append=False, want_beacons=True)
+    assert st.status() == 0
+    g_buf, g_cnt = host_u16(st.buf).reshape(cfg.U, cfg.C, D), st.cnt.cpu().numpy()
+    for u in range(cfg.U):
+        c = int(refs[u].cnt[0])
+        assert refs[u].compressions == 1
+        assert int(g_cnt[u]) == c
+        assert np.array_equal(g_buf[u, :c], refs[u].items), u
+        idx, _ = refs[u].beacons()
+        assert np.array_equal(st.bidx[u].cpu().numpy(), idx), u
+    ring = host_u16(st.ring).reshape(cfg.U, cfg.W, D)
+    for t in range(128 - cfg.W, 128):
+        assert np.array_equal(ring[:, (units["step"] + 1 + t) % cfg.W], qs[t])
