@@ -289,6 +289,23 @@ int bkv_score_noalloc(const bkv_dims* dims, const void* K, const int32_t* L,
                       const void* beacons, const int32_t* n_beacons, const int32_t* cur_pos,
                       float* scores, int32_t* device_status, bkv_stream_t stream);
 
+/*
+ * Test hook for the device-side timeout path of the scoring calls
+ * (bkv_score, bkv_score_noalloc and the scoring step of bkv_round).  Every
+ * mbarrier wait of those kernels is bounded; with wait_ns > 0 the bound is
+ * wait_ns nanoseconds instead of 2 s.  With stall = 1 the MMA issuer of
+ * each scoring CTA issues nothing, so the waits on its accumulator
+ * barriers run out: the kernels then record BKV_ETIMEOUT in the status
+ * word, let every role drain (loads already issued land, no MMA is left
+ * running) and return normally, leaving the device usable.  Scores are
+ * then undefined.  stall = 0 and wait_ns = 0 restore normal operation.
+ * The setting is process-wide and is read when a call is made; it is meant
+ * for tests of the error path only.  (The BeaconKV paper has no
+ * counterpart.)  Returns BKV_EINVAL for stall outside {0, 1} or wait_ns
+ * outside [0, 2e9].
+ */
+int bkv_test_wait_timeout(int32_t stall, int64_t wait_ns);
+
 /* Static description of a return code. */
 const char* bkv_strerror(int code);
 

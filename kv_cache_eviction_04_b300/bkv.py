@@ -59,16 +59,17 @@ _lib.bkv_score_noalloc.argtypes = [_dp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp,
 _lib.bkv_round.argtypes = [_dp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                            _vp, _vp, _vp, _vp]
 _lib.bkv_get_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]
+_lib.bkv_test_wait_timeout.argtypes = [_i32, _i64]
 _lib.bkv_strerror.argtypes = [ctypes.c_int]
 _lib.bkv_strerror.restype = ctypes.c_char_p
 for _f in ("bkv_workspace_size", "bkv_workspace_init", "bkv_fps_update", "bkv_score",
            "bkv_select_compact", "bkv_get_status", "bkv_version", "bkv_score_noalloc",
-           "bkv_round"):
+           "bkv_round", "bkv_test_wait_timeout"):
     getattr(_lib, _f).restype = ctypes.c_int
 
 EXPORTS = ("bkv_workspace_size", "bkv_workspace_init", "bkv_fps_update", "bkv_score",
            "bkv_select_compact", "bkv_get_status", "bkv_strerror", "bkv_version",
-           "bkv_score_noalloc", "bkv_round")
+           "bkv_score_noalloc", "bkv_round", "bkv_test_wait_timeout")
 
 # Bytes of the library's fixed scratch behind bkv_score_noalloc.
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -164,6 +165,13 @@ def get_status(workspace, stream=None) -> int:
     _check(_lib.bkv_get_status(_ptr(workspace), _stream(stream), ctypes.byref(st)),
            "bkv_get_status")
     return st.value
+
+
+def test_wait_timeout(stall: bool, wait_ns: int = 0):
+    """Test hook of the scoring kernels' timeout path (bkv_test_wait_timeout):
+    with ``stall`` their MMA issuer issues nothing and every wait gives up
+    after ``wait_ns``; ``test_wait_timeout(False)`` restores normal operation."""
+    _check(_lib.bkv_test_wait_timeout(1 if stall else 0, int(wait_ns)), "bkv_test_wait_timeout")
 
 
 def raw(name: str):

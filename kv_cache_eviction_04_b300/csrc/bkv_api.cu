@@ -2,6 +2,7 @@
 // validation, workspace layout, TMA descriptors and kernel launches.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstddef>
 #include <cstring>
@@ -23,8 +24,6 @@ using bkv::WsHeader;
 // The binding mirrors this layout (13 int32 fields, then the double).
 static_assert(offsetof(bkv_dims, rope_theta) == 56 && sizeof(bkv_dims) == 64,
               "bkv_dims layout");
-
-constexpr int kMaxSmem = 232448;  // bytes of shared memory a CTA may opt into on sm_103
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -60,7 +59,10 @@ int sm_count() {
 struct ScoreShape {
   int NQ, NQ16, nrows_part, ngrp, ntiles, tiles_per_split, nsplit;
   bool fused;
+  int cluster;  // > 0: single-pass scoring on a cluster of this many CTAs per unit
 };
+
+constexpr int kMaxSmem = 232448;  // bytes of shared memory a CTA may opt into on sm_103
 
 ScoreShape score_shape(const bkv_dims* d) {
   ScoreShape s{};
@@ -69,6 +71,22 @@ ScoreShape score_shape(const bkv_dims* d) {
   s.nrows_part = (s.NQ + 127) / 128 * 128;
   s.ngrp = (s.NQ16 + 255) / 256;
   s.ntiles = (d->L_cap + 127) / 128;
+  // Max aggregation over at most 128 rows, with a unit's logits fitting the
+  // TMEM of at most 8 CTAs (4 key tiles each, L_cap <= 4096), and few
+  // enough units that all their clusters run at once (one CTA per SM): one
+  // pass, the keys of a unit spread over a thread-block cluster.  With more
+  // units the one-CTA-per-unit kernel below keeps every SM busy with less
+  // fixed work per key (each CTA builds its own query operand).
+  const int ncl = (s.ntiles + 3) / 4;
+  if (d->agg == BKV_AGG_MAX && s.NQ16 <= 128 && ncl <= 8 &&
+      static_cast<int64_t>(d->U) * ncl <= sm_count() &&
+      bkv::score_smem_bytes(d->d, s.NQ16, d->W, false, ncl) <= static_cast<size_t>(kMaxSmem)) {
+    s.cluster = ncl;
+    s.fused = false;
+    s.tiles_per_split = s.ntiles;
+    s.nsplit = 1;
+    return s;
+  }
   // One CTA per unit runs both passes when the rows fit one CTA and there
   // are enough units to fill the GPU (or the caches are short); otherwise the
   // keys of a unit are split over CTAs and the passes are two launches.
@@ -142,6 +160,11 @@ int make_map(CUtensorMap* map, const void* base, uint64_t n0, uint64_t n1, uint6
 }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? BKV_OK : BKV_ECUDA; }
+
+// Wait-timeout test setting of the scoring calls (bkv_test_wait_timeout),
+// process-wide: the MMA issuer stalls and every wait gives up after wait_ns.
+std::atomic<int32_t> g_test_stall{0};
+std::atomic<int64_t> g_test_wait_ns{0};
 
 }  // namespace
 
@@ -235,7 +258,8 @@ int score_prepare(const bkv_dims* dims, const void* K, const int32_t* L, const i
   if (!aligned16(K) || (recent_q && !aligned16(recent_q)) || (beacons && !aligned16(beacons)))
     return BKV_EINVAL;
   const ScoreShape s = score_shape(dims);
-  if (bkv::score_smem_bytes(dims->d, s.NQ16, dims->W, s.fused) > static_cast<size_t>(kMaxSmem))
+  if (bkv::score_smem_bytes(dims->d, s.NQ16, dims->W, s.fused, s.cluster) >
+      static_cast<size_t>(kMaxSmem))
     return BKV_EUNSUPPORTED;
   bkv::ScoreParams& p = *out;
   p = bkv::ScoreParams{};
@@ -249,6 +273,8 @@ int score_prepare(const bkv_dims* dims, const void* K, const int32_t* L, const i
   p.part = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + bkv::kWsHeaderBytes);
   p.ws = static_cast<WsHeader*>(workspace);
   p.step = step;
+  p.slot_now = dims->W > 0 ? static_cast<int32_t>(step % dims->W) : 0;
+  p.step_cap = static_cast<int32_t>(step < (int64_t(1) << 30) ? step : (int64_t(1) << 30));
   p.U = dims->U;
   p.G = dims->G;
   p.d = dims->d;
@@ -262,9 +288,13 @@ int score_prepare(const bkv_dims* dims, const void* K, const int32_t* L, const i
   p.nsplit = s.nsplit;
   p.tiles_per_split = s.tiles_per_split;
   p.fused = s.fused ? 1 : 0;
+  p.cluster = s.cluster;
   p.agg = dims->agg;
   p.causal = dims->causal_recent;
   p.early_reads = 0;
+  const int64_t wns = g_test_wait_ns.load();
+  p.wait_ns = wns > 0 ? static_cast<uint64_t>(wns) : bkv::kWaitBudgetNs;
+  p.stall = g_test_stall.load();
   p.qscale = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dims->d)));
   for (int i = 0; i < dims->d / 2; ++i) {
     const double f = std::pow(dims->rope_theta, -2.0 * i / static_cast<double>(dims->d));
@@ -440,6 +470,15 @@ int bkv_score_noalloc(const bkv_dims* dims, const void* K, const int32_t* L,
       cudaMemcpyAsync(device_status, base, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) !=
           cudaSuccess)
     return BKV_ECUDA;
+  return BKV_OK;
+}
+
+int bkv_test_wait_timeout(int32_t stall, int64_t wait_ns) {
+  if ((stall != 0 && stall != 1) || wait_ns < 0 ||
+      wait_ns > static_cast<int64_t>(bkv::kWaitBudgetNs))
+    return BKV_EINVAL;
+  g_test_wait_ns.store(wait_ns);
+  g_test_stall.store(stall);
   return BKV_OK;
 }
 

@@ -44,12 +44,13 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
+                                         uint64_t budget_ns = kWaitBudgetNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && globaltimer() - t0 > kWaitBudgetNs) return false;
+    if ((i & 255u) == 255u && globaltimer() - t0 > budget_ns) return false;
   }
 }
 

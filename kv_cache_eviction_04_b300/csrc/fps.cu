@@ -143,35 +143,47 @@ __device__ __forceinline__ float staged_elem(const uint8_t* sb, int j, int k) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// Streaming the buffer's 64-column chunks through the stage ring once more
-// (item threads only; thread 0 issues the TMA loads): chunk c goes to stage
-// c % kStages, and a stage is refilled once all item threads are done with
-// it.  Bit s of `fph` is the parity of the next completion of full[s].
-struct ChunkStream {
+// The buffer's 64-column chunks once more, for the seed recheck right after
+// the Gram (item threads only; thread 0 issues the TMA loads).  The last
+// min(kStages, nchunks) chunks are still in their stages (chunk c in stage
+// c % kStages) and are taken first, stage by stage, with no wait; the
+// earlier chunks are reloaded into the stages as those are released, each
+// overlapping the work on the chunks before it.  Position k of the order
+// holds chunk chunk_at(k).  Bit s of `fph` is the parity of the next
+// completion of full[s].
+struct ChunkOrder {
   FpsShared* sh;
   const CUtensorMap* bmap;
   uint8_t* stages;
   uint32_t stage_bytes, box_bytes;
   int u, nchunks;
+  __device__ __forceinline__ int nres() const { return min(kStages, nchunks); }
+  __device__ __forceinline__ int first_res() const { return nchunks - nres(); }
+  __device__ __forceinline__ int chunk_at(int k) const {
+    const int S = nres(), f = first_res();
+    if (k >= S) return k - S;
+    return S < kStages ? k : f + ((k - f % kStages) + kStages) % kStages;
+  }
   __device__ __forceinline__ void load(int c, int st) const {
     mbar_arrive_expect_tx(&sh->full[st], box_bytes);
     tma_load_3d(stages + st * stage_bytes, bmap, &sh->full[st], 64 * c, 0, u);
   }
-  __device__ __forceinline__ void begin() const {
-    if (threadIdx.x == 0)
-      for (int c = 0; c < min(kStages, nchunks); ++c) load(c, c);
-  }
-  // Waits for chunk c in every item thread; null when it does not arrive.
-  __device__ __forceinline__ const uint8_t* wait(int c, uint32_t& fph) const {
-    const int st = c % kStages;
+  // The chunk at position k in every item thread; null when it does not arrive.
+  __device__ __forceinline__ const uint8_t* get(int k, uint32_t& fph) const {
+    const int st = chunk_at(k) % kStages;
+    if (k < nres()) return stages + st * stage_bytes;
     const bool ok = item_sync_and(wait_bar(&sh->full[st], (fph >> st) & 1));
     fph ^= 1u << st;
     return ok ? stages + st * stage_bytes : nullptr;
   }
-  // After all item threads are done with chunk c.
-  __device__ __forceinline__ void release(int c) const {
+  // After all item threads are done with position k: refill its stage with
+  // the next earlier chunk that maps to it, if any.
+  __device__ __forceinline__ void release(int k) const {
     item_sync();
-    if (threadIdx.x == 0 && c + kStages < nchunks) load(c + kStages, c % kStages);
+    if (threadIdx.x != 0) return;
+    const int c = chunk_at(k), st = c % kStages, f = first_res();
+    const int next = k < nres() ? (st < f ? st : -1) : (c + kStages < f ? c + kStages : -1);
+    if (next >= 0) load(next, st);
   }
 };
 
@@ -251,7 +263,7 @@ __device__ void fps_pick(const FpsParams& p, const CUtensorMap* bmap, FpsShared*
       sh->rn64[i] = ff_value(r);
       sh->rr[i] = make_float2(r.hi, r.lo);
     }
-    const ChunkStream cs{sh, bmap, stages, stage_bytes, box_bytes, u, nchunks};
+    const ChunkOrder cs{sh, bmap, stages, stage_bytes, box_bytes, u, nchunks};
     bool rok = true;
     for (int c = tid; c < nc; c += kItems) sh->cacc[c] = FF{0.f, 0.f};
     item_sync();
@@ -262,9 +274,8 @@ __device__ void fps_pick(const FpsParams& p, const CUtensorMap* bmap, FpsShared*
     // get identical values.
     const bool in_regs = nc <= kItemWarps;
     FF dreg{0.f, 0.f};
-    cs.begin();
-    for (int c = 0; c < nchunks && rok; ++c) {
-      const uint8_t* sb = cs.wait(c, fph);
+    for (int k = 0; k < nchunks && rok; ++k) {
+      const uint8_t* sb = cs.get(k, fph);
       rok = sb != nullptr;
       if (!rok) break;
       // warp w: items [32 w, 32 w + 32) in four groups of eight; lane l:
@@ -277,7 +288,8 @@ __device__ void fps_pick(const FpsParams& p, const CUtensorMap* bmap, FpsShared*
       const uint8_t* colb = sb + (lane & 3) * 4;
       const int pc = lane >> 2;
       if (32 * warp < n) {  // rows up to 32 (warp + 1) - 1 < stage rows
-#pragma unroll
+        // (a short loop body: this code runs rarely and is fetched cold)
+#pragma unroll 1
         for (int e = 0; e < 8; ++e)
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -316,7 +328,7 @@ __device__ void fps_pick(const FpsParams& p, const CUtensorMap* bmap, FpsShared*
           if (lane == 0) sh->cacc[cc] = ff_merge(sh->cacc[cc], d);
         }
       }
-      cs.release(c);
+      cs.release(k);
     }
     if (rok && in_regs && warp < nc) {
 #pragma unroll

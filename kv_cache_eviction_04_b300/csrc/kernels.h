@@ -21,6 +21,8 @@ struct ScoreParams {
   float2* part;  // [U][nsplit][nrows_part] (running max, sum of exp2), log2 units
   WsHeader* ws;
   int64_t step;
+  int32_t slot_now;         // step % W: the ring slot of the newest query (0 when W = 0)
+  int32_t step_cap;         // min(step, 2^30): ring slots older than this were never written
   int32_t U, G, d, W, M, L_cap;
   int32_t NQ;               // (W + M) * G scoring rows
   int32_t NQ16;             // NQ rounded up to 16
@@ -30,15 +32,20 @@ struct ScoreParams {
   int32_t tiles_per_split;  // 128-key tiles per split
   int32_t agg, causal;
   int32_t fused;            // 1: one CTA per unit runs both passes (NQ16 <= 256)
+  int32_t cluster;          // > 0: one pass on a cluster of this many CTAs per unit
+                            // (max aggregation, NQ16 <= 128, at most 4 key tiles per CTA)
   int32_t early_reads;      // 1: the previous kernel of the stream is the beacon selection,
                             // which writes none of K, kpos, L, cur_pos (read before waiting)
+  uint64_t wait_ns;         // budget of every mbarrier wait (ns)
+  int32_t stall;            // wait-timeout test: the MMA issuer issues nothing, so the waits
+                            // on its accumulator barriers run out after wait_ns
   float qscale;             // log2(e) / sqrt(d)
   float freq_hi[64];        // theta^(-2i/d) = freq_hi + freq_lo
   float freq_lo[64];
 };
 
 cudaError_t launch_score(const ScoreParams& p, const CUtensorMap& kmap, cudaStream_t st);
-size_t score_smem_bytes(int d, int NQ16, int W, bool fused);
+size_t score_smem_bytes(int d, int NQ16, int W, bool fused, int cluster);
 
 // --------------------------------------------------------- select+compact
 struct SelectParams {

@@ -49,8 +49,9 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 // any wait of the CTA has timed out (`abort` set) later waits fail at once,
 // so every role drains its loop without blocking and all threads still meet
 // at the CTA's barriers.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* abort) {
-  bool ok = *reinterpret_cast<volatile int32_t*>(abort) == 0 && wait_bar(bar, parity);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int32_t* abort,
+                                          uint64_t budget_ns) {
+  bool ok = *reinterpret_cast<volatile int32_t*>(abort) == 0 && wait_bar(bar, parity, budget_ns);
   ok = __all_sync(0xffffffffu, ok);
   if (!ok) *reinterpret_cast<volatile int32_t*>(abort) = 1;
   return ok;
@@ -84,9 +85,10 @@ __device__ __forceinline__ int row_position(const ScoreParams& p, int u, int r, 
   if (r >= p.NQ) return INT32_MIN;
   const int item = r / p.G;
   if (item < p.W) {
-    const int64_t age = ((p.step - item) % p.W + p.W) % p.W;
-    if (age > p.step) return INT32_MIN;
-    return cur - static_cast<int32_t>(age);
+    // age of ring slot `item`: steps since it was written (slot_now = step % W)
+    const int age = (p.slot_now - item + p.W) % p.W;
+    if (age > p.step_cap) return INT32_MIN;  // never written (older than step 0)
+    return cur - age;
   }
   return (item - p.W < nb) ? cur : INT32_MIN;
 }
@@ -128,17 +130,24 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
   constexpr int H = D / 2;
   // one thread per (row, pair of 8 consecutive rotary pairs), four items at
   // a time: all of a batch's global loads are issued before any is used.
-  // The first batch is loaded before anything else that waits on global
-  // memory; rows without an item (no beacon there) are loaded where the
-  // memory exists and zeroed below.
+  // Rows without an item (no beacon there) are loaded where the memory
+  // exists and zeroed below.
   constexpr int kGroups = H / 8;
   constexpr int kBatch = 4;
   const int total = nrows * kGroups;
   uint4 va[kBatch], vb[kBatch];
-  // cos/sin of every (age, frequency); age 0 is the current position.  The
-  // positions are not written by the beacon selection, so this runs before
-  // waiting for it.
+  // The recent queries, beacons and beacon counts come from the previous
+  // call (the beacon selection).  When the kernel has already waited for it
+  // their first loads go out at once and land while the table below is
+  // computed; inside a round the table is computed before the wait.
   const int32_t cur = p.cur_pos[u];
+  int nb_raw = 0;
+  if (!p.early_reads) {
+    load_query_batch<D, kBatch>(p, u, row0, total, tid, nthr, va, vb);
+    if (p.M > 0) nb_raw = p.n_beacons[u];
+  }
+  // cos/sin of every (age, frequency); age 0 is the current position.  The
+  // positions are not written by the beacon selection.
   const int nage = max(p.W, 1);
   for (int idx = tid; idx < nage * H; idx += nthr) {
     const int age = idx / H, i = idx % H;
@@ -147,11 +156,12 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
     sincosf(a, &s, &c);
     cs[idx] = make_float2(c, s);
   }
-  // the recent queries, beacons and beacon counts come from the previous
-  // call (the beacon selection)
-  pdl_wait();
-  load_query_batch<D, kBatch>(p, u, row0, total, tid, nthr, va, vb);
-  const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
+  if (p.early_reads) {
+    pdl_wait();
+    load_query_batch<D, kBatch>(p, u, row0, total, tid, nthr, va, vb);
+    if (p.M > 0) nb_raw = p.n_beacons[u];
+  }
+  const int nb = p.M > 0 ? min(max(nb_raw, 0), p.M) : 0;
   for (int r = tid; r < nrows; r += nthr) row_pos[r] = row_position(p, u, row0 + r, nb, cur);
   named_sync(bar, nthr);
   for (int idx0 = tid; idx0 < total; idx0 += kBatch * nthr) {
@@ -162,28 +172,32 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
       if (idx >= total) break;
       const int r = idx / kGroups, grp = idx % kGroups;
       const int32_t pos = row_pos[r];
-      uint16_t hi0[8], hi1[8], lo0[8], lo1[8];
+      // rotated, scaled pairs, rounded to bf16 two at a time (hi), then the
+      // exact remainders rounded likewise (lo)
+      __nv_bfloat162 hi0[4], hi1[4], lo0[4], lo1[4];
       if (pos == INT32_MIN) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) hi0[k] = hi1[k] = lo0[k] = lo1[k] = 0;
+        for (int k = 0; k < 4; ++k) hi0[k] = hi1[k] = lo0[k] = lo1[k] = __floats2bfloat162_rn(0.f, 0.f);
       } else {
         const int age = cur - pos;
         const uint16_t* a16 = reinterpret_cast<const uint16_t*>(&va[t]);
         const uint16_t* b16 = reinterpret_cast<const uint16_t*>(&vb[t]);
+        float y0[8], y1[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int i = grp * 8 + k;
           const float2 csv = cs[age * H + i];
           const float x0 = bf16_bits_to_float(a16[k]), x1 = bf16_bits_to_float(b16[k]);
-          const float y0 = (x0 * csv.x - x1 * csv.y) * p.qscale;
-          const float y1 = (x1 * csv.x + x0 * csv.y) * p.qscale;
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(y0), h1 = __float2bfloat16_rn(y1);
-          const __nv_bfloat16 l0 = __float2bfloat16_rn(y0 - __bfloat162float(h0));
-          const __nv_bfloat16 l1 = __float2bfloat16_rn(y1 - __bfloat162float(h1));
-          hi0[k] = __bfloat16_as_ushort(h0);
-          hi1[k] = __bfloat16_as_ushort(h1);
-          lo0[k] = __bfloat16_as_ushort(l0);
-          lo1[k] = __bfloat16_as_ushort(l1);
+          y0[k] = (x0 * csv.x - x1 * csv.y) * p.qscale;
+          y1[k] = (x1 * csv.x + x0 * csv.y) * p.qscale;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          hi0[k] = __floats2bfloat162_rn(y0[2 * k], y0[2 * k + 1]);
+          hi1[k] = __floats2bfloat162_rn(y1[2 * k], y1[2 * k + 1]);
+          const float2 h0 = __bfloat1622float2(hi0[k]), h1 = __bfloat1622float2(hi1[k]);
+          lo0[k] = __floats2bfloat162_rn(y0[2 * k] - h0.x, y0[2 * k + 1] - h0.y);
+          lo1[k] = __floats2bfloat162_rn(y1[2 * k] - h1.x, y1[2 * k + 1] - h1.y);
         }
       }
       // 8 consecutive elements = one 16-byte chunk of the swizzled image
@@ -247,26 +261,39 @@ __device__ __forceinline__ void init_barriers(Barriers* bars, int ns) {
   fence_mbar_init();
 }
 
+// Before a TMA producer leaves: every tile load it issued has landed
+// (bounded waits), so no copy into shared memory is still in flight when the
+// CTA exits, even after another role gave up.  Only the last NS loads can
+// still be pending: each earlier one was consumed before its stage was
+// refilled.  On the normal path every phase has completed and this returns
+// at once.
+__device__ __forceinline__ void drain_loads(uint64_t* full, int NS, int issued, uint64_t budget) {
+  for (int k = max(0, issued - NS); k < issued; ++k) wait_bar(&full[k % NS], (k / NS) & 1, budget);
+}
+
 // TMA producer (one elected lane of warp 0): stream the split's key tiles.
 template <int D, int NS>
 __device__ void produce_tiles(const ScoreParams& p, const CUtensorMap* kmap, Barriers* bars,
                               uint8_t* stages, int u, int t0, int ntl) {
   constexpr uint32_t kStageBytes = kTileKeys * D * 2;
   prefetch_tmap(kmap);
+  int issued = 0;
   for (int i = 0; i < ntl; ++i) {
     const int st = i % NS;
     if (*reinterpret_cast<volatile int32_t*>(&bars->abort_flag) != 0 ||
-        !wait_bar(&bars->empty[st], ((i / NS) & 1) ^ 1)) {
+        !wait_bar(&bars->empty[st], ((i / NS) & 1) ^ 1, p.wait_ns)) {
       bars->abort_flag = 1;
       record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
-      return;
+      break;
     }
     mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
     const int j0 = (t0 + i) * kTileKeys;
 #pragma unroll
     for (int a = 0; a < D / 64; ++a)
       tma_load_3d(stages + st * kStageBytes + a * 16384, kmap, &bars->full[st], 64 * a, j0, u);
+    issued = i + 1;
   }
+  drain_loads(bars->full, NS, issued, p.wait_ns);
 }
 
 // --------------------------------------------------------------- pass 1
@@ -311,10 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                      kThreads - 32, 1);
     if (warp == 1) {
       // ---------------- MMA issuer: D[row][key] = sum_k Q[row][k] K[key][k]
-      for (int i = 0; i < ntl; ++i) {
+      int last = -1;
+      for (int i = 0; i < (p.stall ? 0 : ntl); ++i) {
         const int st = i % NS, b = i & 1;
-        if (!warp_wait(&bars->full[st], (i / NS) & 1, &bars->abort_flag) ||
-            !warp_wait(&bars->tempty[b], ((i >> 1) & 1) ^ 1, &bars->abort_flag)) {
+        if (!warp_wait(&bars->full[st], (i / NS) & 1, &bars->abort_flag, p.wait_ns) ||
+            !warp_wait(&bars->tempty[b], ((i >> 1) & 1) ^ 1, &bars->abort_flag, p.wait_ns)) {
           if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
           break;
         }
@@ -337,7 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bars->tfull[b]);
         }
         __syncwarp();
+        last = i;
       }
+      // the MMAs have completed before TMEM is released, even if the
+      // epilogue gave up on them
+      if (last >= 0) wait_bar(&bars->tfull[last & 1], (last >> 1) & 1, p.wait_ns);
     } else {
       // ---------------- epilogue: thread = one row; running max / sum of exp2
       const int q = warp & 3;
@@ -357,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jn = (t0 + i + 1) * kTileKeys + et;
         kp_next = (i + 1 < ntl && jn < L) ? kpu[jn] : INT32_MAX;
         named_sync(2, kEpiThreads);
-        if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
+        if (warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag, p.wait_ns)) {
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < kTileKeys / 32; ++c) {
@@ -476,10 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
       // ---------------- MMA issuer: D[key][row] = sum_k K[key][k] Q[row][k]
       const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(N));
-      for (int i = 0; i < ntl; ++i) {
+      int last = -1;
+      for (int i = 0; i < (p.stall ? 0 : ntl); ++i) {
         const int st = i % NS, b = i & 1;
-        if (!warp_wait(&bars->full[st], (i / NS) & 1, &bars->abort_flag) ||
-            !warp_wait(&bars->tempty[b], ((i >> 1) & 1) ^ 1, &bars->abort_flag)) {
+        if (!warp_wait(&bars->full[st], (i / NS) & 1, &bars->abort_flag, p.wait_ns) ||
+            !warp_wait(&bars->tempty[b], ((i >> 1) & 1) ^ 1, &bars->abort_flag, p.wait_ns)) {
           if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
           break;
         }
@@ -502,7 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bars->tfull[b]);
         }
         __syncwarp();
+        last = i;
       }
+      if (last >= 0) wait_bar(&bars->tfull[last & 1], (last >> 1) & 1, p.wait_ns);
     } else {
       // ---------------- epilogue: thread = one key
       const int q = warp & 3;
@@ -523,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = (t0 + i) * kTileKeys + q * 32 + lane;
         const int32_t kpj = kp_ahead;
         kp_ahead = (i + 1 < ntl && j + kTileKeys < L) ? kpu[j + kTileKeys] : INT32_MAX;
-        if (!warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag)) {
+        if (!warp_wait(&bars->tfull[b], (i >> 1) & 1, &bars->abort_flag, p.wait_ns)) {
           if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
           continue;
         }
@@ -679,7 +714,8 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
   }
   lmin = __reduce_min_sync(0xffffffffu, lmin);
   if (lane == 0) atomicMin(&bars->minrow, lmin);
-  warp_wait(&bars->tmax_ready, 0, &bars->abort_flag);
+  if (!warp_wait(&bars->tmax_ready, 0, &bars->abort_flag, p.wait_ns) && lane == 0)
+    record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
   named_sync(2, kFusedEpi);
   const int32_t minrow = bars->minrow;
   // A tile whose largest key position is within every live row's limit (and
@@ -693,7 +729,7 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
       kph[ht] = j < L ? kpu[j] : INT32_MAX;
       half_sync(h);
     }
-    if (warp_wait(&bars->tfull[h], (i >> 1) & 1, &bars->abort_flag)) {
+    if (warp_wait(&bars->tfull[h], (i >> 1) & 1, &bars->abort_flag, p.wait_ns)) {
       tc_fence_after();
 #pragma unroll
       for (int blk = 0; blk < NR; ++blk)
@@ -772,7 +808,7 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
     const int32_t kpj = tile_open ? INT32_MIN : (j < L ? kpu[j] : INT32_MAX);
     float r0 = -INFINITY, r1 = -INFINITY, r2 = -INFINITY, r3 = -INFINITY;  // max
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;                          // mean
-    if (warp_wait(&bars->tfull[h], (i >> 1) & 1, &bars->abort_flag)) {
+    if (warp_wait(&bars->tfull[h], (i >> 1) & 1, &bars->abort_flag, p.wait_ns)) {
       tc_fence_after();
       const bool nomask = tile_open || __all_sync(0xffffffffu, kpj <= minpos);
       const int32_t kpm = nomask ? INT32_MIN : kpj;
@@ -952,16 +988,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // follow.
     if (lane == 0) {
       for (int i = 0; i < first; ++i) issue(i);
+      int issued = first;
       for (int i = first; i < niter; ++i) {
         const int st = i % NS;
         if (*reinterpret_cast<volatile int32_t*>(&bars->abort_flag) != 0 ||
-            !wait_bar(&bars->empty[st], ((i / NS) & 1) ^ 1)) {
+            !wait_bar(&bars->empty[st], ((i / NS) & 1) ^ 1, p.wait_ns)) {
           bars->abort_flag = 1;
           record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
           break;
         }
         issue(i);
+        issued = i + 1;
       }
+      drain_loads(bars->full, NS, issued, p.wait_ns);
     }
     __syncwarp();
   } else {
@@ -970,10 +1009,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     if (warp == 1) {
       // ---------------- MMA issuer
       const uint32_t idesc2 = idesc_bf16_f32(128, static_cast<uint32_t>(p.NQ16));
-      for (int i = 0; i < 2 * nt; ++i) {
+      int last = -1;
+      for (int i = 0; i < (p.stall ? 0 : 2 * nt); ++i) {
         const int st = i % NS, b = i & 1;
-        if (!warp_wait(&bars->full[st], (i / NS) & 1, &bars->abort_flag) ||
-            !warp_wait(&bars->tempty[b], ((i >> 1) & 1) ^ 1, &bars->abort_flag)) {
+        if (!warp_wait(&bars->full[st], (i / NS) & 1, &bars->abort_flag, p.wait_ns) ||
+            !warp_wait(&bars->tempty[b], ((i >> 1) & 1) ^ 1, &bars->abort_flag, p.wait_ns)) {
           if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
           break;
         }
@@ -1014,7 +1054,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           mma_commit(&bars->tfull[b]);
         }
         __syncwarp();
+        last = i;
       }
+      if (last >= 0) wait_bar(&bars->tfull[last & 1], (last >> 1) & 1, p.wait_ns);
     } else {
       if (p.agg == BKV_AGG_MAX)
         fused_epilogue<D, NR, kBufCols, true>(p, u, nt, L, tbase, bars, row_pos, lse, mz, part,
@@ -1028,6 +1070,284 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tbase, kCols);
+}
+
+// --------------------------------------------------------------- cluster
+// One pass over the keys, for max aggregation and up to 128 scoring rows:
+// the keys of a unit are spread over a thread-block cluster of ncl CTAs,
+// and each CTA keeps the logits of its own (at most four) 128-key tiles in
+// its TMEM for the whole call (rows on the 128 lanes, one 128-column block
+// per tile; 4 x 128 fp32 columns = all 512).  Nothing is computed twice and
+// every key tile is read from memory once:
+//   pass 1  thread = row: running max and sum of exp2 over the CTA's keys
+//           (the two halves of the epilogue take alternate tiles and merge);
+//   merge   every CTA posts its per-row (max, sum) in its shared memory, the
+//           cluster meets at a hardware barrier, and every CTA merges all
+//           posts of a row in rank order (distributed shared memory), so all
+//           CTAs hold bit-identical log2-sum-exp values;
+//   pass 2  the logits are read from TMEM once more: for each key the lanes
+//           (rows) of a warp reduce max_r (s - lse_r) with redux.sync on
+//           order-preserving keys, the four lane quarters combine through a
+//           shared-memory atomicMax, and the score is exp2 of the maximum.
+// Warp 0 issues the CTA's tile loads (one stage per tile, no refills), warp
+// 1 the MMAs (hi and lo query terms into one accumulator per tile), warps
+// 2..9 are the epilogue.
+constexpr int kClTiles = 4;  // tiles per CTA: 4 x 128 TMEM columns
+
+struct __align__(16) ClBars {
+  uint64_t full[kClTiles];
+  uint64_t tfull[kClTiles];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t minrow;   // smallest key-position limit over the live rows
+  int32_t minpos;   // smallest position over the live rows
+  int32_t tmax[kClTiles];  // largest key position per tile (keys past L: unbounded)
+};
+static_assert(sizeof(ClBars) % 16 == 0, "arrays after the barriers need 16-byte alignment");
+
+template <int D>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    score_cluster_kernel(const __grid_constant__ ScoreParams p,
+                         const __grid_constant__ CUtensorMap kmap) {
+  pdl_trigger();  // select + compact may set up; it waits for this grid before reading it
+  if (!p.early_reads) pdl_wait();
+  constexpr uint32_t kQBytes = 128 * D * 2;
+  constexpr uint32_t kStageBytes = kTileKeys * D * 2;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, kTileKeys);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* q_hi = smem;
+  uint8_t* q_lo = q_hi + kQBytes;
+  uint8_t* stages = q_lo + kQBytes;
+  ClBars* bars = reinterpret_cast<ClBars*>(stages + kClTiles * kStageBytes);
+  int32_t* row_pos = reinterpret_cast<int32_t*>(bars + 1);        // [128]
+  float2* mz = reinterpret_cast<float2*>(row_pos + 128);          // [128] second half's (m, z)
+  float2* post = mz + 128;                                        // [128] this CTA's (m, z)
+  int32_t* kp = reinterpret_cast<int32_t*>(post + 128);           // [4][128] key positions
+  uint32_t* keymax = reinterpret_cast<uint32_t*>(kp + kClTiles * 128);  // [4][128]
+  float2* cs = reinterpret_cast<float2*>(keymax + kClTiles * 128);      // [max(W,1)][D/2]
+
+  const int ncl = static_cast<int>(cluster_nctarank());
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int u = blockIdx.x / ncl;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int L = p.L[u];
+  if (L < 0 || L > p.L_cap) {
+    if (threadIdx.x == 0 && rank == 0) record_error(p.ws, BKV_EDEVICE, kSiteScoreState);
+    L = 0;
+  }
+  // tiles [t0, t1) of the unit: rank r takes its share of the layout's
+  // tiles (at most kClTiles), cut at the unit's length
+  const int ntc = (p.L_cap + kTileKeys - 1) / kTileKeys;
+  const int nt = (L + kTileKeys - 1) / kTileKeys;
+  const int t0 = min(rank * ntc / ncl, nt);
+  const int t1 = min((rank + 1) * ntc / ncl, nt);
+  const int ntl = t1 - t0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kClTiles; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->tfull[i], 1);
+      bars->tmax[i] = INT32_MIN;
+    }
+    bars->abort_flag = 0;
+    bars->minrow = INT32_MAX;
+    bars->minpos = INT32_MAX;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer: every tile of the CTA at once
+    if (lane == 0) {
+      prefetch_tmap(&kmap);
+      for (int i = 0; i < ntl; ++i) {
+        mbar_arrive_expect_tx(&bars->full[i], kStageBytes);
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_3d(stages + i * kStageBytes + a * 16384, &kmap, &bars->full[i], 64 * a,
+                      (t0 + i) * kTileKeys, u);
+      }
+      // every load has landed before the CTA can leave (bounded)
+      for (int i = 0; i < ntl; ++i) wait_bar(&bars->full[i], 0, p.wait_ns);
+    }
+    __syncwarp();
+  } else {
+    // the epilogue stages the CTA's key positions while the queries build
+    // (the positions are not written by the beacon selection)
+    const int et = threadIdx.x - 64;  // 0..255 in the epilogue
+    if (warp >= 2) {
+      const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
+      for (int e = et; e < kClTiles * 128; e += kFusedEpi) {
+        const int j = t0 * kTileKeys + e;
+        const int32_t v = (e < ntl * kTileKeys && j < L) ? kpu[j] : INT32_MAX;
+        kp[e] = v;
+        keymax[e] = 0u;
+        const int32_t wm = __reduce_max_sync(0xffffffffu, v);
+        if (lane == 0 && e < ntl * kTileKeys) atomicMax(&bars->tmax[e / kTileKeys], wm);
+      }
+    }
+    build_queries<D>(p, u, 0, 128, q_hi, q_lo, row_pos, cs, threadIdx.x - 32,
+                     kFusedThreads - 32, 1);
+    if (warp == 1) {
+      // ---------------- MMA issuer: tile i -> TMEM columns [128 i, 128 i + 128)
+      int last = -1;
+      for (int i = 0; i < (p.stall ? 0 : ntl); ++i) {
+        if (!warp_wait(&bars->full[i], 0, &bars->abort_flag, p.wait_ns)) {
+          if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t kbase = smem_u32(stages + i * kStageBytes);
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t qbase = smem_u32(part ? q_lo : q_hi);
+#pragma unroll
+            for (int a = 0; a < D / 64; ++a)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tbase + i * kTileKeys, sdesc_sw128(qbase + a * 16384 + kk * 32),
+                         sdesc_sw128(kbase + a * 16384 + kk * 32), kIdesc, (part | a | kk) != 0);
+          }
+          mma_commit(&bars->tfull[i]);
+        }
+        __syncwarp();
+        last = i;
+      }
+      if (last >= 0) wait_bar(&bars->tfull[last], 0, p.wait_ns);
+    } else {
+      // ---------------- pass 1: thread = row, running max / sum of exp2
+      const int q = warp & 3, h = (warp - 2) >> 2;
+      const int r = q * 32 + lane;  // TMEM lane = row
+      const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+      const int32_t rp = row_pos[r];
+      const int32_t lim = (p.causal || rp == INT32_MIN) ? rp : INT32_MAX - 1;
+      const int32_t lw = __reduce_min_sync(0xffffffffu, rp != INT32_MIN ? lim : INT32_MAX);
+      const int32_t pw = __reduce_min_sync(0xffffffffu, rp != INT32_MIN ? rp : INT32_MAX);
+      if (lane == 0) {
+        atomicMin(&bars->minrow, lw);
+        atomicMin(&bars->minpos, pw);
+      }
+      named_sync(2, kFusedEpi);  // key positions, tile maxima and row limits in place
+      const int32_t minrow = bars->minrow;
+      float m = -INFINITY, z = 0.f;
+      for (int i = h; i < ntl; i += 2) {
+        const bool masked = !(bars->tmax[i] <= minrow);  // block-uniform
+        if (warp_wait(&bars->tfull[i], 0, &bars->abort_flag, p.wait_ns)) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[64];  // keys 64 c .. 64 c + 63 of tile i
+            const uint32_t col = tbase + lane_addr + i * kTileKeys + c * 64;
+            tmem_ld32(col, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(col + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_wait_ld();
+            if (masked) {
+              const int* kh = kp + i * kTileKeys + 64 * c;
+#pragma unroll
+              for (int k = 0; k < 64; ++k)
+                v[k] = kh[k] > lim ? __float_as_uint(-INFINITY) : v[k];
+            }
+            row_update(m, z, v);
+          }
+        } else if (lane == 0) {
+          record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+        }
+      }
+      // the two halves of a row merge into this CTA's (max, sum) post
+      if (h == 1) mz[r] = make_float2(m, z);
+      named_sync(2, kFusedEpi);
+      if (h == 0) {
+        const float2 o = mz[r];
+        const float mm = fmaxf(m, o.x);
+        float zz = 0.f;
+        if (mm != -INFINITY) {
+          if (m != -INFINITY) zz += z * ex2(m - mm);
+          if (o.x != -INFINITY) zz += o.y * ex2(o.x - mm);
+        }
+        post[r] = make_float2(mm, zz);
+      }
+    }
+  }
+  // every CTA's posts are in place and visible to the cluster
+  __syncwarp();
+  cluster_sync();
+  if (warp >= 2) {
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    const int r = q * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const int32_t rp = row_pos[r];
+    const int32_t lim = (p.causal || rp == INT32_MIN) ? rp : INT32_MAX - 1;
+    // log2-sum-exp of row r over the whole unit: every rank's post, merged
+    // in rank order (the same order, so the same bits, in every CTA)
+    float mm = -INFINITY;
+    for (int k = 0; k < ncl; ++k) mm = fmaxf(mm, ld_cluster_f32(cluster_map(&post[r].x, k)));
+    float zz = 0.f;
+    if (mm != -INFINITY)
+      for (int k = 0; k < ncl; ++k) {
+        const float mk = ld_cluster_f32(cluster_map(&post[r].x, k));
+        const float zk = ld_cluster_f32(cluster_map(&post[r].y, k));
+        if (mk != -INFINITY) zz += zk * ex2(mk - mm);
+      }
+    // empty rows (no position, or no visible key): every probability is 0
+    const float lse = (rp != INT32_MIN && zz > 0.f) ? mm + lg2(zz) : INFINITY;
+    const int32_t minpos = bars->minpos;
+    // ---------------- pass 2: per key, max over the rows of s - lse
+    for (int i = h; i < ntl; i += 2) {
+      const bool open = bars->tmax[i] <= minpos;  // every row sees every key of the tile
+      if (warp_wait(&bars->tfull[i], 0, &bars->abort_flag, p.wait_ns)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < kTileKeys / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + lane_addr + i * kTileKeys + c * 32, v);
+          tmem_wait_ld();
+          const int* kh = kp + i * kTileKeys + 32 * c;
+          uint32_t mine = 0u;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            float x = __uint_as_float(v[k]) - lse;
+            if (!open && kh[k] > lim) x = -INFINITY;
+            // x <= 0 (lse is at least the row's largest logit); for x in
+            // [-inf, 0] the complement of the bits orders like x
+            const uint32_t key = ~__float_as_uint(fminf(x, 0.f));
+            const uint32_t best = __reduce_max_sync(0xffffffffu, key);
+            mine = lane == k ? best : mine;
+          }
+          atomicMax(&keymax[i * kTileKeys + 32 * c + lane], mine);
+        }
+      } else if (lane == 0) {
+        record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+      }
+    }
+    named_sync(2, kFusedEpi);
+    const int et = threadIdx.x - 64;
+    float* dst = p.scores + static_cast<size_t>(u) * p.L_cap + t0 * kTileKeys;
+    for (int e = et; e < ntl * kTileKeys; e += kFusedEpi)
+      if (t0 * kTileKeys + e < L) dst[e] = ex2(__uint_as_float(~keymax[e]));
+  }
+  tc_fence_before();
+  __syncthreads();
+  // no CTA leaves while another may still read its posts
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+template <int D>
+size_t cluster_smem(int W) {
+  return 1024 + 2 * static_cast<size_t>(128) * D * 2 + kClTiles * kTileKeys * D * 2 +
+         sizeof(ClBars) + 128 * 4 + 2 * 128 * 8 + 2 * kClTiles * 128 * 4 +
+         static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
 }
 
 template <int D, int NS, int NR>
@@ -1073,7 +1393,8 @@ cudaError_t launch(Kern kernel, dim3 grid, size_t smem, cudaStream_t st, const S
 
 }  // namespace
 
-size_t score_smem_bytes(int d, int NQ16, int W, bool fused) {
+size_t score_smem_bytes(int d, int NQ16, int W, bool fused, int cluster) {
+  if (cluster > 0) return d == 128 ? cluster_smem<128>(W) : cluster_smem<64>(W);
   if (fused) {
     const bool one = NQ16 <= 128;
     if (d == 128) return one ? fused_smem<128, 4, 1>(W) : fused_smem<128, 2, 2>(W);
@@ -1091,6 +1412,29 @@ size_t score_smem_bytes(int d, int NQ16, int W, bool fused) {
 }
 
 cudaError_t launch_score(const ScoreParams& p, const CUtensorMap& kmap, cudaStream_t st) {
+  if (p.cluster > 0) {
+    auto* kernel = p.d == 128 ? score_cluster_kernel<128> : score_cluster_kernel<64>;
+    const size_t smem = p.d == 128 ? cluster_smem<128>(p.W) : cluster_smem<64>(p.W);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.U * p.cluster));
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, kernel, p, kmap);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   if (p.fused) {
     const dim3 g(p.U);
     const bool one = p.NQ16 <= 128;

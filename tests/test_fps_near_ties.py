@@ -1,0 +1,66 @@
+"""FPS decisions that are near-ties at the scale of the fp32 error bound.
+
+The kernels decide each FPS step (seed, then every greedy pick) in fp32
+from the tensor-core Gram and accept that decision only when the winner
+leads the runner-up by more than 2 tau; inside that band the contenders are
+re-decided from the bf16 inputs with exact products and error-free sums.
+These buffers put many decisions at fp64 gaps of 0.5 tau to 4 tau: just
+inside and just outside the band, where a wrong bound or a faulty recheck
+would flip an index.  The indices must equal the oracle's, bit for bit.
+"""
+import numpy as np
+import pytest
+
+from kv_cache_eviction_04_b300 import workload as wl
+from tests.conftest import gpu_available
+from tests.near_ties import near_tie_units
+
+SHAPES = {
+    # name: (workload, units, seed): 255 items of D = 512 (one CTA per unit);
+    # 511 items of D = 640 (a cluster of four CTAs per unit)
+    "qwen3_4b": (wl.CONFIGS[2], 32, 71),
+    "qwen3_14b_c512": (wl.CONFIGS[5], 8, 72),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_near_tie_buffers_cover_the_band(name):
+    cfg, U, seed = SHAPES[name]
+    _, in_band = near_tie_units(seed, U, cfg.C - 1, cfg.G * cfg.d, cfg.M)
+    assert in_band["seed"] >= U // 2, in_band
+    assert in_band["greedy"] >= 4 * U, in_band
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_fps_near_ties_bit_exact(name):
+    if not gpu_available():
+        pytest.skip("needs a CUDA device")
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import oracle
+    from kv_cache_eviction_04_b300 import bkv
+    from tests.gpu_util import dev, host_u16
+
+    cfg, U, seed = SHAPES[name]
+    n, D = cfg.C - 1, cfg.G * cfg.d
+    X, _ = near_tie_units(seed, U, n, D, cfg.M)
+    buf = np.zeros((U, cfg.C, D), np.uint16)
+    buf[:, :n] = X
+    dims = bkv.Dims.make(U, cfg.G, cfg.d, cfg.W, cfg.M, cfg.C, cfg.B_KV, cfg.Rw, cfg.L,
+                         cfg.theta)
+    ws = bkv.make_workspace(dims)
+    t_buf = dev(buf)
+    cnt = dev(np.full(U, n, np.int32))
+    bidx = torch.full((U, cfg.M), -7, dtype=torch.int32, device="cuda")
+    beac = torch.zeros((U, cfg.M, cfg.G, cfg.d), dtype=torch.int16, device="cuda")
+    nb = torch.zeros(U, dtype=torch.int32, device="cuda")
+    bkv.fps_update(dims, None, 0, None, t_buf, cnt, True, bidx, beac, nb, ws)
+    assert bkv.get_status(ws) == 0
+    got = bidx.cpu().numpy()
+    for u in range(U):
+        ref = oracle.fps(X[u], cfg.M)
+        assert np.array_equal(got[u], ref), (u, got[u][:8], ref[:8])
+        assert np.array_equal(host_u16(beac[u]).reshape(cfg.M, D), X[u][ref])

@@ -570,3 +570,29 @@ def test_fps_decode_cycle_replay():
     ring = host_u16(st.ring).reshape(cfg.U, cfg.W, D)
     for t in range(128 - cfg.W, 128):
         assert np.array_equal(ring[:, (units["step"] + 1 + t) % cfg.W], qs[t])
+
+
+@pytest.mark.parametrize("L_cap,Ls,causal", [(4096, [4096, 4001, 2049, 129], 1),
+                                              (4096, [4096, 3333, 512, 1], 0),
+                                              (640, [640, 639, 511, 257], 1),
+                                              (128, [128, 100, 1, 64], 1)])
+def test_score_parity_single_pass_cluster_shapes(L_cap, Ls, causal):
+    """Max aggregation with at most 128 rows scores in one pass on a cluster
+    of ceil(L_cap / 512) CTAs per unit (logits resident in TMEM, per-row
+    statistics merged over distributed shared memory).  Cache strides of
+    one tile up to the largest cluster (8 CTAs at 4096 keys), ragged
+    lengths, causal and non-causal rows, against the oracle (the 119-row
+    R1-Distill-Qwen-7B shape with one beacon, keys cut to L_cap)."""
+    cfg = wl.config4(1)
+    units = wl.make_units(cfg, range(len(Ls)))
+    for k in ("K", "V", "kpos"):
+        units[k] = np.ascontiguousarray(units[k][:, :L_cap])
+    units["L"] = np.array(Ls, dtype=np.int32)
+    st = DeviceState(units, cfg.with_(B_KV=min(cfg.B_KV, L_cap)), causal=causal)
+    _upload_oracle_beacons(st, units, cfg)
+    st.score()
+    assert st.status() == 0
+    _score_check(cfg, units, st, "max", bool(causal))
+    sg = st.scores.cpu().numpy()
+    for u, n in enumerate(Ls):
+        assert np.all(sg[u, n:] == -1.0), "wrote past L"
