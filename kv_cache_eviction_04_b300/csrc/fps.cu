@@ -66,8 +66,6 @@ struct __align__(16) FpsShared {
   double cont_val[kItems];
   double rn64[kItems];       // seed recheck: fp64 1/||x_i||
   float2 rr[kItems];         // seed recheck: 1/||x_i|| as an unevaluated float pair
-  FF tpart[kItemWarps][64];  // seed recheck: per-warp partial sums of T over one chunk
-  FF cacc[kItems];           // seed recheck: running x_a . T of every contender
   double pair64[kMaxPairs];
   int16_t pair_a[kMaxPairs];  // item of a pair's contender
   int16_t pair_s[kMaxPairs];  // its chosen item
@@ -76,20 +74,8 @@ struct __align__(16) FpsShared {
 };
 
 // Barrier of the eight item warps only (the producer warp idles after the
-// Gram), plain and with an AND reduction.
+// Gram).
 __device__ __forceinline__ void item_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kItems) : "memory"); }
-__device__ __forceinline__ bool item_sync_and(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "n"(kItems)
-      : "memory");
-  return r != 0;
-}
 
 // Top2 over the items (thread t < 256 = item t, every item thread calls)
 // under the order "smaller value first, then smaller item"; the result is
@@ -135,63 +121,11 @@ __device__ __forceinline__ double exact_rnorm(const FpsShared* sh, int a) {
   return ff_value(ff_rsqrt(FF{sh->n2h[a], sh->n2l[a]}));
 }
 
-// Element (row j, column k) of a staged 64-column chunk: rows of 128 bytes
-// whose 16-byte pieces are swizzled by row & 7.
-__device__ __forceinline__ float staged_elem(const uint8_t* sb, int j, int k) {
-  const uint16_t b = *reinterpret_cast<const uint16_t*>(
-      sb + j * 128 + ((((k >> 3) ^ (j & 7)) << 4) | ((k & 7) << 1)));
-  return __uint_as_float(static_cast<uint32_t>(b) << 16);
-}
-
-// The buffer's 64-column chunks once more, for the seed recheck right after
-// the Gram (item threads only; thread 0 issues the TMA loads).  The last
-// min(kStages, nchunks) chunks are still in their stages (chunk c in stage
-// c % kStages) and are taken first, stage by stage, with no wait; the
-// earlier chunks are reloaded into the stages as those are released, each
-// overlapping the work on the chunks before it.  Position k of the order
-// holds chunk chunk_at(k).  Bit s of `fph` is the parity of the next
-// completion of full[s].
-struct ChunkOrder {
-  FpsShared* sh;
-  const CUtensorMap* bmap;
-  uint8_t* stages;
-  uint32_t stage_bytes, box_bytes;
-  int u, nchunks;
-  __device__ __forceinline__ int nres() const { return min(kStages, nchunks); }
-  __device__ __forceinline__ int first_res() const { return nchunks - nres(); }
-  __device__ __forceinline__ int chunk_at(int k) const {
-    const int S = nres(), f = first_res();
-    if (k >= S) return k - S;
-    return S < kStages ? k : f + ((k - f % kStages) + kStages) % kStages;
-  }
-  __device__ __forceinline__ void load(int c, int st) const {
-    mbar_arrive_expect_tx(&sh->full[st], box_bytes);
-    tma_load_3d(stages + st * stage_bytes, bmap, &sh->full[st], 64 * c, 0, u);
-  }
-  // The chunk at position k in every item thread; null when it does not arrive.
-  __device__ __forceinline__ const uint8_t* get(int k, uint32_t& fph) const {
-    const int st = chunk_at(k) % kStages;
-    if (k < nres()) return stages + st * stage_bytes;
-    const bool ok = item_sync_and(wait_bar(&sh->full[st], (fph >> st) & 1));
-    fph ^= 1u << st;
-    return ok ? stages + st * stage_bytes : nullptr;
-  }
-  // After all item threads are done with position k: refill its stage with
-  // the next earlier chunk that maps to it, if any.
-  __device__ __forceinline__ void release(int k) const {
-    item_sync();
-    if (threadIdx.x != 0) return;
-    const int c = chunk_at(k), st = c % kStages, f = first_res();
-    const int next = k < nres() ? (st < f ? st : -1) : (c + kStages < f ? c + kStages : -1);
-    if (next >= 0) load(next, st);
-  }
-};
-
 // Seed and greedy steps over the Gram in TMEM (the eight item warps only;
 // thread i owns item i and its TMEM lane).  Writes sh->sel[0, m).
-__device__ void fps_pick(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
-                         uint8_t* stages, uint32_t stage_bytes, uint32_t box_bytes,
-                         uint32_t tbase, uint32_t fph, bool gram_ok, int u, int n, int m) {
+// `stages` is free scratch here (the seed recheck's partial sums).
+__device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uint32_t tbase,
+                         bool gram_ok, int u, int n, int m) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i = tid;
   const int D = p.D;
@@ -199,7 +133,6 @@ __device__ void fps_pick(const FpsParams& p, const CUtensorMap* bmap, FpsShared*
   const uint16_t* X = p.buf + static_cast<size_t>(u) * p.C * D;
   const int N = (n + 15) & ~15;
   const int nbands = (n + 127) / 128;
-  const int nchunks = D / 64;
   // item of this thread: band h = warp / 4, TMEM lane quarter = warp % 4
   const int h = warp >> 2, q = warp & 3;
   const bool band_live = h < nbands;
@@ -250,123 +183,89 @@ __device__ void fps_pick(const FpsParams& p, const CUtensorMap* bmap, FpsShared*
     // Near-tie: re-decide among the contenders with exact-product sums.
     // sum_j cos(a, j) = r_a * (x_a . T) with T = sum_j r_j x_j, so T is
     // built once and each contender needs one dot product with it; the
-    // item's own term (n2_a r_a) r_a is then removed.  The buffer streams
-    // through the stage ring again.  Per 64-column chunk, warp w sums the
-    // items [32 w, 32 w + 32) of every column (exact bf16 x fp32 products by
-    // TwoProd, TwoSum sums); the eight warps' partial sums are then merged
-    // in a fixed order, and one warp
-    // per contender adds that chunk's part of x_a . T.  Two identical items
-    // get bit-identical values, so the lowest slot wins an exact tie.
+    // item's own term (n2_a r_a) r_a is then removed.  T is formed from the
+    // buffer in global memory (it was just streamed, so it sits in L2) in
+    // one compact loop: thread t takes the 16-byte column octet t % (D/8)
+    // and every (256 / (D/8))-th item from t / (D/8) on, with eight
+    // independent float pairs (exact bf16 x fp32 products by TwoProd,
+    // TwoSum sums); the groups' partial sums are merged in a fixed order.
+    // One warp per contender then forms x_a . T.  Two identical items get
+    // bit-identical values, so the lowest slot wins an exact tie.
     const int nc = collect_contenders(i < n && mean <= t.v1 + 2.f * taum, sh);
     {
       const FF r = i < n ? ff_rsqrt(FF{sh->n2h[i], sh->n2l[i]}) : FF{0.f, 0.f};
       sh->rn64[i] = ff_value(r);
       sh->rr[i] = make_float2(r.hi, r.lo);
     }
-    const ChunkOrder cs{sh, bmap, stages, stage_bytes, box_bytes, u, nchunks};
-    bool rok = true;
-    for (int c = tid; c < nc; c += kItems) sh->cacc[c] = FF{0.f, 0.f};
     item_sync();
-    // With at most eight contenders, warp cc keeps contender cc's per-lane
-    // partial sums in a register across chunks and merges the lanes once at
-    // the end; otherwise each chunk's part is merged and added to cacc.  All
-    // contenders of a recheck take the same path, so identical items still
-    // get identical values.
-    const bool in_regs = nc <= kItemWarps;
-    FF dreg{0.f, 0.f};
-    for (int k = 0; k < nchunks && rok; ++k) {
-      const uint8_t* sb = cs.get(k, fph);
-      rok = sb != nullptr;
-      if (!rok) break;
-      // warp w: items [32 w, 32 w + 32) in four groups of eight; lane l:
-      // columns 2l and 2l + 1 (one 32-bit word of a row).  Eight independent
-      // sums per thread, merged in a fixed order.  Row j has swizzle pattern
-      // j & 7 = e for the e-th item of a group.
-      FF acc[4][2];
+    const int noct = D / 8;               // 16-byte column octets: 8..256
+    const int ngrp = kItems / noct;       // item groups: 1..32
+    FF* Tp = reinterpret_cast<FF*>(stages);           // [ngrp][D] partial sums
+    FF* T = Tp + static_cast<size_t>(ngrp) * D;       // [D]
+    if (tid < ngrp * noct) {
+      const int g = tid / noct, o = tid - g * noct;
+      FF acc[8];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) acc[g][0] = acc[g][1] = FF{0.f, 0.f};
-      const uint8_t* colb = sb + (lane & 3) * 4;
-      const int pc = lane >> 2;
-      if (32 * warp < n) {  // rows up to 32 (warp + 1) - 1 < stage rows
-        // (a short loop body: this code runs rarely and is fetched cold)
-#pragma unroll 1
-        for (int e = 0; e < 8; ++e)
+      for (int e = 0; e < 8; ++e) acc[e] = FF{0.f, 0.f};
+      const uint4* col = reinterpret_cast<const uint4*>(X) + o;
+#pragma unroll 2
+      for (int j = g; j < n; j += ngrp) {
+        const uint4 v = col[static_cast<size_t>(j) * noct];
+        const float2 r = sh->rr[j];
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            // rows past n hold no item: a zero value and weight add exactly nothing
-            const int j = 32 * warp + 8 * g + e;
-            uint32_t w = *reinterpret_cast<const uint32_t*>(colb + j * 128 + ((pc ^ e) << 4));
-            w = j < n ? w : 0u;
-            const float2 r = sh->rr[j];
-            ff_add_scaled(acc[g][0], __uint_as_float(w << 16), r.x, r.y);
-            ff_add_scaled(acc[g][1], __uint_as_float(w & 0xFFFF0000u), r.x, r.y);
-          }
-      }
-#pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2)
-        sh->tpart[warp][2 * lane + q2] =
-            ff_merge(ff_merge(acc[0][q2], acc[1][q2]), ff_merge(acc[2][q2], acc[3][q2]));
-      item_sync();
-      for (int cc = warp; cc < nc; cc += kItemWarps) {
-        const int a = sh->cont[cc];
-        FF d{0.f, 0.f};
-#pragma unroll
-        for (int kk = lane; kk < 64; kk += 32) {
-          const FF(*tp)[64] = sh->tpart;
-          const FF tk = ff_merge(ff_merge(ff_merge(tp[0][kk], tp[1][kk]), ff_merge(tp[2][kk], tp[3][kk])),
-                                 ff_merge(ff_merge(tp[4][kk], tp[5][kk]), ff_merge(tp[6][kk], tp[7][kk])));
-          ff_add_scaled(d, staged_elem(sb, a, kk), tk.hi, tk.lo);
-        }
-        if (in_regs) {
-          dreg = ff_merge(dreg, d);
-        } else {
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const FF other{__shfl_xor_sync(0xffffffffu, d.hi, o), __shfl_xor_sync(0xffffffffu, d.lo, o)};
-            d = ff_merge(d, other);
-          }
-          if (lane == 0) sh->cacc[cc] = ff_merge(sh->cacc[cc], d);
+        for (int hh = 0; hh < 4; ++hh) {
+          ff_add_scaled(acc[2 * hh], __uint_as_float(wv[hh] << 16), r.x, r.y);
+          ff_add_scaled(acc[2 * hh + 1], __uint_as_float(wv[hh] & 0xFFFF0000u), r.x, r.y);
         }
       }
-      cs.release(k);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) Tp[static_cast<size_t>(g) * D + 8 * o + e] = acc[e];
     }
-    if (rok && in_regs && warp < nc) {
+    item_sync();
+    for (int k = tid; k < D; k += kItems) {
+      FF tk = Tp[k];
+      for (int g = 1; g < ngrp; ++g) tk = ff_merge(tk, Tp[static_cast<size_t>(g) * D + k]);
+      T[k] = tk;
+    }
+    item_sync();
+    for (int cc = warp; cc < nc; cc += kItemWarps) {
+      const int a = sh->cont[cc];
+      const uint32_t* xa = reinterpret_cast<const uint32_t*>(X + static_cast<size_t>(a) * D);
+      FF d{0.f, 0.f};
+      for (int k2 = 2 * lane; k2 < D; k2 += 64) {
+        const uint32_t w = xa[k2 / 2];
+        ff_add_scaled(d, __uint_as_float(w << 16), T[k2].hi, T[k2].lo);
+        ff_add_scaled(d, __uint_as_float(w & 0xFFFF0000u), T[k2 + 1].hi, T[k2 + 1].lo);
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        const FF other{__shfl_xor_sync(0xffffffffu, dreg.hi, o), __shfl_xor_sync(0xffffffffu, dreg.lo, o)};
-        dreg = ff_merge(dreg, other);
+        const FF other{__shfl_xor_sync(0xffffffffu, d.hi, o), __shfl_xor_sync(0xffffffffu, d.lo, o)};
+        d = ff_merge(d, other);
       }
-      if (lane == 0) sh->cacc[warp] = dreg;
-    }
-    item_sync();
-    if (rok) {
-      for (int cc = tid; cc < nc; cc += kItems) {
-        const int a = sh->cont[cc];
+      if (lane == 0) {
         const double ra = sh->rn64[a];
         const double n2a = static_cast<double>(sh->n2h[a]) + static_cast<double>(sh->n2l[a]);
-        sh->cont_val[cc] = (ff_value(sh->cacc[cc]) * ra - (n2a * ra) * ra) / static_cast<double>(n - 1);
+        sh->cont_val[cc] = (ff_value(d) * ra - (n2a * ra) * ra) / static_cast<double>(n - 1);
       }
-      item_sync();
-      if (tid == 0) {
-        int best = -1;
-        double bv = 0.0;
-        for (int c = 0; c < nc; ++c) {  // ascending index: strict < keeps the lowest
-          const double v = sh->cont_val[c];
-          if (best < 0 || v < bv) {
-            best = sh->cont[c];
-            bv = v;
-          }
-        }
-        sh->winner = best;
-      }
-      item_sync();
-      seed = sh->winner;
-    } else if (tid == 0) {
-      // a chunk that never landed: later chunks' copies may still be in
-      // flight, so the CTA takes on no further unit
-      record_error(p.ws, BKV_ETIMEOUT, kSiteFpsWait);
-      sh->abort_flag = 1;
     }
+    item_sync();
+    if (tid == 0) {
+      int best = -1;
+      double bv = 0.0;
+      for (int c = 0; c < nc; ++c) {  // ascending index: strict < keeps the lowest
+        const double v = sh->cont_val[c];
+        if (best < 0 || v < bv) {
+          best = sh->cont[c];
+          bv = v;
+        }
+      }
+      sh->winner = best;
+    }
+    item_sync();
+    seed = sh->winner;
+    // the staged chunks were overwritten by the partial sums: none is
+    // resident any more (the greedy steps read the buffer from global memory)
   }
 
   // ---- greedy farthest-point steps
@@ -486,9 +385,7 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   tc_fence_after();
   const uint32_t tbase = sh->tmem_base;
 
-  // Chunk c of the buffer goes to stage c % kStages; bit s of `fph` is the
-  // parity of the next completion of full[s] (the same in every thread).
-  uint32_t fph = 0;
+  // Chunk c of the buffer goes to stage c % kStages.
   auto load_chunk = [&](int c, int st) {
     mbar_arrive_expect_tx(&sh->full[st], box_bytes);
     tma_load_3d(stages + st * stage_bytes, bmap, &sh->full[st], 64 * c, 0, u);
@@ -566,7 +463,6 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
       if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteFpsWait);
     }
   }
-  for (int c = 0; c < nchunks; ++c) fph ^= 1u << (c % kStages);
   warp_wait(&sh->done, 0, &sh->abort_flag);
   tc_fence_after();
   if (tid < kItems) {
@@ -581,7 +477,7 @@ __device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared
   __syncthreads();
   const bool gram_ok = sh->abort_flag == 0;  // block-uniform
   if (warp < kItemWarps)
-    fps_pick(p, bmap, sh, stages, stage_bytes, box_bytes, tbase, fph, gram_ok, u, n, m);
+    fps_pick(p, sh, stages, tbase, gram_ok, u, n, m);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

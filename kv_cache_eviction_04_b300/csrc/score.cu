@@ -93,6 +93,15 @@ __device__ __forceinline__ int row_position(const ScoreParams& p, int u, int r, 
   return (item - p.W < nb) ? cur : INT32_MIN;
 }
 
+// The cos/sin table of the query build: entry (age, i) at
+// age * (D/2 + 4) + (i % 8) * (D/16) + i / 8.  A warp of the build reads, for
+// one k = i % 8, the D/16 consecutive entries of its rows' ages, and the
+// padded row stride puts different ages on different banks.
+__host__ __device__ constexpr int cs_stride(int D) { return D / 2 + 4; }
+__host__ __device__ constexpr size_t cs_bytes(int W, int D) {
+  return static_cast<size_t>(W > 0 ? W : 1) * cs_stride(D) * 8;
+}
+
 // Build the rotated, scaled, hi/lo-split query operand for rows
 // [row0, row0 + nrows) in two K-major 128B-swizzled smem images.  Run by
 // `nthr` threads with ids tid in [0, nthr); ends with named barrier `bar`.
@@ -123,6 +132,29 @@ __device__ __forceinline__ void load_query_batch(const ScoreParams& p, int u, in
   }
 }
 
+// L1 prefetches of the addresses load_query_batch reads (no registers held).
+template <int D, int kBatch>
+__device__ __forceinline__ void prefetch_query_batch(const ScoreParams& p, int u, int row0,
+                                                     int total, int idx0, int nthr) {
+  constexpr int H = D / 2;
+  constexpr int kGroups = H / 8;
+#pragma unroll
+  for (int t = 0; t < kBatch; ++t) {
+    const int idx = idx0 + t * nthr;
+    if (idx < total) {
+      const int rr = row0 + idx / kGroups, grp = idx % kGroups;
+      const int item = rr / p.G, g = rr % p.G;
+      if (item < p.W + p.M) {
+        const uint16_t* src =
+            item < p.W ? p.recent_q + ((static_cast<size_t>(u) * p.W + item) * p.G + g) * D
+                       : p.beacons + ((static_cast<size_t>(u) * p.M + (item - p.W)) * p.G + g) * D;
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(src + grp * 8));
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(src + H + grp * 8));
+      }
+    }
+  }
+}
+
 template <int D>
 __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, uint8_t* q_hi,
                               uint8_t* q_lo, int32_t* row_pos, float2* cs, int tid, int nthr,
@@ -138,30 +170,26 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
   uint4 va[kBatch], vb[kBatch];
   // The recent queries, beacons and beacon counts come from the previous
   // call (the beacon selection).  When the kernel has already waited for it
-  // their first loads go out at once and land while the table below is
-  // computed; inside a round the table is computed before the wait.
+  // the first batch is prefetched into L1 at once, landing while the table
+  // below is computed; inside a round the table is computed before the wait.
   const int32_t cur = p.cur_pos[u];
-  int nb_raw = 0;
-  if (!p.early_reads) {
-    load_query_batch<D, kBatch>(p, u, row0, total, tid, nthr, va, vb);
-    if (p.M > 0) nb_raw = p.n_beacons[u];
-  }
+  if (!p.early_reads) prefetch_query_batch<D, kBatch>(p, u, row0, total, tid, nthr);
   // cos/sin of every (age, frequency); age 0 is the current position.  The
-  // positions are not written by the beacon selection.
+  // positions are not written by the beacon selection.  Consecutive threads
+  // take consecutive ages of one frequency, so the lanes of a warp read the
+  // same few frequencies from the parameter space (different addresses in
+  // one warp would be served one after another).
   const int nage = max(p.W, 1);
   for (int idx = tid; idx < nage * H; idx += nthr) {
-    const int age = idx / H, i = idx % H;
+    const int i = idx / nage, age = idx - i * nage;
     const float a = reduce_angle(static_cast<float>(cur - age), p.freq_hi[i], p.freq_lo[i]);
     float s, c;
     sincosf(a, &s, &c);
-    cs[idx] = make_float2(c, s);
+    cs[age * cs_stride(D) + (i & 7) * (H / 8) + (i >> 3)] = make_float2(c, s);
   }
-  if (p.early_reads) {
-    pdl_wait();
-    load_query_batch<D, kBatch>(p, u, row0, total, tid, nthr, va, vb);
-    if (p.M > 0) nb_raw = p.n_beacons[u];
-  }
-  const int nb = p.M > 0 ? min(max(nb_raw, 0), p.M) : 0;
+  if (p.early_reads) pdl_wait();
+  load_query_batch<D, kBatch>(p, u, row0, total, tid, nthr, va, vb);
+  const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
   for (int r = tid; r < nrows; r += nthr) row_pos[r] = row_position(p, u, row0 + r, nb, cur);
   named_sync(bar, nthr);
   for (int idx0 = tid; idx0 < total; idx0 += kBatch * nthr) {
@@ -173,40 +201,43 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
       const int r = idx / kGroups, grp = idx % kGroups;
       const int32_t pos = row_pos[r];
       // rotated, scaled pairs, rounded to bf16 two at a time (hi), then the
-      // exact remainders rounded likewise (lo)
-      __nv_bfloat162 hi0[4], hi1[4], lo0[4], lo1[4];
-      if (pos == INT32_MIN) {
+      // exact remainders rounded likewise (lo); packed 32-bit words
+      uint32_t hi0[4] = {0u, 0u, 0u, 0u}, hi1[4] = {0u, 0u, 0u, 0u};
+      uint32_t lo0[4] = {0u, 0u, 0u, 0u}, lo1[4] = {0u, 0u, 0u, 0u};
+      if (pos != INT32_MIN) {
+        const float2* csa = cs + (cur - pos) * cs_stride(D) + grp;
+        const uint32_t wa[4] = {va[t].x, va[t].y, va[t].z, va[t].w};
+        const uint32_t wb[4] = {vb[t].x, vb[t].y, vb[t].z, vb[t].w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) hi0[k] = hi1[k] = lo0[k] = lo1[k] = __floats2bfloat162_rn(0.f, 0.f);
-      } else {
-        const int age = cur - pos;
-        const uint16_t* a16 = reinterpret_cast<const uint16_t*>(&va[t]);
-        const uint16_t* b16 = reinterpret_cast<const uint16_t*>(&vb[t]);
-        float y0[8], y1[8];
+        for (int k2 = 0; k2 < 4; ++k2) {
+          float y0[2], y1[2];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int i = grp * 8 + k;
-          const float2 csv = cs[age * H + i];
-          const float x0 = bf16_bits_to_float(a16[k]), x1 = bf16_bits_to_float(b16[k]);
-          y0[k] = (x0 * csv.x - x1 * csv.y) * p.qscale;
-          y1[k] = (x1 * csv.x + x0 * csv.y) * p.qscale;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          hi0[k] = __floats2bfloat162_rn(y0[2 * k], y0[2 * k + 1]);
-          hi1[k] = __floats2bfloat162_rn(y1[2 * k], y1[2 * k + 1]);
-          const float2 h0 = __bfloat1622float2(hi0[k]), h1 = __bfloat1622float2(hi1[k]);
-          lo0[k] = __floats2bfloat162_rn(y0[2 * k] - h0.x, y0[2 * k + 1] - h0.y);
-          lo1[k] = __floats2bfloat162_rn(y1[2 * k] - h1.x, y1[2 * k + 1] - h1.y);
+          for (int e = 0; e < 2; ++e) {
+            const int k = 2 * k2 + e;  // pair grp * 8 + k
+            const float2 csv = csa[k * (H / 8)];
+            const float x0 = __uint_as_float(e ? (wa[k2] & 0xFFFF0000u) : (wa[k2] << 16));
+            const float x1 = __uint_as_float(e ? (wb[k2] & 0xFFFF0000u) : (wb[k2] << 16));
+            y0[e] = (x0 * csv.x - x1 * csv.y) * p.qscale;
+            y1[e] = (x1 * csv.x + x0 * csv.y) * p.qscale;
+          }
+          const __nv_bfloat162 h0 = __floats2bfloat162_rn(y0[0], y0[1]);
+          const __nv_bfloat162 h1 = __floats2bfloat162_rn(y1[0], y1[1]);
+          const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+          const __nv_bfloat162 l0 = __floats2bfloat162_rn(y0[0] - f0.x, y0[1] - f0.y);
+          const __nv_bfloat162 l1 = __floats2bfloat162_rn(y1[0] - f1.x, y1[1] - f1.y);
+          hi0[k2] = *reinterpret_cast<const uint32_t*>(&h0);
+          hi1[k2] = *reinterpret_cast<const uint32_t*>(&h1);
+          lo0[k2] = *reinterpret_cast<const uint32_t*>(&l0);
+          lo1[k2] = *reinterpret_cast<const uint32_t*>(&l1);
         }
       }
       // 8 consecutive elements = one 16-byte chunk of the swizzled image
       const uint32_t o0 = sw128_offset(r, grp * 8, nrows);
       const uint32_t o1 = sw128_offset(r, H + grp * 8, nrows);
-      *reinterpret_cast<uint4*>(q_hi + o0) = *reinterpret_cast<const uint4*>(hi0);
-      *reinterpret_cast<uint4*>(q_hi + o1) = *reinterpret_cast<const uint4*>(hi1);
-      *reinterpret_cast<uint4*>(q_lo + o0) = *reinterpret_cast<const uint4*>(lo0);
-      *reinterpret_cast<uint4*>(q_lo + o1) = *reinterpret_cast<const uint4*>(lo1);
+      *reinterpret_cast<uint4*>(q_hi + o0) = make_uint4(hi0[0], hi0[1], hi0[2], hi0[3]);
+      *reinterpret_cast<uint4*>(q_hi + o1) = make_uint4(hi1[0], hi1[1], hi1[2], hi1[3]);
+      *reinterpret_cast<uint4*>(q_lo + o0) = make_uint4(lo0[0], lo0[1], lo0[2], lo0[3]);
+      *reinterpret_cast<uint4*>(q_lo + o1) = make_uint4(lo1[0], lo1[1], lo1[2], lo1[3]);
     }
   }
   fence_proxy_async_shared();  // generic smem writes -> visible to the tensor core
@@ -898,7 +929,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   float* part = reinterpret_cast<float*>(mz + kRows);         // [2][128] second half's maxima
   int32_t* kp = reinterpret_cast<int32_t*>(part + 256);       // [2][128] pass-1 key positions + [2][4] chunk maxima
   float2* cs = reinterpret_cast<float2*>(kp + 264);           // [max(W,1)][D/2]
-  int32_t* tmax = reinterpret_cast<int32_t*>(cs + (p.W > 0 ? p.W : 1) * (D / 2));  // [kTmaxTiles]
+  int32_t* tmax = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(cs) + cs_bytes(p.W, D));  // [kTmaxTiles]
 
   const int u = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1347,25 +1378,25 @@ template <int D>
 size_t cluster_smem(int W) {
   return 1024 + 2 * static_cast<size_t>(128) * D * 2 + kClTiles * kTileKeys * D * 2 +
          sizeof(ClBars) + 128 * 4 + 2 * 128 * 8 + 2 * kClTiles * 128 * 4 +
-         static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
+         cs_bytes(W, D);
 }
 
 template <int D, int NS, int NR>
 size_t fused_smem(int W) {
   return 1024 + 2 * static_cast<size_t>(NR) * 128 * D * 2 + NS * kTileKeys * D * 2 +
          sizeof(Barriers) + NR * 128 * (4 + 4 + 8) + 256 * 4 + 264 * 4 +
-         static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8 + kTmaxTiles * 4;
+         cs_bytes(W, D) + kTmaxTiles * 4;
 }
 
 template <int D, int NS>
 size_t stats_smem(int W) {
   return 1024 + 2 * 128 * D * 2 + NS * kTileKeys * D * 2 + sizeof(Barriers) + 128 * 4 + 256 * 4 +
-         static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
+         cs_bytes(W, D);
 }
 template <int D, int NS, int NMAX>
 size_t final_smem(int W) {
   return 1024 + 2 * NMAX * D * 2 + NS * kTileKeys * D * 2 + sizeof(Barriers) + 256 * 4 +
-         256 * 4 + static_cast<size_t>(W > 0 ? W : 1) * (D / 2) * 8;
+         256 * 4 + cs_bytes(W, D);
 }
 
 // pdl: launched as a programmatic dependent of the previous kernel of the
