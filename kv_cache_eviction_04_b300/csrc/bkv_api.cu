@@ -300,6 +300,8 @@ int score_prepare(const bkv_dims* dims, const void* K, const int32_t* L, const i
     const double f = std::pow(dims->rope_theta, -2.0 * i / static_cast<double>(dims->d));
     p.freq_hi[i] = static_cast<float>(f);
     p.freq_lo[i] = static_cast<float>(f - static_cast<double>(p.freq_hi[i]));
+    p.step_cos[i] = static_cast<float>(std::cos(f));
+    p.step_sin[i] = static_cast<float>(std::sin(f));
   }
   return make_map(map, K, static_cast<uint64_t>(dims->d), static_cast<uint64_t>(dims->L_cap),
                   static_cast<uint64_t>(dims->U), 128);

@@ -42,6 +42,8 @@ struct ScoreParams {
   float qscale;             // log2(e) / sqrt(d)
   float freq_hi[64];        // theta^(-2i/d) = freq_hi + freq_lo
   float freq_lo[64];
+  float step_cos[64];       // cos and sin of theta^(-2i/d) (one position step)
+  float step_sin[64];
 };
 
 cudaError_t launch_score(const ScoreParams& p, const CUtensorMap& kmap, cudaStream_t st);

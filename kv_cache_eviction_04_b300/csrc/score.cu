@@ -175,17 +175,29 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
   const int32_t cur = p.cur_pos[u];
   if (!p.early_reads) prefetch_query_batch<D, kBatch>(p, u, row0, total, tid, nthr);
   // cos/sin of every (age, frequency); age 0 is the current position.  The
-  // positions are not written by the beacon selection.  Consecutive threads
-  // take consecutive ages of one frequency, so the lanes of a warp read the
+  // positions are not written by the beacon selection.  A thread takes one
+  // frequency and a block of eight ages: sincosf at the block's first age,
+  // then seven rotations by -theta_i (cos/sin of theta_i from the host),
+  // each adding at most a couple of ulp.  Consecutive threads take
+  // consecutive blocks of one frequency, so the lanes of a warp read the
   // same few frequencies from the parameter space (different addresses in
   // one warp would be served one after another).
   const int nage = max(p.W, 1);
-  for (int idx = tid; idx < nage * H; idx += nthr) {
-    const int i = idx / nage, age = idx - i * nage;
-    const float a = reduce_angle(static_cast<float>(cur - age), p.freq_hi[i], p.freq_lo[i]);
+  const int nblk = (nage + 7) / 8;
+  for (int idx = tid; idx < nblk * H; idx += nthr) {
+    const int i = idx / nblk, a0 = (idx - i * nblk) * 8;
+    const float ang = reduce_angle(static_cast<float>(cur - a0), p.freq_hi[i], p.freq_lo[i]);
     float s, c;
-    sincosf(a, &s, &c);
-    cs[age * cs_stride(D) + (i & 7) * (H / 8) + (i >> 3)] = make_float2(c, s);
+    sincosf(ang, &s, &c);
+    const float c1 = p.step_cos[i], s1 = p.step_sin[i];
+    float2* dst = cs + (i & 7) * (H / 8) + (i >> 3);
+    const int a1 = min(a0 + 8, nage);
+    for (int a = a0; a < a1; ++a) {
+      dst[a * cs_stride(D)] = make_float2(c, s);
+      const float cn = fmaf(c, c1, s * s1);  // angle of age a + 1: one step of theta_i less
+      s = fmaf(s, c1, -(c * s1));
+      c = cn;
+    }
   }
   if (p.early_reads) pdl_wait();
   load_query_batch<D, kBatch>(p, u, row0, total, tid, nthr, va, vb);
@@ -249,8 +261,8 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
 struct __align__(16) Barriers {
   uint64_t full[8];
   uint64_t empty[8];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t tfull[4];   // accumulator buffers: 2 (split kernels, fused with 256 rows) or 4
+  uint64_t tempty[4];
   uint64_t tmax_ready;  // fused kernel: the per-tile key-position maxima are in place
   uint32_t tmem_base;
   int32_t abort_flag;
@@ -715,7 +727,7 @@ __device__ __forceinline__ void row_update(float& m, float& z, const uint32_t (&
 // Epilogue of the fused kernel (warps 2..9; thread et = threadIdx.x - 64).
 // kMax: max aggregation (else the mean), a template parameter so that the
 // per-element loops carry no branch on it.
-template <int D, int NR, uint32_t kBufCols, bool kMax>
+template <int D, int NR, uint32_t kBufCols, int kNBuf, bool kMax>
 __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int nt, int L,
                                                uint32_t tbase, Barriers* bars, int32_t* row_pos,
                                                float* lse, float2* mz, float* part,
@@ -725,7 +737,8 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
   const int h = (warp - 2) >> 2;               // half: 0 = warps 2..5, 1 = warps 6..9
   const int ht = (threadIdx.x - 64) & 127;     // thread within the half
   const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-  const uint32_t buf = tbase + lane_addr + h * kBufCols;  // this half's accumulator
+  // accumulator of iteration i (tile i, then tile i - nt in pass 2)
+  auto acc_of = [&](int i) { return tbase + lane_addr + (i % kNBuf) * kBufCols; };
   const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
   int32_t* kph = kp + h * 128;                 // this half's staged key positions
   (void)part;
@@ -760,8 +773,9 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
       kph[ht] = j < L ? kpu[j] : INT32_MAX;
       half_sync(h);
     }
-    if (warp_wait(&bars->tfull[h], (i >> 1) & 1, &bars->abort_flag, p.wait_ns)) {
+    if (warp_wait(&bars->tfull[i % kNBuf], (i / kNBuf) & 1, &bars->abort_flag, p.wait_ns)) {
       tc_fence_after();
+      const uint32_t buf = acc_of(i);
 #pragma unroll
       for (int blk = 0; blk < NR; ++blk)
 #pragma unroll
@@ -774,7 +788,7 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
           if (blk == NR - 1 && c == 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) arrive_tempty(&bars->tempty[h]);
+            if (lane == 0) arrive_tempty(&bars->tempty[i % kNBuf]);
           }
           if (masked) {
             const int lm = lim[blk];
@@ -839,8 +853,9 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
     const int32_t kpj = tile_open ? INT32_MIN : (j < L ? kpu[j] : INT32_MAX);
     float r0 = -INFINITY, r1 = -INFINITY, r2 = -INFINITY, r3 = -INFINITY;  // max
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;                          // mean
-    if (warp_wait(&bars->tfull[h], (i >> 1) & 1, &bars->abort_flag, p.wait_ns)) {
+    if (warp_wait(&bars->tfull[i % kNBuf], (i / kNBuf) & 1, &bars->abort_flag, p.wait_ns)) {
       tc_fence_after();
+      const uint32_t buf = acc_of(i);
       const bool nomask = tile_open || __all_sync(0xffffffffu, kpj <= minpos);
       const int32_t kpm = nomask ? INT32_MIN : kpj;
       // chunks of 32 rows in pairs: both TMEM loads issued before one wait
@@ -855,11 +870,23 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
         if (c + 2 >= nchunks) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) arrive_tempty(&bars->tempty[h]);
+          if (lane == 0) arrive_tempty(&bars->tempty[i % kNBuf]);
         }
         const int nv = min(two ? 64 : 32, N - c * 32);  // valid rows here (multiple of 16)
         const float4* l4 = reinterpret_cast<const float4*>(lse + c * 32);
         const int4* p4 = reinterpret_cast<const int4*>(row_pos + c * 32);
+        if (is_max && nomask && nv == 64) {
+          // every row of these 64 sees this key: no positions, no selects
+#pragma unroll
+          for (int k4 = 0; k4 < 16; ++k4) {
+            const float4 lv = l4[k4];
+            r0 = fmaxf(r0, __uint_as_float(v[k4 * 4 + 0]) - lv.x);
+            r1 = fmaxf(r1, __uint_as_float(v[k4 * 4 + 1]) - lv.y);
+            r2 = fmaxf(r2, __uint_as_float(v[k4 * 4 + 2]) - lv.z);
+            r3 = fmaxf(r3, __uint_as_float(v[k4 * 4 + 3]) - lv.w);
+          }
+          continue;
+        }
         // No branch per group of four rows: rows past nv read whatever lies
         // past them in shared memory (lse and row_pos are followed by other
         // arrays of the kernel) and are discarded by the selects.
@@ -914,7 +941,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   constexpr uint32_t kQBytes = kRows * D * 2;  // one query image (hi or lo)
   constexpr uint32_t kStageBytes = kTileKeys * D * 2;
   constexpr uint32_t kBufCols = NR == 1 ? 128 : 256;  // TMEM columns per accumulator
-  constexpr uint32_t kCols = 2 * kBufCols;
+  // accumulators in TMEM: four of 128 columns (128 rows) or two of 256, so
+  // that the MMAs of a tile can run while the epilogue still reads earlier
+  // ones (each half of the epilogue owns every other accumulator)
+  constexpr int kNBuf = NR == 1 ? 4 : 2;
+  constexpr uint32_t kCols = kNBuf * kBufCols;
   constexpr uint32_t kIdesc1 = idesc_bf16_f32(128, kTileKeys);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -942,7 +973,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       mbar_init(&bars->full[i], 1);
       mbar_init(&bars->empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNBuf; ++i) {
       mbar_init(&bars->tfull[i], 1);
       mbar_init(&bars->tempty[i], 8);  // one arrival per epilogue warp
     }
@@ -1042,9 +1073,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const uint32_t idesc2 = idesc_bf16_f32(128, static_cast<uint32_t>(p.NQ16));
       int last = -1;
       for (int i = 0; i < (p.stall ? 0 : 2 * nt); ++i) {
-        const int st = i % NS, b = i & 1;
+        const int st = i % NS, b = i % kNBuf;
         if (!warp_wait(&bars->full[st], (i / NS) & 1, &bars->abort_flag, p.wait_ns) ||
-            !warp_wait(&bars->tempty[b], ((i >> 1) & 1) ^ 1, &bars->abort_flag, p.wait_ns)) {
+            !warp_wait(&bars->tempty[b], ((i / kNBuf) & 1) ^ 1, &bars->abort_flag, p.wait_ns)) {
           if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
           break;
         }
@@ -1087,13 +1118,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         __syncwarp();
         last = i;
       }
-      if (last >= 0) wait_bar(&bars->tfull[last & 1], (last >> 1) & 1, p.wait_ns);
+      if (last >= 0) wait_bar(&bars->tfull[last % kNBuf], (last / kNBuf) & 1, p.wait_ns);
     } else {
       if (p.agg == BKV_AGG_MAX)
-        fused_epilogue<D, NR, kBufCols, true>(p, u, nt, L, tbase, bars, row_pos, lse, mz, part,
+        fused_epilogue<D, NR, kBufCols, kNBuf, true>(p, u, nt, L, tbase, bars, row_pos, lse, mz, part,
                                               kp, tmax);
       else
-        fused_epilogue<D, NR, kBufCols, false>(p, u, nt, L, tbase, bars, row_pos, lse, mz, part,
+        fused_epilogue<D, NR, kBufCols, kNBuf, false>(p, u, nt, L, tbase, bars, row_pos, lse, mz, part,
                                                kp, tmax);
     }
   }
