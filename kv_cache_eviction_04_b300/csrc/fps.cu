@@ -208,15 +208,26 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = FF{0.f, 0.f};
       const uint4* col = reinterpret_cast<const uint4*>(X) + o;
-#pragma unroll 2
-      for (int j = g; j < n; j += ngrp) {
-        const uint4 v = col[static_cast<size_t>(j) * noct];
-        const float2 r = sh->rr[j];
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      // eight items' loads in flight before any is used; items past n are
+      // zero and add exactly nothing
+#pragma unroll 1
+      for (int j0 = g; j0 < n; j0 += 8 * ngrp) {
+        uint4 v[8];
+        float2 r[8];
 #pragma unroll
-        for (int hh = 0; hh < 4; ++hh) {
-          ff_add_scaled(acc[2 * hh], __uint_as_float(wv[hh] << 16), r.x, r.y);
-          ff_add_scaled(acc[2 * hh + 1], __uint_as_float(wv[hh] & 0xFFFF0000u), r.x, r.y);
+        for (int q = 0; q < 8; ++q) {
+          const int j = j0 + q * ngrp;
+          v[q] = j < n ? col[static_cast<size_t>(j) * noct] : make_uint4(0u, 0u, 0u, 0u);
+          r[q] = j < n ? sh->rr[j] : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t wv[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+          for (int hh = 0; hh < 4; ++hh) {
+            ff_add_scaled(acc[2 * hh], __uint_as_float(wv[hh] << 16), r[q].x, r[q].y);
+            ff_add_scaled(acc[2 * hh + 1], __uint_as_float(wv[hh] & 0xFFFF0000u), r[q].x, r[q].y);
+          }
         }
       }
 #pragma unroll
@@ -244,9 +255,13 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
         d = ff_merge(d, other);
       }
       if (lane == 0) {
-        const double ra = sh->rn64[a];
-        const double n2a = static_cast<double>(sh->n2h[a]) + static_cast<double>(sh->n2l[a]);
-        sh->cont_val[cc] = (ff_value(d) * ra - (n2a * ra) * ra) / static_cast<double>(n - 1);
+        // sum over j != a of cos(a, j) = r_a (x_a . T) - 1 for a nonzero
+        // item (its own term r_a^2 ||x_a||^2 is 1), 0 for a zero one; the
+        // common factor 1 / (n - 1) of the mean does not change the order
+        const float2 ra = sh->rr[a];
+        FF v = ff_mul(d, FF{ra.x, ra.y});
+        if (ra.x != 0.f) ff_add(v, -1.f);
+        sh->cont_val[cc] = ff_value(v);
       }
     }
     item_sync();
@@ -361,7 +376,7 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
 // CTA runs at most one non-trivial selection per launch (after a compress
 // the buffer holds M items and the beacon pass takes all of them), so the
 // mbarriers start from phase 0 here.
-__device__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
+__device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
                           uint8_t* stages, int stage_rows, int u, int n, int m) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (m <= 0) return 0;
