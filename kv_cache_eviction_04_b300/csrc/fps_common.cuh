@@ -138,6 +138,15 @@ __device__ __forceinline__ FF ff_merge(FF a, FF b) {
   ff_add(r, b.hi);
   return r;
 }
+// a * b for two unevaluated pairs, ~2^-46 relative: TwoProd of the high
+// parts by fma, the cross terms added to its error, one Fast2Sum.
+__device__ __forceinline__ FF ff_mul(FF a, FF b) {
+  const float p = a.hi * b.hi;
+  float e = fmaf(a.hi, b.hi, -p);
+  e = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, e));
+  const float s = p + e;
+  return FF{s, e - (s - p)};
+}
 __device__ __forceinline__ double ff_value(FF a) {
   return static_cast<double>(a.hi) + static_cast<double>(a.lo);
 }
