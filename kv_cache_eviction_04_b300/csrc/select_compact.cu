@@ -41,8 +41,13 @@
 namespace bkv {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+// Threads per CTA: 512 for the order-preserving layout (its selection and
+// gathers are latency-bound loops, and more warps hide more of the
+// latency), 256 for the hole-filling one (its copy loop holds 144
+// registers per thread).
+template <bool kFill>
+__host__ __device__ constexpr int threads_of() { return kFill ? 256 : 512; }
+constexpr int kMaxWarps = 16;
 constexpr int kMaxBufs = 8;             // ring of wave buffers (count set by the host)
 constexpr uint32_t kBufBig = 32768;     // bytes of one wave of one CTA (RS rows of K and V)
 constexpr uint32_t kBufSmall = 16384;   // the same when a very large B_KV leaves less room
@@ -55,6 +60,7 @@ __device__ __forceinline__ uint32_t order_key(float s) {
 }
 
 // Inclusive block-wide prefix sum of one int per thread.
+template <int NT>
 __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -71,6 +77,7 @@ __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot) {
 }
 
 // Block-wide sum of one int per thread (every thread gets it).
+template <int NT>
 __device__ __forceinline__ int block_sum(int v, int* warp_tot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = __reduce_add_sync(0xffffffffu, v);
@@ -79,15 +86,15 @@ __device__ __forceinline__ int block_sum(int v, int* warp_tot) {
   __syncthreads();
   int t = 0;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) t += warp_tot[w];
+  for (int w = 0; w < NT / 32; ++w) t += warp_tot[w];
   return t;
 }
 
 struct __align__(16) Smem {
   uint64_t wbar[kMaxBufs];  // per ring buffer: a wave's gathered bytes have landed
   int32_t hist[2048];
-  int32_t warp_tot[kWarps];
-  int32_t warp_eq[kWarps];
+  int32_t warp_tot[kMaxWarps];
+  int32_t warp_eq[kMaxWarps];
   uint32_t prefix;
   int32_t krem;
   int32_t first;
@@ -107,19 +114,31 @@ __host__ __device__ inline size_t bufs_offset(int B) {
 
 // Select the kept slots of unit u into kept_s[0, n_kept); returns n_kept.
 // keys_s: the unit's order keys in shared memory, or null (read scores).
+// kStaged: the keys are read from keys_s (shared memory), else from the
+// scores in global memory; a template parameter so that no key read
+// carries a load of the other source (a runtime choice per read let both
+// loads be issued, a global load for every key of every pass).
+template <int NT, bool kStaged>
 __device__ int select_kept(const SelectParams& p, const float* sc, const uint32_t* keys_s,
                            int L, int32_t* kept_s, Smem* sm) {
   const int tid = threadIdx.x, lane = tid & 31;
+  constexpr int kWarps = NT / 32;
+  constexpr int kBins = 2048 / NT;  // histogram bins each thread scans
   const int n_kept = L <= p.B ? L : p.B;
   if (L <= p.B) {
-    for (int i = tid; i < n_kept; i += kThreads) kept_s[i] = i;
+    for (int i = tid; i < n_kept; i += NT) kept_s[i] = i;
     __syncthreads();
     return n_kept;
   }
-  auto key_at = [&](int j) { return keys_s != nullptr ? keys_s[j] : order_key(sc[j]); };
+  auto key_at = [&](int j) {
+    if constexpr (kStaged)
+      return keys_s[j];
+    else
+      return order_key(sc[j]);
+  };
   // ---------------- radix select of the (B - R)-th largest candidate:
-  // digits of 11, 11 and 10 bits from the top; thread t owns the 8 bins
-  // 2047 - 8t .. 2040 - 8t (descending) in the scan of each pass
+  // digits of 11, 11 and 10 bits from the top; thread t owns the kBins bins
+  // from 2047 - kBins t down (descending) in the scan of each pass
   const int ncand = L - p.R;
   const int k = p.B - p.R;
   uint32_t prefix = 0;
@@ -133,17 +152,17 @@ __device__ int select_kept(const SelectParams& p, const float* sc, const uint32_
       const uint32_t dmask = kDigit[pass];
       const uint32_t hmask = pass == 0 ? 0u : (0xFFFFFFFFu << (kShift[pass - 1]));
 #pragma unroll
-      for (int b8 = 0; b8 < 8; ++b8) sm->hist[tid * 8 + b8] = 0;
+      for (int b8 = 0; b8 < kBins; ++b8) sm->hist[tid * kBins + b8] = 0;
       __syncthreads();
       // four slots per thread per step, loaded before any is used (indices
       // clamped into range; slots past ncand are discarded)
-      for (int j0 = 0; j0 < ncand; j0 += 4 * kThreads) {
+      for (int j0 = 0; j0 < ncand; j0 += 4 * NT) {
         uint32_t kv[4];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) kv[q4] = key_at(min(j0 + q4 * kThreads + tid, ncand - 1));
+        for (int q4 = 0; q4 < 4; ++q4) kv[q4] = key_at(min(j0 + q4 * NT + tid, ncand - 1));
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          const bool in = j0 + q4 * kThreads + tid < ncand;
+          const bool in = j0 + q4 * NT + tid < ncand;
           const uint32_t key = kv[q4];
           const bool hit = in && (key & hmask) == prefix;
           const uint32_t bin = (key >> shift) & dmask;
@@ -151,19 +170,19 @@ __device__ int select_kept(const SelectParams& p, const float* sc, const uint32_
         }
       }
       __syncthreads();
-      int c[8], loc = 0;
+      int c[kBins], loc = 0;
 #pragma unroll
-      for (int b8 = 0; b8 < 8; ++b8) {
-        c[b8] = sm->hist[2047 - tid * 8 - b8];
+      for (int b8 = 0; b8 < kBins; ++b8) {
+        c[b8] = sm->hist[2047 - tid * kBins - b8];
         loc += c[b8];
       }
-      const int incl = block_incl_scan(loc, sm->warp_tot);
+      const int incl = block_incl_scan<NT>(loc, sm->warp_tot);
       int above = incl - loc;  // candidates in higher bins than this thread's
       if (above < krem && incl >= krem) {
 #pragma unroll
-        for (int b8 = 0; b8 < 8; ++b8) {
+        for (int b8 = 0; b8 < kBins; ++b8) {
           if (above < krem && above + c[b8] >= krem) {
-            sm->prefix = prefix | (static_cast<uint32_t>(2047 - tid * 8 - b8) << shift);
+            sm->prefix = prefix | (static_cast<uint32_t>(2047 - tid * kBins - b8) << shift);
             sm->krem = krem - above;
           }
           above += c[b8];
@@ -265,16 +284,17 @@ __device__ int select_kept(const SelectParams& p, const float* sc, const uint32_
 // source) pairs with 16-byte loads and stores, kFillAhead per thread in
 // flight (the copy is bound by the bytes each SM keeps in flight).
 // `hole` holds up to n entries, `bits` up to n bits.
+template <int NT>
 __device__ void fill_compact(const SelectParams& p, int u, int rank, int ncl, int n,
                              const int32_t* kept_s, int32_t* hole, uint32_t* bits, Smem* sm,
                              int32_t* kp, uint8_t* Kb, uint8_t* Vb, uint32_t rb) {
   const int tid = threadIdx.x;
   const int nwords = (n + 31) >> 5;
-  for (int w = tid; w < nwords; w += kThreads) bits[w] = 0u;
+  for (int w = tid; w < nwords; w += NT) bits[w] = 0u;
   int below = 0;  // kept slots below n: a prefix of the ascending list
-  for (int j = tid; j < n; j += kThreads) below += kept_s[j] < n ? 1 : 0;
-  const int c = block_sum(below, sm->warp_tot);  // its barriers also publish the zeroed bits
-  for (int j = tid; j < c; j += kThreads) atomicOr(&bits[kept_s[j] >> 5], 1u << (kept_s[j] & 31));
+  for (int j = tid; j < n; j += NT) below += kept_s[j] < n ? 1 : 0;
+  const int c = block_sum<NT>(below, sm->warp_tot);  // its barriers also publish the zeroed bits
+  for (int j = tid; j < c; j += NT) atomicOr(&bits[kept_s[j] >> 5], 1u << (kept_s[j] & 31));
   __syncthreads();
   // ascending hole list: thread t takes words [t wpt, (t + 1) wpt) of the map
   auto hole_bits = [&](int w) {
@@ -282,11 +302,11 @@ __device__ void fill_compact(const SelectParams& p, int u, int rank, int ncl, in
     const int valid = n - 32 * w;  // slots of this word below n
     return valid < 32 ? m & ((1u << valid) - 1u) : m;
   };
-  const int wpt = (nwords + kThreads - 1) / kThreads;
+  const int wpt = (nwords + NT - 1) / NT;
   const int w0 = min(nwords, tid * wpt), w1 = min(nwords, w0 + wpt);
   int cnt = 0;
   for (int w = w0; w < w1; ++w) cnt += __popc(hole_bits(w));
-  int pos = block_incl_scan(cnt, sm->warp_tot) - cnt;
+  int pos = block_incl_scan<NT>(cnt, sm->warp_tot) - cnt;
   for (int w = w0; w < w1; ++w) {
     uint32_t m = hole_bits(w);
     while (m != 0u) {
@@ -298,24 +318,24 @@ __device__ void fill_compact(const SelectParams& p, int u, int rank, int ncl, in
   const int h = n - c;  // holes = kept slots at or past n
   if (rank == 0 && p.kept != nullptr) {  // the source slot of every row
     int32_t* ko = p.kept + static_cast<size_t>(u) * p.B;
-    for (int i = tid; i < p.B; i += kThreads) ko[i] = i < n ? i : -1;
+    for (int i = tid; i < p.B; i += NT) ko[i] = i < n ? i : -1;
     __syncthreads();
-    for (int k = tid; k < h; k += kThreads) ko[hole[k]] = kept_s[c + k];
+    for (int k = tid; k < h; k += NT) ko[hole[k]] = kept_s[c + k];
   }
   const int k0 = static_cast<int>(static_cast<int64_t>(h) * rank / ncl);
   const int k1 = static_cast<int>(static_cast<int64_t>(h) * (rank + 1) / ncl);
-  for (int k = k0 + tid; k < k1; k += kThreads) kp[hole[k]] = kp[kept_s[c + k]];
+  for (int k = k0 + tid; k < k1; k += NT) kp[hole[k]] = kp[kept_s[c + k]];
   // element e of this CTA's pairs: pair k0 + e / per_pair, 16-byte piece
   // e % per_pair (K pieces first, then V)
   const int ppr = static_cast<int>(rb / 16);
   const int per_pair = 2 * ppr;
   const int total = (k1 - k0) * per_pair;
-  for (int e0 = tid; e0 < total; e0 += kFillAhead * kThreads) {
+  for (int e0 = tid; e0 < total; e0 += kFillAhead * NT) {
     uint4 v[kFillAhead];
     uint8_t* dst[kFillAhead];
 #pragma unroll
     for (int q = 0; q < kFillAhead; ++q) {
-      const int e = e0 + q * kThreads;
+      const int e = e0 + q * NT;
       const int ec = e < total ? e : total - 1;  // clamped: a valid address, store skipped
       const int k = k0 + ec / per_pair, pc = ec % per_pair;
       const bool is_v = pc >= ppr;
@@ -334,8 +354,9 @@ __device__ void fill_compact(const SelectParams& p, int u, int rank, int ncl, in
 // that its copy loop's registers do not lower the occupancy of the
 // order-preserving one.
 template <bool kFill>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(threads_of<kFill>())
     select_compact_kernel(const __grid_constant__ SelectParams p) {
+  constexpr int NT = threads_of<kFill>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem* sm = reinterpret_cast<Smem*>(smem_raw);
   int32_t* kept_s = reinterpret_cast<int32_t*>(smem_raw + kept_offset());
@@ -378,38 +399,54 @@ __global__ void __launch_bounds__(kThreads)
       (L > p.B && lbytes <= (kpos_s ? tail_off : static_cast<size_t>(nbufs) * bufb))
           ? reinterpret_cast<uint32_t*>(bufs)
           : nullptr;
+  // When the unit's rows are 16-byte aligned (then so are keys_s + 4i and
+  // kpos_s + 4i: the ring is 1024-byte aligned) the staging copies are
+  // 16-byte cp.async copies, all of them in flight at once (a long cache's
+  // 128 KB of scores would otherwise arrive a few loads per thread at a
+  // time); the scores are then turned into order keys in place.
+  const bool sc16 = (reinterpret_cast<uintptr_t>(sc) & 15u) == 0;
+  const bool kp16 = (reinterpret_cast<uintptr_t>(kp) & 15u) == 0;
+  const int n4 = L >> 2;
+  if (keys_s != nullptr && sc16)
+    for (int i = tid; i < n4; i += NT) cp_async16(keys_s + 4 * i, sc + 4 * i);
+  if (kpos_s != nullptr && kp16)
+    for (int i = tid; i < n4; i += NT) cp_async16(kpos_s + 4 * i, kp + 4 * i);
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
   if (keys_s != nullptr) {
-    // 16-byte loads when the unit's scores are aligned (then keys_s + 4i is
-    // too: the ring is 1024-byte aligned)
-    if ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0) {
-      const float4* s4 = reinterpret_cast<const float4*>(sc);
-      const int n4 = L >> 2;
-#pragma unroll 8
-      for (int i = tid; i < n4; i += kThreads) {
-        const float4 v = s4[i];
-        reinterpret_cast<uint4*>(keys_s)[i] =
-            make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+    if (sc16) {
+      uint4* k4 = reinterpret_cast<uint4*>(keys_s);
+      for (int i = tid; i < n4; i += NT) {
+        const uint4 v = k4[i];
+        k4[i] = make_uint4(order_key(__uint_as_float(v.x)), order_key(__uint_as_float(v.y)),
+                           order_key(__uint_as_float(v.z)), order_key(__uint_as_float(v.w)));
       }
-      for (int j = 4 * n4 + tid; j < L; j += kThreads) keys_s[j] = order_key(sc[j]);
+      for (int j = 4 * n4 + tid; j < L; j += NT) keys_s[j] = order_key(sc[j]);
     } else {
 #pragma unroll 8
-      for (int j = tid; j < L; j += kThreads) keys_s[j] = order_key(sc[j]);
+      for (int j = tid; j < L; j += NT) keys_s[j] = order_key(sc[j]);
     }
   }
   if (kpos_s != nullptr) {
+    if (kp16) {
+      for (int j = 4 * n4 + tid; j < L; j += NT) kpos_s[j] = kp[j];
+    } else {
 #pragma unroll 8
-    for (int j = tid; j < L; j += kThreads) kpos_s[j] = kp[j];
+      for (int j = tid; j < L; j += NT) kpos_s[j] = kp[j];
+    }
   }
   __syncthreads();
-  const int n_kept = select_kept(p, sc, keys_s, L, kept_s, sm);
+  const int n_kept = keys_s != nullptr ? select_kept<NT, true>(p, sc, keys_s, L, kept_s, sm)
+                                       : select_kept<NT, false>(p, sc, keys_s, L, kept_s, sm);
   // first destination row whose source differs (kept[i] == i before it)
-  for (int i = tid; i < n_kept; i += kThreads)
+  for (int i = tid; i < n_kept; i += NT)
     if (kept_s[i] != i) atomicMin(&sm->first, i);
   __syncthreads();  // the keys in the ring are dead from here on
   const int first = min(sm->first, n_kept);
 
   if constexpr (kFill) {
-    fill_compact(p, u, rank, ncl, n_kept, kept_s, kpn, reinterpret_cast<uint32_t*>(bufs), sm, kp,
+    fill_compact<NT>(p, u, rank, ncl, n_kept, kept_s, kpn, reinterpret_cast<uint32_t*>(bufs), sm, kp,
                  p.K + ubase * rb, p.V + ubase * rb, rb);
     cluster_sync();  // every CTA of the unit has read L and finished its copies
     if (rank == 0 && tid == 0 && valid) p.L[u] = n_kept;
@@ -417,7 +454,7 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   if (rank == 0 && p.kept != nullptr)
-    for (int i = tid; i < p.B; i += kThreads)
+    for (int i = tid; i < p.B; i += NT)
       p.kept[static_cast<size_t>(u) * p.B + i] = i < n_kept ? kept_s[i] : -1;
 
   // ---------------- compaction in cluster-wide waves
@@ -443,15 +480,15 @@ __global__ void __launch_bounds__(kThreads)
   //    commit group per wave.
   const int warp = tid >> 5, lane = tid & 31;
   int nruns = 0;
-  for (int i = first + tid; i < n_kept; i += kThreads)
+  for (int i = first + tid; i < n_kept; i += NT)
     nruns += (i == first || kept_s[i - 1] + 1 != kept_s[i]) ? 1 : 0;
-  const bool use_tma = 4 * block_sum(nruns, sm->warp_tot) <= n_kept - first;
+  const bool use_tma = 4 * block_sum<NT>(nruns, sm->warp_tot) <= n_kept - first;
   const int ppr = static_cast<int>(rb / 16);  // 16-byte pieces per row
   auto issue_cp = [&](int w) {  // every thread
     int r0, cnt;
     slice(w, r0, cnt);
     uint8_t* buf = bufs + (w % nbufs) * bufb;
-    for (int e = tid; e < 2 * cnt * ppr; e += kThreads) {
+    for (int e = tid; e < 2 * cnt * ppr; e += NT) {
       const int t = e / ppr, pc = e % ppr;
       const bool is_v = t >= cnt;
       const int row = is_v ? t - cnt : t;
@@ -502,12 +539,19 @@ __global__ void __launch_bounds__(kThreads)
   // New kpos of every row this CTA writes, gathered while those gathers fly
   // and before the first wave's barrier (no CTA writes kpos before it);
   // entry w * RS + t = wave w, row t.
-  for (int e = tid; e < nw * RS; e += kThreads) {
-    int r0, cnt;
-    slice(e / RS, r0, cnt);
-    if (e % RS < cnt) {
-      const int src = kept_s[r0 + e % RS];
-      kpn[e] = kpos_s != nullptr ? kpos_s[src] : kp[src];
+  // (the staged and the global source in separate loops, so that no read
+  // also issues a load of the other)
+  if (kpos_s != nullptr) {
+    for (int e = tid; e < nw * RS; e += NT) {
+      int r0, cnt;
+      slice(e / RS, r0, cnt);
+      if (e % RS < cnt) kpn[e] = kpos_s[kept_s[r0 + e % RS]];
+    }
+  } else {
+    for (int e = tid; e < nw * RS; e += NT) {
+      int r0, cnt;
+      slice(e / RS, r0, cnt);
+      if (e % RS < cnt) kpn[e] = kp[kept_s[r0 + e % RS]];
     }
   }
   __syncthreads();  // the staged key positions are dead from here on
@@ -568,10 +612,12 @@ __global__ void __launch_bounds__(kThreads)
 
 // Ring of the copy waves: buffers of 32 KB (16 KB when a very large B_KV
 // leaves no room for three of 32 KB).  As many as fit (at most 8) when there
-// are few units, each CTA then streaming with a deep pipeline; with many
-// units, just enough to stage a unit's keys (at least 3), so that two CTAs
-// share an SM and one copies while the other selects.  nbufs = 0: not even
-// three buffers fit.
+// are few units, each CTA then streaming with a deep pipeline.  With many
+// units, just enough to stage a unit's keys (at least 3) when that lets two
+// CTAs share an SM, so that one copies while the other selects; when even
+// that ring is too large for two CTAs per SM (long caches, large B_KV), the
+// deep ring again, since a lone CTA per SM then needs every wave in flight
+// it can hold.  nbufs = 0: not even three buffers fit.
 void select_ring(int B, int L_cap, bool many_units, int* nbufs, int* buf_bytes) {
   const size_t off = bufs_offset(B);
   size_t bb = kBufBig;
@@ -586,7 +632,9 @@ void select_ring(int B, int L_cap, bool many_units, int* nbufs, int* buf_bytes) 
   if (many_units) {
     const size_t stage = (static_cast<size_t>(L_cap) * 4 + bb - 1) / bb;
     const int want = stage < 3 ? 3 : static_cast<int>(stage);
-    n = want < n ? want : n;
+    // two CTAs share an SM's 228 KB (each also reserves 1 KB)
+    const bool two_per_sm = off + static_cast<size_t>(want) * bb <= 113 * 1024;
+    if (two_per_sm && want < n) n = want;
   }
   *nbufs = n;
 }
@@ -602,7 +650,7 @@ cudaError_t launch_select_compact(const SelectParams& p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(p.U * p.ncl));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(p.fill ? threads_of<true>() : threads_of<false>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
