@@ -145,10 +145,67 @@ def run_reference(args, rank, world):
 # --------------------------------------------------------------- clocks
 
 
+class _NvmlLib:
+    """The few read-only NVML queries the clock sampler makes, through
+    ctypes on the driver's libnvidia-ml.so.1 (for images without the pynvml
+    module).  Method names and constants as in pynvml."""
+
+    NVML_CLOCK_SM = 1
+    nvmlClocksEventReasonSwPowerCap = 0x4
+    nvmlClocksEventReasonHwSlowdown = 0x8
+    nvmlClocksEventReasonSwThermalSlowdown = 0x20
+    nvmlClocksEventReasonHwThermalSlowdown = 0x40
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self._ok(self.lib.nvmlInit_v2())
+
+    def _ok(self, rc):
+        if rc != 0:
+            raise RuntimeError(f"NVML error {rc}")
+
+    def nvmlInit(self):
+        pass
+
+    def nvmlDeviceGetHandleByPciBusId(self, bus):
+        h = self.c.c_void_p()
+        self._ok(self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), self.c.byref(h)))
+        return h
+
+    def nvmlDeviceGetHandleByIndex(self, i):
+        h = self.c.c_void_p()
+        self._ok(self.lib.nvmlDeviceGetHandleByIndex_v2(self.c.c_uint(i), self.c.byref(h)))
+        return h
+
+    def _uint(self, fn, *args):
+        v = self.c.c_uint()
+        self._ok(fn(*args, self.c.byref(v)))
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, h, t):
+        return self._uint(self.lib.nvmlDeviceGetClockInfo, h, self.c.c_int(t))
+
+    def nvmlDeviceGetMaxClockInfo(self, h, t):
+        return self._uint(self.lib.nvmlDeviceGetMaxClockInfo, h, self.c.c_int(t))
+
+    def nvmlDeviceGetPowerUsage(self, h):
+        return self._uint(self.lib.nvmlDeviceGetPowerUsage, h)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self.c.c_ulonglong()
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._ok(fn(h, self.c.byref(v)))
+        return v.value
+
+
 class ClockSampler:
     """Samples SM clock, power and clock-event reasons of one GPU every
-    10 ms from a thread (NVML, read-only queries), so that even a short
-    timed region gets samples.  Falls back to an nvidia-smi loop."""
+    2 ms from a thread (NVML, read-only queries: pynvml, else ctypes on the
+    driver's NVML library), so that even a short timed region gets samples.
+    Falls back to an nvidia-smi loop."""
 
     REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
                ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
@@ -170,7 +227,10 @@ class ClockSampler:
 
     def start(self):
         try:
-            import pynvml as nv
+            try:
+                import pynvml as nv
+            except ImportError:
+                nv = _NvmlLib()
             nv.nvmlInit()
             self.nv, self.h = nv, self._handle(nv)
             self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
@@ -217,7 +277,7 @@ class ClockSampler:
                 self.rows.append((sm, rs, pw))
             except Exception:
                 pass
-            self.stop_ev.wait(0.01)
+            self.stop_ev.wait(0.002)
 
     def stop(self):
         self.stop_ev.set()

@@ -41,12 +41,13 @@
 namespace bkv {
 namespace {
 
-// Threads per CTA: 512 for the order-preserving layout (its selection and
-// gathers are latency-bound loops, and more warps hide more of the
-// latency), 256 for the hole-filling one (its copy loop holds 144
-// registers per thread).
-template <bool kFill>
-__host__ __device__ constexpr int threads_of() { return kFill ? 256 : 512; }
+// Threads per CTA: 256, or 512 for long caches in the order-preserving
+// layout, whose selection passes over tens of thousands of keys are
+// latency-bound loops that more warps hide better (measured on 32768 keys:
+// 2.76 against 3.42 ms for the 32K-cache round; on caches of 1 to 2 K keys
+// 256 threads were faster).  The hole-filling copy loop holds 144
+// registers per thread, so that layout stays at 256.
+constexpr int kLongCache = 8192;  // L_cap from which the ordered layout takes 512 threads
 constexpr int kMaxWarps = 16;
 constexpr int kMaxBufs = 8;             // ring of wave buffers (count set by the host)
 constexpr uint32_t kBufBig = 32768;     // bytes of one wave of one CTA (RS rows of K and V)
@@ -353,10 +354,9 @@ __device__ void fill_compact(const SelectParams& p, int u, int rank, int ncl, in
 // kFill: the hole-filling compaction (p.fill), a separate instantiation so
 // that its copy loop's registers do not lower the occupancy of the
 // order-preserving one.
-template <bool kFill>
-__global__ void __launch_bounds__(threads_of<kFill>())
+template <bool kFill, int NT>
+__global__ void __launch_bounds__(NT)
     select_compact_kernel(const __grid_constant__ SelectParams p) {
-  constexpr int NT = threads_of<kFill>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem* sm = reinterpret_cast<Smem*>(smem_raw);
   int32_t* kept_s = reinterpret_cast<int32_t*>(smem_raw + kept_offset());
@@ -645,12 +645,14 @@ size_t select_smem_bytes(int B, int nbufs, int buf_bytes) {
 
 cudaError_t launch_select_compact(const SelectParams& p, cudaStream_t st) {
   const size_t smem = select_smem_bytes(p.B, p.nbufs, p.buf_bytes);
-  auto* kernel = p.fill ? select_compact_kernel<true> : select_compact_kernel<false>;
+  const bool wide = !p.fill && p.L_cap >= kLongCache;
+  auto* kernel = p.fill ? select_compact_kernel<true, 256>
+                        : (wide ? select_compact_kernel<false, 512> : select_compact_kernel<false, 256>);
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(p.U * p.ncl));
-  cfg.blockDim = dim3(p.fill ? threads_of<true>() : threads_of<false>());
+  cfg.blockDim = dim3(wide ? 512 : 256);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
