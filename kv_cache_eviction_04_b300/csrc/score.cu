@@ -44,6 +44,18 @@ __device__ __forceinline__ float lg2(float x) {
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
+// Named barrier that also ORs a predicate over its n threads: every thread
+// gets the same verdict (for decisions that must be uniform across warps).
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+      " barrier.cta.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 
 // Every lane of the warp waits on `bar`; the verdict is warp-uniform.  Once
 // any wait of the CTA has timed out (`abort` set) later waits fail at once,
@@ -155,6 +167,95 @@ __device__ __forceinline__ void prefetch_query_batch(const ScoreParams& p, int u
   }
 }
 
+// cos/sin of every (age, frequency) of the query build; age 0 is the
+// current position `cur`.  The positions are not written by the beacon
+// selection.  A thread takes one frequency and a block of eight ages:
+// sincosf at the block's first age, then seven rotations by -theta_i
+// (cos/sin of theta_i from the host), each adding at most a couple of ulp.
+// Consecutive threads take consecutive blocks of one frequency, so the lanes
+// of a warp read the same few frequencies from the parameter space
+// (different addresses in one warp would be served one after another).
+template <int D>
+__device__ __forceinline__ void build_cs_table(const ScoreParams& p, int32_t cur, float2* cs,
+                                               int tid, int nthr) {
+  constexpr int H = D / 2;
+  const int nage = max(p.W, 1);
+  const int nblk = (nage + 7) / 8;
+  for (int idx = tid; idx < nblk * H; idx += nthr) {
+    const int i = idx / nblk, a0 = (idx - i * nblk) * 8;
+    const float ang = reduce_angle(static_cast<float>(cur - a0), p.freq_hi[i], p.freq_lo[i]);
+    float s, c;
+    sincosf(ang, &s, &c);
+    const float c1 = p.step_cos[i], s1 = p.step_sin[i];
+    float2* dst = cs + (i & 7) * (H / 8) + (i >> 3);
+    const int a1 = min(a0 + 8, nage);
+    for (int a = a0; a < a1; ++a) {
+      dst[a * cs_stride(D)] = make_float2(c, s);
+      const float cn = fmaf(c, c1, s * s1);  // angle of age a + 1: one step of theta_i less
+      s = fmaf(s, c1, -(c * s1));
+      c = cn;
+    }
+  }
+}
+
+// Rotate, scale and hi/lo-split the query items idx0, idx0 + nthr, ...
+// (kBatch of them, as load_query_batch loaded them) and store them in the
+// two K-major 128B-swizzled images of `nrows` rows.
+template <int D, int kBatch>
+__device__ __forceinline__ void store_query_batch(const ScoreParams& p, int nrows, int total,
+                                                  int idx0, int nthr, const uint4 (&va)[kBatch],
+                                                  const uint4 (&vb)[kBatch],
+                                                  const int32_t* row_pos, const float2* cs,
+                                                  int32_t cur, uint8_t* q_hi, uint8_t* q_lo) {
+  constexpr int H = D / 2;
+  constexpr int kGroups = H / 8;
+#pragma unroll
+  for (int t = 0; t < kBatch; ++t) {
+    const int idx = idx0 + t * nthr;
+    if (idx >= total) break;
+    const int r = idx / kGroups, grp = idx % kGroups;
+    const int32_t pos = row_pos[r];
+    // rotated, scaled pairs, rounded to bf16 two at a time (hi), then the
+    // exact remainders rounded likewise (lo); packed 32-bit words
+    uint32_t hi0[4] = {0u, 0u, 0u, 0u}, hi1[4] = {0u, 0u, 0u, 0u};
+    uint32_t lo0[4] = {0u, 0u, 0u, 0u}, lo1[4] = {0u, 0u, 0u, 0u};
+    if (pos != INT32_MIN) {
+      const float2* csa = cs + (cur - pos) * cs_stride(D) + grp;
+      const uint32_t wa[4] = {va[t].x, va[t].y, va[t].z, va[t].w};
+      const uint32_t wb[4] = {vb[t].x, vb[t].y, vb[t].z, vb[t].w};
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        float y0[2], y1[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int k = 2 * k2 + e;  // pair grp * 8 + k
+          const float2 csv = csa[k * (H / 8)];
+          const float x0 = __uint_as_float(e ? (wa[k2] & 0xFFFF0000u) : (wa[k2] << 16));
+          const float x1 = __uint_as_float(e ? (wb[k2] & 0xFFFF0000u) : (wb[k2] << 16));
+          y0[e] = (x0 * csv.x - x1 * csv.y) * p.qscale;
+          y1[e] = (x1 * csv.x + x0 * csv.y) * p.qscale;
+        }
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(y0[0], y0[1]);
+        const __nv_bfloat162 h1 = __floats2bfloat162_rn(y1[0], y1[1]);
+        const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
+        const __nv_bfloat162 l0 = __floats2bfloat162_rn(y0[0] - f0.x, y0[1] - f0.y);
+        const __nv_bfloat162 l1 = __floats2bfloat162_rn(y1[0] - f1.x, y1[1] - f1.y);
+        hi0[k2] = *reinterpret_cast<const uint32_t*>(&h0);
+        hi1[k2] = *reinterpret_cast<const uint32_t*>(&h1);
+        lo0[k2] = *reinterpret_cast<const uint32_t*>(&l0);
+        lo1[k2] = *reinterpret_cast<const uint32_t*>(&l1);
+      }
+    }
+    // 8 consecutive elements = one 16-byte chunk of the swizzled image
+    const uint32_t o0 = sw128_offset(r, grp * 8, nrows);
+    const uint32_t o1 = sw128_offset(r, H + grp * 8, nrows);
+    *reinterpret_cast<uint4*>(q_hi + o0) = make_uint4(hi0[0], hi0[1], hi0[2], hi0[3]);
+    *reinterpret_cast<uint4*>(q_hi + o1) = make_uint4(hi1[0], hi1[1], hi1[2], hi1[3]);
+    *reinterpret_cast<uint4*>(q_lo + o0) = make_uint4(lo0[0], lo0[1], lo0[2], lo0[3]);
+    *reinterpret_cast<uint4*>(q_lo + o1) = make_uint4(lo1[0], lo1[1], lo1[2], lo1[3]);
+  }
+}
+
 template <int D>
 __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, uint8_t* q_hi,
                               uint8_t* q_lo, int32_t* row_pos, float2* cs, int tid, int nthr,
@@ -174,31 +275,7 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
   // below is computed; inside a round the table is computed before the wait.
   const int32_t cur = p.cur_pos[u];
   if (!p.early_reads) prefetch_query_batch<D, kBatch>(p, u, row0, total, tid, nthr);
-  // cos/sin of every (age, frequency); age 0 is the current position.  The
-  // positions are not written by the beacon selection.  A thread takes one
-  // frequency and a block of eight ages: sincosf at the block's first age,
-  // then seven rotations by -theta_i (cos/sin of theta_i from the host),
-  // each adding at most a couple of ulp.  Consecutive threads take
-  // consecutive blocks of one frequency, so the lanes of a warp read the
-  // same few frequencies from the parameter space (different addresses in
-  // one warp would be served one after another).
-  const int nage = max(p.W, 1);
-  const int nblk = (nage + 7) / 8;
-  for (int idx = tid; idx < nblk * H; idx += nthr) {
-    const int i = idx / nblk, a0 = (idx - i * nblk) * 8;
-    const float ang = reduce_angle(static_cast<float>(cur - a0), p.freq_hi[i], p.freq_lo[i]);
-    float s, c;
-    sincosf(ang, &s, &c);
-    const float c1 = p.step_cos[i], s1 = p.step_sin[i];
-    float2* dst = cs + (i & 7) * (H / 8) + (i >> 3);
-    const int a1 = min(a0 + 8, nage);
-    for (int a = a0; a < a1; ++a) {
-      dst[a * cs_stride(D)] = make_float2(c, s);
-      const float cn = fmaf(c, c1, s * s1);  // angle of age a + 1: one step of theta_i less
-      s = fmaf(s, c1, -(c * s1));
-      c = cn;
-    }
-  }
+  build_cs_table<D>(p, cur, cs, tid, nthr);
   if (p.early_reads) pdl_wait();
   load_query_batch<D, kBatch>(p, u, row0, total, tid, nthr, va, vb);
   const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
@@ -206,51 +283,8 @@ __device__ void build_queries(const ScoreParams& p, int u, int row0, int nrows, 
   named_sync(bar, nthr);
   for (int idx0 = tid; idx0 < total; idx0 += kBatch * nthr) {
     if (idx0 != tid) load_query_batch<D, kBatch>(p, u, row0, total, idx0, nthr, va, vb);
-#pragma unroll
-    for (int t = 0; t < kBatch; ++t) {
-      const int idx = idx0 + t * nthr;
-      if (idx >= total) break;
-      const int r = idx / kGroups, grp = idx % kGroups;
-      const int32_t pos = row_pos[r];
-      // rotated, scaled pairs, rounded to bf16 two at a time (hi), then the
-      // exact remainders rounded likewise (lo); packed 32-bit words
-      uint32_t hi0[4] = {0u, 0u, 0u, 0u}, hi1[4] = {0u, 0u, 0u, 0u};
-      uint32_t lo0[4] = {0u, 0u, 0u, 0u}, lo1[4] = {0u, 0u, 0u, 0u};
-      if (pos != INT32_MIN) {
-        const float2* csa = cs + (cur - pos) * cs_stride(D) + grp;
-        const uint32_t wa[4] = {va[t].x, va[t].y, va[t].z, va[t].w};
-        const uint32_t wb[4] = {vb[t].x, vb[t].y, vb[t].z, vb[t].w};
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-          float y0[2], y1[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int k = 2 * k2 + e;  // pair grp * 8 + k
-            const float2 csv = csa[k * (H / 8)];
-            const float x0 = __uint_as_float(e ? (wa[k2] & 0xFFFF0000u) : (wa[k2] << 16));
-            const float x1 = __uint_as_float(e ? (wb[k2] & 0xFFFF0000u) : (wb[k2] << 16));
-            y0[e] = (x0 * csv.x - x1 * csv.y) * p.qscale;
-            y1[e] = (x1 * csv.x + x0 * csv.y) * p.qscale;
-          }
-          const __nv_bfloat162 h0 = __floats2bfloat162_rn(y0[0], y0[1]);
-          const __nv_bfloat162 h1 = __floats2bfloat162_rn(y1[0], y1[1]);
-          const float2 f0 = __bfloat1622float2(h0), f1 = __bfloat1622float2(h1);
-          const __nv_bfloat162 l0 = __floats2bfloat162_rn(y0[0] - f0.x, y0[1] - f0.y);
-          const __nv_bfloat162 l1 = __floats2bfloat162_rn(y1[0] - f1.x, y1[1] - f1.y);
-          hi0[k2] = *reinterpret_cast<const uint32_t*>(&h0);
-          hi1[k2] = *reinterpret_cast<const uint32_t*>(&h1);
-          lo0[k2] = *reinterpret_cast<const uint32_t*>(&l0);
-          lo1[k2] = *reinterpret_cast<const uint32_t*>(&l1);
-        }
-      }
-      // 8 consecutive elements = one 16-byte chunk of the swizzled image
-      const uint32_t o0 = sw128_offset(r, grp * 8, nrows);
-      const uint32_t o1 = sw128_offset(r, H + grp * 8, nrows);
-      *reinterpret_cast<uint4*>(q_hi + o0) = make_uint4(hi0[0], hi0[1], hi0[2], hi0[3]);
-      *reinterpret_cast<uint4*>(q_hi + o1) = make_uint4(hi1[0], hi1[1], hi1[2], hi1[3]);
-      *reinterpret_cast<uint4*>(q_lo + o0) = make_uint4(lo0[0], lo0[1], lo0[2], lo0[3]);
-      *reinterpret_cast<uint4*>(q_lo + o1) = make_uint4(lo1[0], lo1[1], lo1[2], lo1[3]);
-    }
+    store_query_batch<D, kBatch>(p, nrows, total, idx0, nthr, va, vb, row_pos, cs, cur, q_hi,
+                                 q_lo);
   }
   fence_proxy_async_shared();  // generic smem writes -> visible to the tensor core
   named_sync(bar, nthr);
@@ -724,48 +758,88 @@ __device__ __forceinline__ void row_update(float& m, float& z, const uint32_t (&
   }
 }
 
-// Epilogue of the fused kernel (warps 2..9; thread et = threadIdx.x - 64).
-// kMax: max aggregation (else the mean), a template parameter so that the
-// per-element loops carry no branch on it.
+// Barriers and per-unit hand-offs of the persistent two-pass kernel; what
+// crosses from one unit to the next is double-buffered by unit parity.
+struct __align__(16) FusedBars {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t tfull[4];   // accumulator buffers: 4 (128 rows) or 2 (256 rows)
+  uint64_t tempty[4];
+  uint64_t qfull[2];   // a unit's query image and row positions are in place
+  uint64_t qempty;     // the MMAs of a unit are done with the query image
+  uint64_t tready[2];  // a unit's per-tile key-position maxima are in place
+  uint64_t edone[2];   // the epilogue is done with a unit (8 warps)
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t minrow[2];   // smallest key-position limit over a unit's live rows
+  int32_t minpos[2];   // smallest position over a unit's live rows
+};
+static_assert(sizeof(FusedBars) % 16 == 0, "arrays after the barriers need 16-byte alignment");
+
+// Warp 0 TMA, warp 1 MMA, warps 2-3 query build of the next unit, warps
+// 4-11 epilogue.
+constexpr int kPersistThreads = 384;
+
+// One warp: the smallest key-position limit and the smallest position over
+// the live rows of a unit's query build, then the build is announced.
+__device__ __forceinline__ void publish_rows(const ScoreParams& p, const int32_t* rp, int nrows,
+                                             FusedBars* bars, int b) {
+  const int lane = threadIdx.x & 31;
+  int32_t lw = INT32_MAX, pw = INT32_MAX;
+  for (int r = lane; r < nrows; r += 32) {
+    const int32_t v = rp[r];
+    if (v != INT32_MIN) {
+      lw = min(lw, p.causal ? v : INT32_MAX - 1);
+      pw = min(pw, v);
+    }
+  }
+  lw = __reduce_min_sync(0xffffffffu, lw);
+  pw = __reduce_min_sync(0xffffffffu, pw);
+  if (lane == 0) {
+    bars->minrow[b] = lw;
+    bars->minpos[b] = pw;
+    mbar_arrive(&bars->qfull[b]);
+  }
+  __syncwarp();
+}
+
+// Epilogue of one unit (warps 4..11).  Iteration i of the unit (tile i in
+// pass 1, tile i - nt in pass 2) is the kernel's iteration g0 + i: it uses
+// accumulator (g0 + i) % kNBuf and is taken by half (g0 + i) % 2, so each
+// half owns every other accumulator.  kMax: max aggregation (else the
+// mean), a template parameter so that the per-element loops carry no branch
+// on it.
 template <int D, int NR, uint32_t kBufCols, int kNBuf, bool kMax>
-__device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int nt, int L,
-                                               uint32_t tbase, Barriers* bars, int32_t* row_pos,
-                                               float* lse, float2* mz, float* part,
-                                               int32_t* kp, const int32_t* tmax) {
+__device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int nt, int L, int g0,
+                                               uint32_t tbase, FusedBars* bars, int32_t* row_pos,
+                                               float* lse, float2* mz, int32_t* kp,
+                                               const int32_t* tmax, int32_t minrow,
+                                               int32_t minpos) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                      // TMEM lane quarter
-  const int h = (warp - 2) >> 2;               // half: 0 = warps 2..5, 1 = warps 6..9
-  const int ht = (threadIdx.x - 64) & 127;     // thread within the half
+  const int h = (warp - 4) >> 2;               // half: 0 = warps 4..7, 1 = warps 8..11
+  const int ht = (threadIdx.x - 128) & 127;    // thread within the half
   const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-  // accumulator of iteration i (tile i, then tile i - nt in pass 2)
-  auto acc_of = [&](int i) { return tbase + lane_addr + (i % kNBuf) * kBufCols; };
+  auto acc_of = [&](int g) { return tbase + lane_addr + (g % kNBuf) * kBufCols; };
   const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
   int32_t* kph = kp + h * 128;                 // this half's staged key positions
-  (void)part;
 
   // ---- pass 1: thread = row (of each row block) over all keys of its
   // half's tiles; running max and sum of exp2
   float m[NR], z[NR];
   int32_t lim[NR];
-  int32_t lmin = INT32_MAX;  // smallest limit over this thread's live rows
 #pragma unroll
   for (int blk = 0; blk < NR; ++blk) {
     const int32_t rp = row_pos[blk * 128 + q * 32 + lane];
     lim[blk] = (p.causal || rp == INT32_MIN) ? rp : INT32_MAX - 1;
-    if (rp != INT32_MIN) lmin = min(lmin, lim[blk]);
     m[blk] = -INFINITY;
     z[blk] = 0.f;
   }
-  lmin = __reduce_min_sync(0xffffffffu, lmin);
-  if (lane == 0) atomicMin(&bars->minrow, lmin);
-  if (!warp_wait(&bars->tmax_ready, 0, &bars->abort_flag, p.wait_ns) && lane == 0)
-    record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
-  named_sync(2, kFusedEpi);
-  const int32_t minrow = bars->minrow;
   // A tile whose largest key position is within every live row's limit (and
   // that has no key past L) needs no mask; for another tile the half stages
   // its key positions in shared memory between two barriers of the half.
-  for (int i = h; i < nt; i += 2) {
+  for (int i = (h - g0) & 1; i < nt; i += 2) {
+    const int g = g0 + i;
     const bool masked = !(i < kTmaxTiles && tmax[i] <= minrow);  // uniform
     if (masked) {
       half_sync(h);  // the half is done with its previous staged tile
@@ -773,9 +847,9 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
       kph[ht] = j < L ? kpu[j] : INT32_MAX;
       half_sync(h);
     }
-    if (warp_wait(&bars->tfull[i % kNBuf], (i / kNBuf) & 1, &bars->abort_flag, p.wait_ns)) {
+    if (warp_wait(&bars->tfull[g % kNBuf], (g / kNBuf) & 1, &bars->abort_flag, p.wait_ns)) {
       tc_fence_after();
-      const uint32_t buf = acc_of(i);
+      const uint32_t buf = acc_of(g);
 #pragma unroll
       for (int blk = 0; blk < NR; ++blk)
 #pragma unroll
@@ -788,7 +862,7 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
           if (blk == NR - 1 && c == 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) arrive_tempty(&bars->tempty[i % kNBuf]);
+            if (lane == 0) arrive_tempty(&bars->tempty[g % kNBuf]);
           }
           if (masked) {
             const int lm = lim[blk];
@@ -824,7 +898,6 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
           if (o.x != -INFINITY) zz += o.y * ex2(o.x - mm);
         }
         if (zz > 0.f) l = mm + lg2(zz);
-        atomicMin(&bars->minpos, rp);
         if (!p.causal) row_pos[r] = INT32_MAX;
       }
       lse[r] = l;
@@ -834,7 +907,6 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
 
   // ---- pass 2: thread = key q * 32 + lane of its half's tiles, over every
   // row; max (or mean) of exp2(s - lse), written directly
-  const int32_t minpos = bars->minpos;
   const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
   const int nrec = p.step + 1 < p.W ? static_cast<int>(p.step + 1) : p.W;
   const float inv_rows = 1.f / static_cast<float>(max((nrec + nb) * p.G, 1));
@@ -842,9 +914,8 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
   const int nchunks = (N + 31) / 32;
   constexpr bool is_max = kMax;
   const int key = q * 32 + lane;
-  // the first pass-2 iteration of this half (iterations nt .. 2 nt - 1)
-  const int i0 = nt + ((h - nt) & 1);
-  for (int i = i0; i < 2 * nt; i += 2) {
+  for (int i = nt + ((h - g0 - nt) & 1); i < 2 * nt; i += 2) {
+    const int g = g0 + i;
     const int ti = i - nt;
     const int j = ti * kTileKeys + key;
     // a tile whose largest key position is at most every row's position
@@ -853,9 +924,9 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
     const int32_t kpj = tile_open ? INT32_MIN : (j < L ? kpu[j] : INT32_MAX);
     float r0 = -INFINITY, r1 = -INFINITY, r2 = -INFINITY, r3 = -INFINITY;  // max
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;                          // mean
-    if (warp_wait(&bars->tfull[i % kNBuf], (i / kNBuf) & 1, &bars->abort_flag, p.wait_ns)) {
+    if (warp_wait(&bars->tfull[g % kNBuf], (g / kNBuf) & 1, &bars->abort_flag, p.wait_ns)) {
       tc_fence_after();
-      const uint32_t buf = acc_of(i);
+      const uint32_t buf = acc_of(g);
       const bool nomask = tile_open || __all_sync(0xffffffffu, kpj <= minpos);
       const int32_t kpm = nomask ? INT32_MIN : kpj;
       // chunks of 32 rows in pairs: both TMEM loads issued before one wait
@@ -870,7 +941,7 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
         if (c + 2 >= nchunks) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) arrive_tempty(&bars->tempty[i % kNBuf]);
+          if (lane == 0) arrive_tempty(&bars->tempty[g % kNBuf]);
         }
         const int nv = min(two ? 64 : 32, N - c * 32);  // valid rows here (multiple of 16)
         const float4* l4 = reinterpret_cast<const float4*>(lse + c * 32);
@@ -927,8 +998,20 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
   }
 }
 
-template <int D, int NS, int NR>
-__global__ void __launch_bounds__(kFusedThreads, 1)
+// Both passes in one persistent kernel: CTA b scores units b, b + G, b + 2G,
+// ... (G = gridDim.x, at most one CTA per SM), and its roles overlap
+// consecutive units: the key tiles of the next unit load while the current
+// one finishes, and the next query operand is built as soon as the MMAs of
+// the current one are done with the single query image.
+//   warp 0      TMA: per unit, the largest key position of each tile, then
+//               every tile twice (pass 1, then pass 2) through the ring;
+//   warp 1      MMA: pass 1 D[row][key] = Q . K (rows on the TMEM lanes),
+//               pass 2 D[key][row] = K . Q (keys on the lanes);
+//   warps 2-3   query build of the next unit (all warps but the TMA warp
+//               build the first unit's together);
+//   warps 4-11  epilogue (fused_epilogue).
+template <int D, int NS, int NR, bool kMax>
+__global__ void __launch_bounds__(kPersistThreads, 1)
     score_fused_kernel(const __grid_constant__ ScoreParams p,
                        const __grid_constant__ CUtensorMap kmap) {
   pdl_trigger();  // select + compact may set up; it waits for this grid before reading it
@@ -953,20 +1036,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   uint8_t* q_hi = smem;
   uint8_t* q_lo = q_hi + kQBytes;
   uint8_t* stages = q_lo + kQBytes;
-  Barriers* bars = reinterpret_cast<Barriers*>(stages + NS * kStageBytes);
-  int32_t* row_pos = reinterpret_cast<int32_t*>(bars + 1);  // [kRows]
-  float* lse = reinterpret_cast<float*>(row_pos + kRows);    // [kRows]
-  float2* mz = reinterpret_cast<float2*>(lse + kRows);        // [kRows] second half's (m, z)
-  float* part = reinterpret_cast<float*>(mz + kRows);         // [2][128] second half's maxima
-  int32_t* kp = reinterpret_cast<int32_t*>(part + 256);       // [2][128] pass-1 key positions + [2][4] chunk maxima
-  float2* cs = reinterpret_cast<float2*>(kp + 264);           // [max(W,1)][D/2]
-  int32_t* tmax = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(cs) + cs_bytes(p.W, D));  // [kTmaxTiles]
+  FusedBars* bars = reinterpret_cast<FusedBars*>(stages + NS * kStageBytes);
+  int32_t* row_pos = reinterpret_cast<int32_t*>(bars + 1);  // [2][kRows], by unit parity
+  float* lse = reinterpret_cast<float*>(row_pos + 2 * kRows);  // [kRows]
+  float2* mz = reinterpret_cast<float2*>(lse + kRows);         // [kRows] second half's (m, z)
+  int32_t* kp = reinterpret_cast<int32_t*>(mz + kRows);        // [2][128] pass-1 key positions
+  float2* cs = reinterpret_cast<float2*>(kp + 256);            // [max(W,1)][D/2 + 4]
+  int32_t* tmax = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(cs) + cs_bytes(p.W, D));  // [2][kTmaxTiles]
 
-  const int u = blockIdx.x;
+  const int G = gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int t0, t1, L;
-  split_tiles(p, u, 0, t0, t1, L);  // tiles_per_split covers the whole cache here
-  const int nt = t1 - t0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -975,12 +1054,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     for (int i = 0; i < kNBuf; ++i) {
       mbar_init(&bars->tfull[i], 1);
-      mbar_init(&bars->tempty[i], 8);  // one arrival per epilogue warp
+      mbar_init(&bars->tempty[i], 8);  // two per warp of the owning half
     }
-    mbar_init(&bars->tmax_ready, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->qfull[b], 1);
+      mbar_init(&bars->tready[b], 1);
+      mbar_init(&bars->edone[b], 8);  // one per epilogue warp
+    }
+    mbar_init(&bars->qempty, 1);
     bars->abort_flag = 0;
-    bars->minpos = INT32_MAX;
-    bars->minrow = INT32_MAX;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -992,93 +1074,109 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
 
+  // the first unit's query operand: every warp but the TMA warp
+  if (warp >= 1) {
+    build_queries<D>(p, blockIdx.x, 0, kRows, q_hi, q_lo, row_pos, cs, threadIdx.x - 32,
+                     kPersistThreads - 32, 1);
+    if (warp == 2) publish_rows(p, row_pos, kRows, bars, 0);
+  }
+
   if (warp == 0) {
-    // ---------------- TMA producer: every tile twice (pass 1, then pass 2).
-    // Iteration i loads tile i % nt.  (An L2 run-ahead of bulk prefetches
+    // ---------------- TMA producer.  (An L2 run-ahead of bulk prefetches
     // measured slower and, on long caches, re-read tiles from HBM.)
-    const int niter = 2 * nt;
-    auto issue = [&](int i) {  // stage i % NS is free
-      const int st = i % NS;
-      mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
-      const int j0 = (i % nt) * kTileKeys;
-#pragma unroll
-      for (int a = 0; a < D / 64; ++a)
-        tma_load_3d(stages + st * kStageBytes + a * 16384, &kmap, &bars->full[st], 64 * a, j0, u);
-    };
-    const int first = min(NS, niter);
     if (lane == 0) prefetch_tmap(&kmap);
-    // Largest key position of every tile (keys past L count as unbounded),
-    // while the first tiles load.  Lane l reads keys 4l .. 4l + 3 of a tile
-    // with one 16-byte load (the address clamped into the row; clamped
-    // loads only cover keys past L), so sixteen tiles' loads are in flight
-    // before any is reduced.  Rows that are not 16-byte aligned take
-    // element loads.
-    {
-      const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
-      const bool vec = (reinterpret_cast<uintptr_t>(p.kpos) & 15u) == 0 && (p.L_cap & 3) == 0 &&
-                       p.L_cap >= 4;
-      const int ntm = min(nt, kTmaxTiles);
-      for (int t0 = 0; t0 < ntm; t0 += 16) {
-        int32_t mx[16];
-        if (vec) {
+    int g = 0, n = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.U && ok; u += G, ++n) {
+      int t0, t1, L;
+      split_tiles(p, u, 0, t0, t1, L);  // tiles_per_split covers the whole cache here
+      const int nt = t1 - t0;
+      // the epilogue is done with the tile maxima of two units back
+      if (n >= 2 &&
+          !warp_wait(&bars->edone[n & 1], ((n - 2) >> 1) & 1, &bars->abort_flag, p.wait_ns)) {
+        if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+        break;
+      }
+      // Largest key position of every tile (keys past L count as
+      // unbounded).  Lane l reads keys 4l .. 4l + 3 of a tile with one
+      // 16-byte load (the address clamped into the row; clamped loads only
+      // cover keys past L), so sixteen tiles' loads are in flight before any
+      // is reduced.  Rows that are not 16-byte aligned take element loads.
+      {
+        int32_t* tm = tmax + (n & 1) * kTmaxTiles;
+        const int32_t* kpu = p.kpos + static_cast<size_t>(u) * p.L_cap;
+        const bool vec = (reinterpret_cast<uintptr_t>(p.kpos) & 15u) == 0 &&
+                         (p.L_cap & 3) == 0 && p.L_cap >= 4;
+        const int ntm = min(nt, kTmaxTiles);
+        for (int ta = 0; ta < ntm; ta += 16) {
+          int32_t mx[16];
+          if (vec) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int j = (t0 + k) * kTileKeys + 4 * lane;
-            const int4 v = *reinterpret_cast<const int4*>(kpu + min(j, p.L_cap - 4));
-            mx[k] = max(max(j < L ? v.x : INT32_MAX, j + 1 < L ? v.y : INT32_MAX),
-                        max(j + 2 < L ? v.z : INT32_MAX, j + 3 < L ? v.w : INT32_MAX));
-          }
-        } else {
+            for (int k = 0; k < 16; ++k) {
+              const int j = (ta + k) * kTileKeys + 4 * lane;
+              const int4 v = *reinterpret_cast<const int4*>(kpu + min(j, p.L_cap - 4));
+              mx[k] = max(max(j < L ? v.x : INT32_MAX, j + 1 < L ? v.y : INT32_MAX),
+                          max(j + 2 < L ? v.z : INT32_MAX, j + 3 < L ? v.w : INT32_MAX));
+            }
+          } else {
 #pragma unroll 1
+            for (int k = 0; k < 16; ++k) {
+              const int j = (ta + k) * kTileKeys + 4 * lane;
+              int32_t m = INT32_MIN;
+              for (int e = 0; e < 4; ++e) m = max(m, j + e < L ? kpu[j + e] : INT32_MAX);
+              mx[k] = m;
+            }
+          }
+#pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const int j = (t0 + k) * kTileKeys + 4 * lane;
-            int32_t m = INT32_MIN;
-            for (int e = 0; e < 4; ++e) m = max(m, j + e < L ? kpu[j + e] : INT32_MAX);
-            mx[k] = m;
+            const int32_t r = __reduce_max_sync(0xffffffffu, mx[k]);
+            if (lane == 0 && ta + k < ntm) tm[ta + k] = r;
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->tready[n & 1]);
+      }
+      // every tile twice: iteration i loads tile i % nt
+      if (lane == 0) {
+        for (int i = 0; i < 2 * nt; ++i, ++g) {
+          const int st = g % NS;
+          if (*reinterpret_cast<volatile int32_t*>(&bars->abort_flag) != 0 ||
+              !wait_bar(&bars->empty[st], ((g / NS) & 1) ^ 1, p.wait_ns)) {
+            bars->abort_flag = 1;
+            record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->full[st], kStageBytes);
+          const int j0 = (i % nt) * kTileKeys;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int32_t r = __reduce_max_sync(0xffffffffu, mx[k]);
-          if (lane == 0 && t0 + k < ntm) tmax[t0 + k] = r;
+          for (int a = 0; a < D / 64; ++a)
+            tma_load_3d(stages + st * kStageBytes + a * 16384, &kmap, &bars->full[st], 64 * a,
+                        j0, u);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tmax_ready);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      g = __shfl_sync(0xffffffffu, g, 0);
     }
-    // The small loads above and the query build's go first; the first tiles
-    // follow.
-    if (lane == 0) {
-      for (int i = 0; i < first; ++i) issue(i);
-      int issued = first;
-      for (int i = first; i < niter; ++i) {
-        const int st = i % NS;
-        if (*reinterpret_cast<volatile int32_t*>(&bars->abort_flag) != 0 ||
-            !wait_bar(&bars->empty[st], ((i / NS) & 1) ^ 1, p.wait_ns)) {
-          bars->abort_flag = 1;
-          record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
-          break;
-        }
-        issue(i);
-        issued = i + 1;
-      }
-      drain_loads(bars->full, NS, issued, p.wait_ns);
-    }
+    // every load has landed before the CTA can leave (bounded)
+    if (lane == 0) drain_loads(bars->full, NS, g, p.wait_ns);
     __syncwarp();
-  } else {
-    build_queries<D>(p, u, 0, kRows, q_hi, q_lo, row_pos, cs, threadIdx.x - 32,
-                     kFusedThreads - 32, 1);
-    if (warp == 1) {
-      // ---------------- MMA issuer
-      const uint32_t idesc2 = idesc_bf16_f32(128, static_cast<uint32_t>(p.NQ16));
-      int last = -1;
-      for (int i = 0; i < (p.stall ? 0 : 2 * nt); ++i) {
-        const int st = i % NS, b = i % kNBuf;
-        if (!warp_wait(&bars->full[st], (i / NS) & 1, &bars->abort_flag, p.wait_ns) ||
-            !warp_wait(&bars->tempty[b], ((i / kNBuf) & 1) ^ 1, &bars->abort_flag, p.wait_ns)) {
-          if (lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
-          break;
-        }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    const uint32_t idesc2 = idesc_bf16_f32(128, static_cast<uint32_t>(p.NQ16));
+    int g = 0, n = 0, commits = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < (p.stall ? 0 : p.U) && ok; u += G, ++n) {
+      int t0, t1, L;
+      split_tiles(p, u, 0, t0, t1, L);
+      const int nt = t1 - t0;
+      ok = warp_wait(&bars->qfull[n & 1], (n >> 1) & 1, &bars->abort_flag, p.wait_ns);
+      tc_fence_after();
+      for (int i = 0; i < 2 * nt && ok; ++i, ++g) {
+        const int st = g % NS, b = g % kNBuf;
+        ok = warp_wait(&bars->full[st], (g / NS) & 1, &bars->abort_flag, p.wait_ns) &&
+             warp_wait(&bars->tempty[b], ((g / kNBuf) & 1) ^ 1, &bars->abort_flag, p.wait_ns);
+        if (!ok) break;
         tc_fence_after();
         if (elect_one()) {
           const uint32_t dt = tbase + b * kBufCols;
@@ -1116,16 +1214,101 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           mma_commit(&bars->tfull[b]);
         }
         __syncwarp();
-        last = i;
       }
-      if (last >= 0) wait_bar(&bars->tfull[last % kNBuf], (last / kNBuf) & 1, p.wait_ns);
-    } else {
-      if (p.agg == BKV_AGG_MAX)
-        fused_epilogue<D, NR, kBufCols, kNBuf, true>(p, u, nt, L, tbase, bars, row_pos, lse, mz, part,
-                                              kp, tmax);
-      else
-        fused_epilogue<D, NR, kBufCols, kNBuf, false>(p, u, nt, L, tbase, bars, row_pos, lse, mz, part,
-                                               kp, tmax);
+      if (!ok && lane == 0) record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+      // the query image is free once this unit's MMAs have finished (a
+      // commit even after a failed wait: it covers every MMA issued)
+      if (elect_one()) mma_commit(&bars->qempty);
+      __syncwarp();
+      ++commits;
+    }
+    // no MMA may still write TMEM when the CTA leaves (bounded)
+    if (commits > 0) wait_bar(&bars->qempty, (commits - 1) & 1, p.wait_ns);
+  } else if (warp < 4) {
+    // ---------------- query build of the units after the first (64
+    // threads), in two steps so that the global loads and the cos/sin table
+    // overlap the wait for the query image: (1) once the epilogue is done
+    // with the row positions of two units back: table, row positions and
+    // the first batch of raw query rows into registers; (2) once the MMAs
+    // of the previous unit are done with the image: rotate, split, store,
+    // and the remaining batches.  The raw rows of the unit after are then
+    // pulled into L2 and its position read.
+    constexpr int kGroups = D / 16;
+    constexpr int kTotal = kRows * kGroups;
+    constexpr int kPer = kTotal / 64;           // items per builder thread
+    constexpr int kB = kPer < 8 ? kPer : 8;     // items per batch
+    static_assert(kPer % kB == 0, "whole batches");
+    const int bt = threadIdx.x - 64;
+    auto pull_rows = [&](int un) {
+      const size_t rb = static_cast<size_t>(p.W) * p.G * D * 2;
+      const size_t bb = static_cast<size_t>(p.M) * p.G * D * 2;
+      const uint8_t* r0 = reinterpret_cast<const uint8_t*>(p.recent_q) + un * rb;
+      for (size_t o = static_cast<size_t>(bt) * 128; o < rb; o += 64 * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(r0 + o));
+      if (bb > 0) {
+        const uint8_t* b0 = reinterpret_cast<const uint8_t*>(p.beacons) + un * bb;
+        for (size_t o = static_cast<size_t>(bt) * 128; o < bb; o += 64 * 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(b0 + o));
+      }
+    };
+    int n = 1;
+    int u = blockIdx.x + G;
+    int32_t cur = 0;
+    if (u < p.U) {
+      pull_rows(u);
+      cur = p.cur_pos[u];
+    }
+    for (; u < p.U; u += G, ++n) {
+      bool ok = n < 2 || warp_wait(&bars->edone[n & 1], ((n - 2) >> 1) & 1, &bars->abort_flag,
+                                   p.wait_ns);
+      // both builder warps leave together (they meet at named barriers)
+      if (named_sync_or(5, 64, !ok)) break;
+      int32_t* rp = row_pos + (n & 1) * kRows;
+      build_cs_table<D>(p, cur, cs, bt, 64);
+      uint4 va[kB], vb[kB];
+      load_query_batch<D, kB>(p, u, 0, kTotal, bt, 64, va, vb);
+      const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
+      for (int r = bt; r < kRows; r += 64) rp[r] = row_position(p, u, r, nb, cur);
+      named_sync(5, 64);
+      ok = warp_wait(&bars->qempty, (n - 1) & 1, &bars->abort_flag, p.wait_ns);
+      if (named_sync_or(5, 64, !ok)) break;
+#pragma unroll 1
+      for (int k = 0; k < kPer; k += kB) {
+        if (k > 0) load_query_batch<D, kB>(p, u, 0, kTotal, bt + k * 64, 64, va, vb);
+        store_query_batch<D, kB>(p, kRows, kTotal, bt + k * 64, 64, va, vb, rp, cs, cur, q_hi,
+                                 q_lo);
+      }
+      fence_proxy_async_shared();  // generic smem writes -> visible to the tensor core
+      named_sync(5, 64);
+      if (warp == 2) publish_rows(p, rp, kRows, bars, n & 1);
+      if (u + G < p.U) {
+        pull_rows(u + G);
+        cur = p.cur_pos[u + G];
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 4..11)
+    int g0 = 0, n = 0;
+    for (int u = blockIdx.x; u < p.U; u += G, ++n) {
+      int t0, t1, L;
+      split_tiles(p, u, 0, t0, t1, L);
+      const int nt = t1 - t0;
+      if (!(warp_wait(&bars->qfull[n & 1], (n >> 1) & 1, &bars->abort_flag, p.wait_ns) &&
+            warp_wait(&bars->tready[n & 1], (n >> 1) & 1, &bars->abort_flag, p.wait_ns)) &&
+          lane == 0)
+        record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+      int32_t* rp = row_pos + (n & 1) * kRows;
+      const int32_t* tm = tmax + (n & 1) * kTmaxTiles;
+      const int32_t minrow = bars->minrow[n & 1], minpos = bars->minpos[n & 1];
+      fused_epilogue<D, NR, kBufCols, kNBuf, kMax>(p, u, nt, L, g0, tbase, bars, rp, lse, mz, kp,
+                                                   tm, minrow, minpos);
+      g0 += 2 * nt;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->edone[n & 1]);
+      // all epilogue warps leave together once any wait has failed
+      if (named_sync_or(2, kFusedEpi,
+                        *reinterpret_cast<volatile int32_t*>(&bars->abort_flag) != 0))
+        break;
     }
   }
   tc_fence_before();
@@ -1415,8 +1598,8 @@ size_t cluster_smem(int W) {
 template <int D, int NS, int NR>
 size_t fused_smem(int W) {
   return 1024 + 2 * static_cast<size_t>(NR) * 128 * D * 2 + NS * kTileKeys * D * 2 +
-         sizeof(Barriers) + NR * 128 * (4 + 4 + 8) + 256 * 4 + 264 * 4 +
-         cs_bytes(W, D) + kTmaxTiles * 4;
+         sizeof(FusedBars) + NR * 128 * (2 * 4 + 4 + 8) + 256 * 4 + cs_bytes(W, D) +
+         2 * kTmaxTiles * 4;
 }
 
 template <int D, int NS>
@@ -1428,6 +1611,17 @@ template <int D, int NS, int NMAX>
 size_t final_smem(int W) {
   return 1024 + 2 * NMAX * D * 2 + NS * kTileKeys * D * 2 + sizeof(Barriers) + 256 * 4 +
          256 * 4 + cs_bytes(W, D);
+}
+
+int num_sms() {
+  static const int n = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      return 148;
+    return v;
+  }();
+  return n;
 }
 
 // pdl: launched as a programmatic dependent of the previous kernel of the
@@ -1498,18 +1692,31 @@ cudaError_t launch_score(const ScoreParams& p, const CUtensorMap& kmap, cudaStre
     return cudaGetLastError();
   }
   if (p.fused) {
-    const dim3 g(p.U);
+    // persistent: at most one CTA per SM, each taking units b, b + G, ...
+    const dim3 g(static_cast<unsigned>(p.U < num_sms() ? p.U : num_sms()));
     const bool one = p.NQ16 <= 128;
-    const int T = kFusedThreads;
-    if (p.d == 128)
-      return one ? launch(score_fused_kernel<128, 4, 1>, g, fused_smem<128, 4, 1>(p.W), st, p,
-                          kmap, T, true)
-                 : launch(score_fused_kernel<128, 2, 2>, g, fused_smem<128, 2, 2>(p.W), st, p,
-                          kmap, T, true);
-    return one ? launch(score_fused_kernel<64, 4, 1>, g, fused_smem<64, 4, 1>(p.W), st, p, kmap, T,
-                        true)
-               : launch(score_fused_kernel<64, 4, 2>, g, fused_smem<64, 4, 2>(p.W), st, p, kmap,
-                        T, true);
+    const int T = kPersistThreads;
+    // max or mean aggregation as separate kernels (one epilogue each keeps
+    // the register allocation free of spills)
+    const bool mx = p.agg == BKV_AGG_MAX;
+    if (p.d == 128) {
+      if (one) {
+        const size_t sm = fused_smem<128, 4, 1>(p.W);
+        return mx ? launch(score_fused_kernel<128, 4, 1, true>, g, sm, st, p, kmap, T, true)
+                  : launch(score_fused_kernel<128, 4, 1, false>, g, sm, st, p, kmap, T, true);
+      }
+      const size_t sm = fused_smem<128, 2, 2>(p.W);
+      return mx ? launch(score_fused_kernel<128, 2, 2, true>, g, sm, st, p, kmap, T, true)
+                : launch(score_fused_kernel<128, 2, 2, false>, g, sm, st, p, kmap, T, true);
+    }
+    if (one) {
+      const size_t sm = fused_smem<64, 4, 1>(p.W);
+      return mx ? launch(score_fused_kernel<64, 4, 1, true>, g, sm, st, p, kmap, T, true)
+                : launch(score_fused_kernel<64, 4, 1, false>, g, sm, st, p, kmap, T, true);
+    }
+    const size_t sm = fused_smem<64, 4, 2>(p.W);
+    return mx ? launch(score_fused_kernel<64, 4, 2, true>, g, sm, st, p, kmap, T, true)
+              : launch(score_fused_kernel<64, 4, 2, false>, g, sm, st, p, kmap, T, true);
   }
   const dim3 g1(p.nsplit, p.nrows_part / 128, p.U);
   const dim3 g2(p.nsplit, p.ngrp, p.U);

@@ -596,3 +596,50 @@ def test_score_parity_single_pass_cluster_shapes(L_cap, Ls, causal):
     sg = st.scores.cpu().numpy()
     for u, n in enumerate(Ls):
         assert np.all(sg[u, n:] == -1.0), "wrote past L"
+
+
+@pytest.mark.parametrize("shape,U,L_cap", [("c1", 600, None), ("c3", 400, None),
+                                             ("c4m16", 300, 640)])
+def test_score_parity_persistent_fused(shape, U, L_cap):
+    """The two-pass kernel is persistent: CTA b scores units b, b + G, ...
+    (G CTAs, at most one per SM), overlapping one unit's tail with the next
+    unit's key loads and query build.  Up to five units per CTA (64-, 128-
+    and 256-row operands, head dims 64 and 128), ragged lengths including
+    empty units, one key and full caches, against the oracle on every unit,
+    and the same bits on a second call.  Units are a tiled pool of distinct
+    seeded units."""
+    cfg = {"c1": wl.CONFIGS[1], "c3": wl.CONFIGS[3], "c4m16": wl.config4(16)}[shape]
+    pool = 24
+    base = wl.make_units(cfg, range(pool))
+    if L_cap is not None:
+        for k in ("K", "V", "kpos"):
+            base[k] = np.ascontiguousarray(base[k][:, :L_cap])
+        cfg = cfg.with_(B_KV=min(cfg.B_KV, L_cap))
+    idx = np.arange(U) % pool
+    units = {k: (v[idx] if getattr(v, "ndim", 0) else v) for k, v in base.items()}
+    n = units["K"].shape[1]
+    rng = np.random.default_rng(U + n)
+    Ls = rng.integers(1, n + 1, size=U)
+    Ls[:6] = [n, 0, 1, 128, 129, n - 1]
+    units["L"] = Ls.astype(np.int32)
+    st = DeviceState(units, cfg)
+    beacons = {}
+    for u in range(pool):
+        un = _unit(base, u)
+        cb = oracle.ContinualBuffer.from_state(un["buf"], int(un["cnt"]), cfg.M)
+        beacons[u] = cb.beacons()[1]
+    for u in range(U):
+        vec = beacons[u % pool]
+        st.nb[u] = len(vec)
+        if len(vec):
+            st.beac[u, : len(vec)] = dev(vec.reshape(len(vec), cfg.G, cfg.d))
+    st.score()
+    assert st.status() == 0
+    _score_check(cfg, units, st)
+    sg = st.scores.cpu().numpy()
+    for u, n_ in enumerate(Ls):
+        assert np.all(sg[u, n_:] == -1.0), "wrote past L"
+    first = sg.copy()
+    st.score()
+    assert st.status() == 0
+    assert np.array_equal(st.scores.cpu().numpy(), first)
