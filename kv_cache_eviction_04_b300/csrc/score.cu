@@ -765,14 +765,17 @@ struct __align__(16) FusedBars {
   uint64_t empty[8];
   uint64_t tfull[4];   // accumulator buffers: 4 (128 rows) or 2 (256 rows)
   uint64_t tempty[4];
-  uint64_t qfull[2];   // a unit's query image and row positions are in place
+  uint64_t qfull[2];   // a unit's query image is in place (its two builders)
   uint64_t qempty;     // the MMAs of a unit are done with the query image
   uint64_t tready[2];  // a unit's per-tile key-position maxima are in place
   uint64_t edone[2];   // the epilogue is done with a unit (8 warps)
+  uint64_t bready[2];  // a unit's cos/sin table and row positions are in place
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t minrow[2];   // smallest key-position limit over a unit's live rows
   int32_t minpos[2];   // smallest position over a unit's live rows
+  int32_t cur[2];      // a unit's current position
+  int32_t pad[2];
 };
 static_assert(sizeof(FusedBars) % 16 == 0, "arrays after the barriers need 16-byte alignment");
 
@@ -781,9 +784,10 @@ static_assert(sizeof(FusedBars) % 16 == 0, "arrays after the barriers need 16-by
 constexpr int kPersistThreads = 384;
 
 // One warp: the smallest key-position limit and the smallest position over
-// the live rows of a unit's query build, then the build is announced.
+// the live rows of a unit's query build, then `count` arrivals on `bar`.
 __device__ __forceinline__ void publish_rows(const ScoreParams& p, const int32_t* rp, int nrows,
-                                             FusedBars* bars, int b) {
+                                             FusedBars* bars, int b, uint64_t* bar,
+                                             uint32_t count) {
   const int lane = threadIdx.x & 31;
   int32_t lw = INT32_MAX, pw = INT32_MAX;
   for (int r = lane; r < nrows; r += 32) {
@@ -798,10 +802,17 @@ __device__ __forceinline__ void publish_rows(const ScoreParams& p, const int32_t
   if (lane == 0) {
     bars->minrow[b] = lw;
     bars->minpos[b] = pw;
-    mbar_arrive(&bars->qfull[b]);
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
   }
   __syncwarp();
 }
+
+// The query build of a unit after the first is shared: the builder warps
+// take items [0, kBuildSplit * total) as soon as the MMAs of the previous
+// unit are done with the image, the epilogue the rest once it has finished
+// the previous unit.
+constexpr int kBuildSplitNum = 3, kBuildSplitDen = 8;
 
 // Epilogue of one unit (warps 4..11).  Iteration i of the unit (tile i in
 // pass 1, tile i - nt in pass 2) is the kernel's iteration g0 + i: it uses
@@ -1057,9 +1068,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       mbar_init(&bars->tempty[i], 8);  // two per warp of the owning half
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->qfull[b], 1);
+      mbar_init(&bars->qfull[b], 2);  // the builders' part and the epilogue's part
       mbar_init(&bars->tready[b], 1);
       mbar_init(&bars->edone[b], 8);  // one per epilogue warp
+      mbar_init(&bars->bready[b], 1);
     }
     mbar_init(&bars->qempty, 1);
     bars->abort_flag = 0;
@@ -1078,7 +1090,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
   if (warp >= 1) {
     build_queries<D>(p, blockIdx.x, 0, kRows, q_hi, q_lo, row_pos, cs, threadIdx.x - 32,
                      kPersistThreads - 32, 1);
-    if (warp == 2) publish_rows(p, row_pos, kRows, bars, 0);
+    if (warp == 2) {
+      publish_rows(p, row_pos, kRows, bars, 0, &bars->qfull[0], 2);
+      // unit 0 takes phase 0 of bready[0] too, so that unit n waits for
+      // phase n / 2 of bready[n % 2]
+      if (lane == 0) mbar_arrive(&bars->bready[0]);
+    }
   }
 
   if (warp == 0) {
@@ -1226,18 +1243,18 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     if (commits > 0) wait_bar(&bars->qempty, (commits - 1) & 1, p.wait_ns);
   } else if (warp < 4) {
     // ---------------- query build of the units after the first (64
-    // threads), in two steps so that the global loads and the cos/sin table
-    // overlap the wait for the query image: (1) once the epilogue is done
-    // with the row positions of two units back: table, row positions and
-    // the first batch of raw query rows into registers; (2) once the MMAs
-    // of the previous unit are done with the image: rotate, split, store,
-    // and the remaining batches.  The raw rows of the unit after are then
-    // pulled into L2 and its position read.
+    // threads).  (1) Once the epilogue is done with the row positions of two
+    // units back: the cos/sin table, the row positions and the first batch
+    // of this role's raw query rows, then the epilogue may join.  (2) Once
+    // the MMAs of the previous unit are done with the image: rotate, split
+    // and store this role's items (the epilogue stores the rest).  The raw
+    // rows of the unit after are then pulled into L2 and its position read.
     constexpr int kGroups = D / 16;
     constexpr int kTotal = kRows * kGroups;
-    constexpr int kPer = kTotal / 64;           // items per builder thread
-    constexpr int kB = kPer < 8 ? kPer : 8;     // items per batch
-    static_assert(kPer % kB == 0, "whole batches");
+    constexpr int kX = kTotal * kBuildSplitNum / kBuildSplitDen;  // the builders' items
+    constexpr int kPer = kX / 64;                 // items per builder thread
+    constexpr int kB = kPer <= 6 ? kPer : kPer / 2;  // items per batch
+    static_assert(kX % 64 == 0 && kPer % kB == 0, "whole batches");
     const int bt = threadIdx.x - 64;
     auto pull_rows = [&](int un) {
       const size_t rb = static_cast<size_t>(p.W) * p.G * D * 2;
@@ -1270,6 +1287,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
       for (int r = bt; r < kRows; r += 64) rp[r] = row_position(p, u, r, nb, cur);
       named_sync(5, 64);
+      if (warp == 2) {
+        if (lane == 0) bars->cur[n & 1] = cur;
+        publish_rows(p, rp, kRows, bars, n & 1, &bars->bready[n & 1], 1);
+      }
       ok = warp_wait(&bars->qempty, (n - 1) & 1, &bars->abort_flag, p.wait_ns);
       if (named_sync_or(5, 64, !ok)) break;
 #pragma unroll 1
@@ -1280,7 +1301,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       }
       fence_proxy_async_shared();  // generic smem writes -> visible to the tensor core
       named_sync(5, 64);
-      if (warp == 2) publish_rows(p, rp, kRows, bars, n & 1);
+      if (bt == 0) mbar_arrive(&bars->qfull[n & 1]);
       if (u + G < p.U) {
         pull_rows(u + G);
         cur = p.cur_pos[u + G];
@@ -1303,6 +1324,26 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       fused_epilogue<D, NR, kBufCols, kNBuf, kMax>(p, u, nt, L, g0, tbase, bars, rp, lse, mz, kp,
                                                    tm, minrow, minpos);
       g0 += 2 * nt;
+      // the epilogue's share of the next unit's query build (items
+      // [kX, total)); the builders have placed the table and row positions
+      if (u + G < p.U) {
+        constexpr int kTotal = kRows * (D / 16);
+        constexpr int kX = kTotal * kBuildSplitNum / kBuildSplitDen;
+        constexpr int kEB = (kTotal - kX + kFusedEpi - 1) / kFusedEpi;
+        const int nn = n + 1, et = threadIdx.x - 128;
+        if (warp_wait(&bars->bready[nn & 1], (nn >> 1) & 1, &bars->abort_flag, p.wait_ns)) {
+          const int32_t cur = bars->cur[nn & 1];
+          uint4 va[kEB], vb[kEB];
+          load_query_batch<D, kEB>(p, u + G, 0, kTotal, kX + et, kFusedEpi, va, vb);
+          store_query_batch<D, kEB>(p, kRows, kTotal, kX + et, kFusedEpi, va, vb,
+                                    row_pos + (nn & 1) * kRows, cs, cur, q_hi, q_lo);
+          fence_proxy_async_shared();  // generic smem writes -> visible to the tensor core
+        } else if (lane == 0) {
+          record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
+        }
+        named_sync(2, kFusedEpi);
+        if (et == 0) mbar_arrive(&bars->qfull[nn & 1]);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->edone[n & 1]);
       // all epilogue warps leave together once any wait has failed
