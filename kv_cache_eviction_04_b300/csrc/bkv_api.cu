@@ -387,7 +387,7 @@ int bkv_fps_update(const bkv_dims* dims, const void* q_new, int64_t step, void* 
   // and compresses only the buffers that step filled.
   if (q_new != nullptr && want_beacons == 0 && !cluster)
     return cuda_rc(bkv::launch_fps_append_compress(p, map, sm_count(), st));
-  return cuda_rc(cluster ? bkv::launch_fps_cluster(p, map, st) : bkv::launch_fps(p, map, st));
+  return cuda_rc(cluster ? bkv::launch_fps_cluster(p, map, st) : bkv::launch_fps(p, map, sm_count(), st));
 }
 
 int bkv_score(const bkv_dims* dims, const void* K, const int32_t* L, const int32_t* kpos,
@@ -438,7 +438,7 @@ int bkv_round(const bkv_dims* dims, const void* q_new, int64_t step, void* recen
   // before it waits for the selection
   sp.early_reads = 1;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  v = cuda_rc(cluster ? bkv::launch_fps_cluster(fp, fmap, st) : bkv::launch_fps(fp, fmap, st));
+  v = cuda_rc(cluster ? bkv::launch_fps_cluster(fp, fmap, st) : bkv::launch_fps(fp, fmap, sm_count(), st));
   if (v != BKV_OK) return v;
   v = cuda_rc(bkv::launch_score(sp, smap, st));
   if (v != BKV_OK) return v;

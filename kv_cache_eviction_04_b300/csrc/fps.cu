@@ -50,6 +50,7 @@ struct __align__(16) FpsShared {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t done;
+  uint64_t seeded;           // the eight item warps are past the seed (its scratch is free)
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t n_sel;
@@ -71,6 +72,7 @@ struct __align__(16) FpsShared {
   int16_t pair_s[kMaxPairs];  // its chosen item
   int32_t ulist[kItems];      // compress pass: full units of the current batch
   int32_t ucount;
+  int32_t preloaded;          // Gram chunks of the next selection already loaded
 };
 
 // Barrier of the eight item warps only (the producer warp idles after the
@@ -283,6 +285,12 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
     // resident any more (the greedy steps read the buffer from global memory)
   }
 
+  // The stages are free from here on (the recheck's scratch is done with):
+  // the producer warp may load the next unit's chunks into them.
+  fence_proxy_async_shared();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sh->seeded);
+
   // ---- greedy farthest-point steps
   if (tid == 0) sh->sel[0] = seed;
   bool chosen = (i == seed);
@@ -375,10 +383,17 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
 // selection order to sh->sel and returns its length (all threads call).  A
 // CTA runs at most one non-trivial selection per launch (after a compress
 // the buffer holds M items and the beacon pass takes all of them), so the
-// mbarriers start from phase 0 here.
+// mbarriers start from phase 0 here, or the persistent beacon kernel
+// initialises them again between units.  sh->preloaded of the unit's first
+// Gram chunks are already loaded (or in flight) into their stages.  With
+// next_u >= 0 the producer warp loads that unit's first chunks during the
+// greedy steps (once the seed's scratch is free), initialising the
+// barriers again first, and leaves their count in sh->preloaded.
 __device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
-                          uint8_t* stages, int stage_rows, int u, int n, int m) {
+                          uint8_t* stages, int stage_rows, int u, int n, int m,
+                          int next_u) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pre = sh->preloaded;
   if (m <= 0) return 0;
   if (n <= m || p.first_m) {  // every item, or the first m (in slot order)
     const int got = min(n, m);
@@ -405,6 +420,7 @@ __device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bm
     mbar_arrive_expect_tx(&sh->full[st], box_bytes);
     tma_load_3d(stages + st * stage_bytes, bmap, &sh->full[st], 64 * c, 0, u);
   };
+  if (tid == kItems) sh->preloaded = 0;  // read by every thread above
 
   // ---- Gram on the tensor core.  One thread of the producer warp streams
   // 64-column chunks of the buffer into the stage ring by TMA and issues the
@@ -420,7 +436,7 @@ __device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bm
     if (lane == 0) {
       bool ok = true;
       const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(N));
-      for (int c = 0; c < min(kStages, nchunks); ++c) load_chunk(c, c);
+      for (int c = pre; c < min(kStages, nchunks); ++c) load_chunk(c, c);
       int next = min(kStages, nchunks);  // next chunk to load
       for (int c = 0; c < nchunks && ok; ++c) {
         // chunk c must have been loaded: block on its stage's release if not
@@ -491,8 +507,40 @@ __device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bm
   }
   __syncthreads();
   const bool gram_ok = sh->abort_flag == 0;  // block-uniform
-  if (warp < kItemWarps)
+  if (warp < kItemWarps) {
     fps_pick(p, sh, stages, tbase, gram_ok, u, n, m);
+  } else if (next_u >= 0 && lane == 0 && gram_ok) {
+    // the next unit's first chunks, while the item warps run the greedy
+    // steps: every wait on the barriers of this unit has completed (the
+    // Gram is done and the seed is past), so they start again from phase 0
+    // every arrival on the stage barriers has landed (the last phase of
+    // each stage is complete) before they are initialised again
+    bool quiet = wait_bar(&sh->seeded, 0);
+    for (int c = max(0, nchunks - kStages); c < nchunks && quiet; ++c)
+      quiet = wait_bar(&sh->empty[c % kStages], (c / kStages) & 1);
+    if (quiet) {
+      for (int st = 0; st < kStages; ++st) {
+        mbar_inval(&sh->full[st]);
+        mbar_inval(&sh->empty[st]);
+        mbar_init(&sh->full[st], 1);
+        mbar_init(&sh->empty[st], kItemWarps + 1);
+      }
+      mbar_inval(&sh->done);
+      mbar_inval(&sh->seeded);
+      mbar_init(&sh->done, 1);
+      mbar_init(&sh->seeded, kItemWarps);
+      fence_mbar_init();
+      const int k = min(kStages, nchunks);
+      for (int c = 0; c < k; ++c) {
+        mbar_arrive_expect_tx(&sh->full[c], box_bytes);
+        tma_load_3d(stages + c * stage_bytes, bmap, &sh->full[c], 64 * c, 0, next_u);
+      }
+      sh->preloaded = k;
+    } else {
+      sh->abort_flag = 1;
+      record_error(p.ws, BKV_ETIMEOUT, kSiteFpsWait);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -510,13 +558,16 @@ __device__ void init_fps_barriers(FpsShared* sh, bool again) {
       mbar_inval(&sh->empty[s]);
     }
     mbar_inval(&sh->done);
+    mbar_inval(&sh->seeded);
   }
   for (int s = 0; s < kStages; ++s) {
     mbar_init(&sh->full[s], 1);
     mbar_init(&sh->empty[s], kItemWarps + 1);  // every item warp read it + the MMAs ran
   }
   mbar_init(&sh->done, 1);
+  mbar_init(&sh->seeded, kItemWarps);
   sh->abort_flag = 0;
+  sh->preloaded = 0;
   fence_mbar_init();
 }
 
@@ -525,7 +576,7 @@ __device__ void init_fps_barriers(FpsShared* sh, bool again) {
 __device__ int compress_unit(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
                              uint8_t* stages, int stage_rows, int u, uint16_t* buf) {
   const int tid = threadIdx.x, D = p.D;
-  const int got = fps_select(p, bmap, sh, stages, stage_rows, u, p.C, p.M);
+  const int got = fps_select(p, bmap, sh, stages, stage_rows, u, p.C, p.M, -1);
   if (tid == 0) {
     for (int k = 0; k < got; ++k) sh->surv[k] = sh->sel[k];
     for (int a = 1; a < got; ++a) {  // insertion sort, got <= 64
@@ -607,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- 3. beacons: FPS over the current buffer (read-only)
   if (p.want_beacons) {
-    const int got = ok_state ? fps_select(p, &bmap, sh, stages, stage_rows, u, c, p.M) : 0;
+    const int got = ok_state ? fps_select(p, &bmap, sh, stages, stage_rows, u, c, p.M, -1) : 0;
     __syncthreads();
     if (p.beacon_idx != nullptr)
       for (int k = tid; k < p.M; k += kThreads)
@@ -623,6 +674,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.n_beacons != nullptr && tid == 0) p.n_beacons[u] = got;
   }
   if (tid == 0 && ok_state) p.cnt[u] = c;
+}
+
+// ---- Beacon selection alone (no append, so no count or buffer changes
+// here), persistent: CTA b selects for units b, b + G, ... (G at most the
+// SM count).  While the item warps run one unit's greedy steps the
+// producer warp loads the next unit's first Gram chunks, so the next Gram
+// starts with most of its buffer in shared memory.
+__device__ __forceinline__ bool runs_gram(const FpsParams& p, int u) {
+  const int c = p.cnt[u];
+  return c >= 0 && c < p.C && c > p.M && p.M > 0 && !p.first_m;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fps_beacons_kernel(const __grid_constant__ FpsParams p,
+                       const __grid_constant__ CUtensorMap bmap, int stage_rows) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+  FpsShared* sh = reinterpret_cast<FpsShared*>(stages + kStages * stage_rows * 128);
+  const int tid = threadIdx.x, G = gridDim.x;
+  pdl_trigger();  // scoring may set up on free SMs; it waits for this grid before reading it
+  const int D = p.D;
+  if (tid == 0) init_fps_barriers(sh, false);
+  __syncthreads();
+  for (int u = blockIdx.x; u < p.U; u += G) {
+    const uint16_t* buf = p.buf + static_cast<size_t>(u) * p.C * D;
+    int c = p.cnt[u];
+    const bool ok_state = c >= 0 && c < p.C;
+    if (!ok_state) {
+      if (tid == 0) record_error(p.ws, BKV_EDEVICE, kSiteFpsState);
+      c = 0;
+    }
+    const int un = u + G;
+    const int next = (un < p.U && runs_gram(p, un)) ? un : -1;
+    const int got = ok_state ? fps_select(p, &bmap, sh, stages, stage_rows, u, c, p.M, next) : 0;
+    __syncthreads();
+    if (p.beacon_idx != nullptr)
+      for (int k = tid; k < p.M; k += kThreads)
+        p.beacon_idx[static_cast<size_t>(u) * p.M + k] = k < got ? sh->sel[k] : -1;
+    if (p.beacons != nullptr) {
+      const int row_vec = D / 8;
+      for (int e = tid; e < got * row_vec; e += kThreads) {
+        const int k = e / row_vec, v = e % row_vec;
+        reinterpret_cast<uint4*>(p.beacons + (static_cast<size_t>(u) * p.M + k) * D)[v] =
+            reinterpret_cast<const uint4*>(buf + static_cast<size_t>(sh->sel[k]) * D)[v];
+      }
+    }
+    if (p.n_beacons != nullptr && tid == 0) p.n_beacons[u] = got;
+    __syncthreads();  // sel is read before the next unit writes it
+    const bool stop = sh->abort_flag != 0;  // block-uniform
+    if (!stop && sh->preloaded == 0 && u + G < p.U) {
+      // nothing was loaded ahead: the barriers start again here
+      if (tid == 0) init_fps_barriers(sh, true);
+      __syncthreads();
+    }
+    if (stop) break;
+  }
+  // no load may still target this CTA's shared memory when it leaves
+  if (tid == kItems)
+    for (int k = 0; k < sh->preloaded; ++k) wait_bar(&sh->full[k], 0);
+  __syncthreads();
 }
 
 // ---- The per-step append on its own (a1), for steps that select no
@@ -735,9 +847,16 @@ size_t fps_smem_bytes(int C) {
   return need < 120 * 1024 ? 120 * 1024 : need;
 }
 
-cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, cudaStream_t st) {
+cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, int sms, cudaStream_t st) {
   const int rows = fps_stage_rows(p.C);
   const size_t smem = fps_smem_bytes(p.C);
+  if (p.q_new == nullptr && p.want_beacons) {
+    // beacon selection alone: the persistent kernel
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fps_beacons_kernel), smem);
+    if (e != cudaSuccess) return e;
+    fps_beacons_kernel<<<p.U < sms ? p.U : sms, kThreads, smem, st>>>(p, bufmap, rows);
+    return cudaGetLastError();
+  }
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fps_update_kernel), smem);
   if (e != cudaSuccess) return e;
   fps_update_kernel<<<p.U, kThreads, smem, st>>>(p, bufmap, rows);

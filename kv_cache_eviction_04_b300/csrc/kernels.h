@@ -83,7 +83,7 @@ struct FpsParams {
   int32_t first_m;        // 1: the first M items instead of FPS (compress keeps them)
 };
 
-cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, cudaStream_t st);
+cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, int sms, cudaStream_t st);
 // The append alone (one warp per unit), then the compress of the buffers it
 // filled (a persistent grid of at most `sms` CTAs); C <= 256, no beacons.
 cudaError_t launch_fps_append_compress(const FpsParams& p, const CUtensorMap& bufmap, int sms,

@@ -64,3 +64,64 @@ def test_fps_near_ties_bit_exact(name):
         ref = oracle.fps(X[u], cfg.M)
         assert np.array_equal(got[u], ref), (u, got[u][:8], ref[:8])
         assert np.array_equal(host_u16(beac[u]).reshape(cfg.M, D), X[u][ref])
+
+
+@pytest.mark.gpu
+def test_fps_persistent_beacons_many_units_bit_exact():
+    """Beacon selection alone runs as a persistent grid (at most one CTA per
+    SM, each taking units b, b + G, ...) that loads the next unit's first
+    Gram chunks during the current unit's greedy steps.  The seed recheck of
+    a near-tie unit uses the same shared memory as scratch, so near-tie
+    units are tiled over 400 units (two or three per CTA), mixed with
+    shorter buffers, buffers of exactly M items (no Gram) and empty ones.
+    Indices and beacon rows must equal the oracle's, bit for bit."""
+    if not gpu_available():
+        pytest.skip("needs a CUDA device")
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import oracle
+    from kv_cache_eviction_04_b300 import bkv
+    from tests.gpu_util import dev, host_u16
+
+    cfg, pool, seed = SHAPES["qwen3_4b"]
+    U = 400
+    n_full, D = cfg.C - 1, cfg.G * cfg.d
+    X, _ = near_tie_units(seed, pool, n_full, D, cfg.M)
+    rng = np.random.default_rng(400)
+    counts = np.full(U, n_full, np.int32)
+    special = rng.choice(U, size=60, replace=False)
+    counts[special[:20]] = rng.integers(cfg.M + 1, n_full, size=20)
+    counts[special[20:40]] = cfg.M
+    counts[special[40:50]] = 0
+    counts[special[50:]] = cfg.M + 1
+    buf = np.zeros((U, cfg.C, D), np.uint16)
+    for u in range(U):
+        buf[u, :counts[u]] = X[u % pool][:counts[u]]
+    dims = bkv.Dims.make(U, cfg.G, cfg.d, cfg.W, cfg.M, cfg.C, cfg.B_KV, cfg.Rw, cfg.L,
+                         cfg.theta)
+    ws = bkv.make_workspace(dims)
+    t_buf = dev(buf)
+    cnt = dev(counts)
+    bidx = torch.full((U, cfg.M), -7, dtype=torch.int32, device="cuda")
+    beac = torch.zeros((U, cfg.M, cfg.G, cfg.d), dtype=torch.int16, device="cuda")
+    nb = torch.zeros(U, dtype=torch.int32, device="cuda")
+    bkv.fps_update(dims, None, 0, None, t_buf, cnt, True, bidx, beac, nb, ws)
+    assert bkv.get_status(ws) == 0
+    got, gnb = bidx.cpu().numpy(), nb.cpu().numpy()
+    refs = {}
+    for u in range(U):
+        key = (u % pool, int(counts[u]))
+        if key not in refs:
+            refs[key] = oracle.fps(X[u % pool][:counts[u]], cfg.M) if counts[u] else \
+                np.zeros(0, np.int64)
+        ref = refs[key]
+        k = len(ref)
+        assert int(gnb[u]) == k, u
+        assert np.array_equal(got[u, :k], ref), (u, got[u][:8], ref[:8])
+        assert np.all(got[u, k:] == -1), u
+        assert np.array_equal(host_u16(beac[u]).reshape(cfg.M, D)[:k], X[u % pool][ref])
+    # the device buffers and counts are read-only here
+    assert np.array_equal(host_u16(t_buf), buf)
+    assert np.array_equal(cnt.cpu().numpy(), counts)
