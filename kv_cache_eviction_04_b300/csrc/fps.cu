@@ -123,15 +123,57 @@ __device__ __forceinline__ double exact_rnorm(const FpsShared* sh, int a) {
   return ff_value(ff_rsqrt(FF{sh->n2h[a], sh->n2l[a]}));
 }
 
+// The same, warp-collective, for a selection whose exact squared norms are
+// formed on demand (a negative n2h marks one not formed yet): the warp forms
+// it from the row in global memory and keeps it.  Two warps that form the
+// same norm at once write the same value.
+__device__ __forceinline__ double exact_rnorm_w(FpsShared* sh, const uint16_t* X, int D, int a) {
+  if (sh->n2h[a] < 0.f) {
+    const FF n2 = warp_dot_rows_ff(X, D, a, a);
+    if ((threadIdx.x & 31) == 0) {
+      sh->n2l[a] = n2.lo;
+      sh->n2h[a] = n2.hi;
+    }
+    return ff_value(ff_rsqrt(n2));
+  }
+  return exact_rnorm(sh, a);
+}
+
+// Exact squared norm of item i's row (one thread), as the Gram phase forms
+// it from the staged chunks: eight float pairs, one per 16-byte piece of a
+// 64-column chunk, merged in a fixed order.
+__device__ __forceinline__ FF row_norm_ff(const uint16_t* X, int D, int i) {
+  FF n2p[8];
+#pragma unroll
+  for (int lc = 0; lc < 8; ++lc) n2p[lc] = FF{0.f, 0.f};
+  const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<size_t>(i) * D);
+#pragma unroll 1
+  for (int c = 0; c < D / 64; ++c) {
+    uint4 v[8];
+#pragma unroll
+    for (int lc = 0; lc < 8; ++lc) v[lc] = row[c * 8 + lc];
+#pragma unroll
+    for (int lc = 0; lc < 8; ++lc) ff_add_products(n2p[lc], v[lc], v[lc]);
+  }
+  return ff_merge(ff_merge(ff_merge(n2p[0], n2p[1]), ff_merge(n2p[2], n2p[3])),
+                  ff_merge(ff_merge(n2p[4], n2p[5]), ff_merge(n2p[6], n2p[7])));
+}
+
 // Seed and greedy steps over the Gram in TMEM (the eight item warps only;
 // thread i owns item i and its TMEM lane).  Writes sh->sel[0, m).
 // `stages` is free scratch here (the seed recheck's partial sums).
+// With `lazy` the Gram phase formed 1/||x|| from an fp32 pairwise sum of
+// the exact squares (relative error <= ~6 u instead of ~1 u from the exact
+// norm): both bands widen by 1e-6, and the exact norms are formed only when
+// a recheck needs them.
+template <bool lazy>
 __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uint32_t tbase,
                          bool gram_ok, int u, int n, int m) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i = tid;
   const int D = p.D;
-  const float tauc = tau_cos(D), taum = tau_mean(D);
+  const float widen = lazy ? 1e-6f : 0.f;
+  const float tauc = tau_cos(D) + widen, taum = tau_mean(D) + widen;
   const uint16_t* X = p.buf + static_cast<size_t>(u) * p.C * D;
   const int N = (n + 15) & ~15;
   const int nbands = (n + 127) / 128;
@@ -194,6 +236,12 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
     // One warp per contender then forms x_a . T.  Two identical items get
     // bit-identical values, so the lowest slot wins an exact tie.
     const int nc = collect_contenders(i < n && mean <= t.v1 + 2.f * taum, sh);
+    if (lazy && i < n) {  // (a template parameter)
+      // the exact norms were not formed in the Gram phase: every item's now
+      const FF n2 = row_norm_ff(X, D, i);
+      sh->n2h[i] = n2.hi;
+      sh->n2l[i] = n2.lo;
+    }
     {
       const FF r = i < n ? ff_rsqrt(FF{sh->n2h[i], sh->n2l[i]}) : FF{0.f, 0.f};
       sh->rn64[i] = ff_value(r);
@@ -332,7 +380,8 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
       if (np <= kMaxPairs) {
         for (int pr = warp; pr < np; pr += kItemWarps) {
           const int a = sh->pair_a[pr], b = sh->pair_s[pr];
-          const double cv = (warp_dot_rows(X, D, a, b) * exact_rnorm(sh, a)) * exact_rnorm(sh, b);
+          const double cv =
+              (warp_dot_rows(X, D, a, b) * exact_rnorm_w(sh, X, D, a)) * exact_rnorm_w(sh, X, D, b);
           if (lane == 0) sh->pair64[pr] = 1.0 - cv;
         }
         item_sync();
@@ -347,11 +396,11 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
         // too many near-minimum pairs: every (contender, chosen) pair
         for (int c = warp; c < nc; c += kItemWarps) {
           const int a = sh->cont[c];
-          const double ra = exact_rnorm(sh, a);
+          const double ra = exact_rnorm_w(sh, X, D, a);
           double dmin = INFINITY;
           for (int s2 = 0; s2 < k; ++s2) {
             const int b = sh->sel[s2];
-            dmin = fmin(dmin, 1.0 - (warp_dot_rows(X, D, a, b) * ra) * exact_rnorm(sh, b));
+            dmin = fmin(dmin, 1.0 - (warp_dot_rows(X, D, a, b) * ra) * exact_rnorm_w(sh, X, D, b));
           }
           if (lane == 0) sh->cont_val[c] = dmin;
         }
@@ -389,6 +438,9 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
 // next_u >= 0 the producer warp loads that unit's first chunks during the
 // greedy steps (once the seed's scratch is free), initialising the
 // barriers again first, and leaves their count in sh->preloaded.
+// `lazy` (a template parameter, so that each kernel carries one copy of the
+// selection): see fps_pick.
+template <bool lazy>
 __device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
                           uint8_t* stages, int stage_rows, int u, int n, int m,
                           int next_u) {
@@ -430,8 +482,12 @@ __device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bm
   // all eight item warps are done with it; the producer refills without
   // waiting while it still has landed chunks to multiply.
   FF n2p[8];  // eight independent partial sums, one per 16-byte piece of a row
+  float f2[8];  // lazy: fp32 partial sums of the exact squares, the same pieces
 #pragma unroll
-  for (int lc = 0; lc < 8; ++lc) n2p[lc] = FF{0.f, 0.f};
+  for (int lc = 0; lc < 8; ++lc) {
+    n2p[lc] = FF{0.f, 0.f};
+    f2[lc] = 0.f;
+  }
   if (warp == kItemWarps) {
     if (lane == 0) {
       bool ok = true;
@@ -480,10 +536,27 @@ __device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bm
       if (!ok) break;
       if (i < n) {
         const uint8_t* row = stages + st * stage_bytes + i * 128;
+        if constexpr (lazy) {
+          // the eight squares of a piece (exact in fp32) summed pairwise,
+          // then added to the piece's running sum
 #pragma unroll
-        for (int lc = 0; lc < 8; ++lc) {
-          const uint4 v = *reinterpret_cast<const uint4*>(row + ((lc ^ (i & 7)) << 4));
-          ff_add_products(n2p[lc], v, v);
+          for (int lc = 0; lc < 8; ++lc) {
+            const uint4 v = *reinterpret_cast<const uint4*>(row + ((lc ^ (i & 7)) << 4));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            float sq[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a = __uint_as_float(w[e] << 16), b = __uint_as_float(w[e] & 0xFFFF0000u);
+              sq[e] = a * a + b * b;
+            }
+            f2[lc] += (sq[0] + sq[1]) + (sq[2] + sq[3]);
+          }
+        } else {
+#pragma unroll
+          for (int lc = 0; lc < 8; ++lc) {
+            const uint4 v = *reinterpret_cast<const uint4*>(row + ((lc ^ (i & 7)) << 4));
+            ff_add_products(n2p[lc], v, v);
+          }
         }
       }
       __syncwarp();
@@ -498,17 +571,26 @@ __device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bm
   tc_fence_after();
   if (tid < kItems) {
     const int i = tid;
-    const FF n2 = ff_merge(ff_merge(ff_merge(n2p[0], n2p[1]), ff_merge(n2p[2], n2p[3])),
-                           ff_merge(ff_merge(n2p[4], n2p[5]), ff_merge(n2p[6], n2p[7])));
-    const float nn = n2.hi + n2.lo;
-    sh->n2h[i] = i < n ? n2.hi : 0.f;
-    sh->n2l[i] = i < n ? n2.lo : 0.f;
+    float nn;
+    if constexpr (lazy) {
+      // squared norm from the fp32 sums (at most 14 roundings of positive
+      // terms for D = 512); the exact one is formed when a recheck needs it
+      nn = ((f2[0] + f2[1]) + (f2[2] + f2[3])) + ((f2[4] + f2[5]) + (f2[6] + f2[7]));
+      sh->n2h[i] = i < n ? -1.f : 0.f;
+      sh->n2l[i] = 0.f;
+    } else {
+      const FF n2 = ff_merge(ff_merge(ff_merge(n2p[0], n2p[1]), ff_merge(n2p[2], n2p[3])),
+                             ff_merge(ff_merge(n2p[4], n2p[5]), ff_merge(n2p[6], n2p[7])));
+      nn = n2.hi + n2.lo;
+      sh->n2h[i] = i < n ? n2.hi : 0.f;
+      sh->n2l[i] = i < n ? n2.lo : 0.f;
+    }
     sh->inv[i] = (i < n && nn > 0.f) ? 1.f / sqrtf(nn) : 0.f;
   }
   __syncthreads();
   const bool gram_ok = sh->abort_flag == 0;  // block-uniform
   if (warp < kItemWarps) {
-    fps_pick(p, sh, stages, tbase, gram_ok, u, n, m);
+    fps_pick<lazy>(p, sh, stages, tbase, gram_ok, u, n, m);
   } else if (next_u >= 0 && lane == 0 && gram_ok) {
     // the next unit's first chunks, while the item warps run the greedy
     // steps: every wait on the barriers of this unit has completed (the
@@ -576,7 +658,7 @@ __device__ void init_fps_barriers(FpsShared* sh, bool again) {
 __device__ int compress_unit(const FpsParams& p, const CUtensorMap* bmap, FpsShared* sh,
                              uint8_t* stages, int stage_rows, int u, uint16_t* buf) {
   const int tid = threadIdx.x, D = p.D;
-  const int got = fps_select(p, bmap, sh, stages, stage_rows, u, p.C, p.M, -1);
+  const int got = fps_select<false>(p, bmap, sh, stages, stage_rows, u, p.C, p.M, -1);
   if (tid == 0) {
     for (int k = 0; k < got; ++k) sh->surv[k] = sh->sel[k];
     for (int a = 1; a < got; ++a) {  // insertion sort, got <= 64
@@ -658,7 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- 3. beacons: FPS over the current buffer (read-only)
   if (p.want_beacons) {
-    const int got = ok_state ? fps_select(p, &bmap, sh, stages, stage_rows, u, c, p.M, -1) : 0;
+    const int got =
+        ok_state ? fps_select<false>(p, &bmap, sh, stages, stage_rows, u, c, p.M, -1) : 0;
     __syncthreads();
     if (p.beacon_idx != nullptr)
       for (int k = tid; k < p.M; k += kThreads)
@@ -686,6 +769,9 @@ __device__ __forceinline__ bool runs_gram(const FpsParams& p, int u) {
   return c >= 0 && c < p.C && c > p.M && p.M > 0 && !p.first_m;
 }
 
+// kLazy (several units per CTA): the exact norms only where a recheck
+// needs them (fps_pick).
+template <bool kLazy>
 __global__ void __launch_bounds__(kThreads, 1)
     fps_beacons_kernel(const __grid_constant__ FpsParams p,
                        const __grid_constant__ CUtensorMap bmap, int stage_rows) {
@@ -708,7 +794,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int un = u + G;
     const int next = (un < p.U && runs_gram(p, un)) ? un : -1;
-    const int got = ok_state ? fps_select(p, &bmap, sh, stages, stage_rows, u, c, p.M, next) : 0;
+    const int got =
+        ok_state ? fps_select<kLazy>(p, &bmap, sh, stages, stage_rows, u, c, p.M, next) : 0;
     __syncthreads();
     if (p.beacon_idx != nullptr)
       for (int k = tid; k < p.M; k += kThreads)
@@ -851,10 +938,13 @@ cudaError_t launch_fps(const FpsParams& p, const CUtensorMap& bufmap, int sms, c
   const int rows = fps_stage_rows(p.C);
   const size_t smem = fps_smem_bytes(p.C);
   if (p.q_new == nullptr && p.want_beacons) {
-    // beacon selection alone: the persistent kernel
-    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fps_beacons_kernel), smem);
+    // beacon selection alone: the persistent kernel, in its throughput
+    // form (exact norms on demand) when a CTA takes more than one unit
+    const bool lazy = p.U > sms;
+    auto* kernel = lazy ? fps_beacons_kernel<true> : fps_beacons_kernel<false>;
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), smem);
     if (e != cudaSuccess) return e;
-    fps_beacons_kernel<<<p.U < sms ? p.U : sms, kThreads, smem, st>>>(p, bufmap, rows);
+    kernel<<<lazy ? sms : p.U, kThreads, smem, st>>>(p, bufmap, rows);
     return cudaGetLastError();
   }
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fps_update_kernel), smem);
