@@ -87,10 +87,12 @@ ScoreShape score_shape(const bkv_dims* d) {
     s.nsplit = 1;
     return s;
   }
-  // One CTA per unit runs both passes when the rows fit one CTA and there
-  // are enough units to fill the GPU (or the caches are short); otherwise the
-  // keys of a unit are split over CTAs and the passes are two launches.
-  s.fused = s.NQ16 <= 256 && (2 * d->U >= sm_count() || s.ntiles <= 24);
+  // The persistent two-pass kernel (one CTA per SM, units in turn) when
+  // there are enough units to fill the GPU, or the rows fit one CTA's
+  // operand and the caches are short; more than 256 rows are then scored
+  // in groups of 256, one after another.  Otherwise the keys of a unit are
+  // split over CTAs and the passes are two launches.
+  s.fused = 2 * d->U >= sm_count() || (s.NQ16 <= 256 && s.ntiles <= 24);
   if (s.fused) {
     s.tiles_per_split = s.ntiles > 0 ? s.ntiles : 1;
     s.nsplit = 1;

@@ -814,6 +814,27 @@ __device__ __forceinline__ void publish_rows(const ScoreParams& p, const int32_t
 // the previous unit.
 constexpr int kBuildSplitNum = 3, kBuildSplitDen = 8;
 
+// Work item n of CTA b in the persistent two-pass kernel: row group n % ngrp
+// (kRows rows from row0) of unit b + (n / ngrp) * G.  More scoring rows than
+// one CTA's operand holds are scored in groups one after another, all groups
+// of a unit in the same CTA.
+struct SubUnit {
+  int u, grp, row0;
+  int nq16;  // rows of the group, rounded up to 16 (the pass-2 MMA's N)
+  int nblk;  // 128-row blocks of the group that hold rows (pass 1)
+};
+__device__ __forceinline__ SubUnit sub_unit(const ScoreParams& p, int n, int G, int kRows,
+                                            int ngrp) {
+  SubUnit w;
+  w.u = blockIdx.x + (n / ngrp) * G;
+  w.grp = n % ngrp;
+  w.row0 = w.grp * kRows;
+  const int nr = min(kRows, p.NQ16 - w.row0);
+  w.nq16 = nr;
+  w.nblk = (nr + 127) / 128;
+  return w;
+}
+
 // Epilogue of one unit (warps 4..11).  Iteration i of the unit (tile i in
 // pass 1, tile i - nt in pass 2) is the kernel's iteration g0 + i: it uses
 // accumulator (g0 + i) % kNBuf and is taken by half (g0 + i) % 2, so each
@@ -825,7 +846,7 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
                                                uint32_t tbase, FusedBars* bars, int32_t* row_pos,
                                                float* lse, float2* mz, int32_t* kp,
                                                const int32_t* tmax, int32_t minrow,
-                                               int32_t minpos) {
+                                               int32_t minpos, int nq16, int nblk, int grp) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                      // TMEM lane quarter
   const int h = (warp - 4) >> 2;               // half: 0 = warps 4..7, 1 = warps 8..11
@@ -865,12 +886,13 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
       for (int blk = 0; blk < NR; ++blk)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
+          if (blk >= nblk) continue;  // a row block of the group without rows
           uint32_t v[64];  // keys 64 c .. 64 c + 63 of the tile
           const uint32_t col = buf + blk * 128 + c * 64;
           tmem_ld32(col, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
           tmem_ld32(col + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           tmem_wait_ld();
-          if (blk == NR - 1 && c == 1) {
+          if (blk == nblk - 1 && c == 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) arrive_tempty(&bars->tempty[g % kNBuf]);
@@ -921,7 +943,7 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
   const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
   const int nrec = p.step + 1 < p.W ? static_cast<int>(p.step + 1) : p.W;
   const float inv_rows = 1.f / static_cast<float>(max((nrec + nb) * p.G, 1));
-  const int N = p.NQ16;
+  const int N = nq16;
   const int nchunks = (N + 31) / 32;
   constexpr bool is_max = kMax;
   const int key = q * 32 + lane;
@@ -1002,9 +1024,12 @@ __device__ __forceinline__ void fused_epilogue(const ScoreParams& p, int u, int 
       record_error(p.ws, BKV_ETIMEOUT, kSiteScoreWait);
     }
     if (j < L) {
+      // the groups of a unit run one after another in this CTA (with the
+      // epilogue's barriers between them): later groups fold into the score
       const float all = is_max ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : (s0 + s1) + (s2 + s3);
-      p.scores[static_cast<size_t>(u) * p.L_cap + j] =
-          is_max ? (all == -INFINITY ? 0.f : ex2(all)) : all * inv_rows;
+      const float sc = is_max ? (all == -INFINITY ? 0.f : ex2(all)) : all * inv_rows;
+      float* dst = p.scores + static_cast<size_t>(u) * p.L_cap + j;
+      *dst = grp == 0 ? sc : (is_max ? fmaxf(*dst, sc) : *dst + sc);
     }
   }
 }
@@ -1086,7 +1111,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
 
-  // the first unit's query operand: every warp but the TMA warp
+  // row groups per unit (more rows than one operand holds)
+  const int ngrp = (p.NQ16 + kRows - 1) / kRows;
+  // the first work item's query operand: every warp but the TMA warp
   if (warp >= 1) {
     build_queries<D>(p, blockIdx.x, 0, kRows, q_hi, q_lo, row_pos, cs, threadIdx.x - 32,
                      kPersistThreads - 32, 1);
@@ -1102,9 +1129,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     // ---------------- TMA producer.  (An L2 run-ahead of bulk prefetches
     // measured slower and, on long caches, re-read tiles from HBM.)
     if (lane == 0) prefetch_tmap(&kmap);
-    int g = 0, n = 0;
+    int g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.U && ok; u += G, ++n) {
+    for (int n = 0; ok; ++n) {
+      const SubUnit w = sub_unit(p, n, G, kRows, ngrp);
+      const int u = w.u;
+      if (u >= p.U) break;
       int t0, t1, L;
       split_tiles(p, u, 0, t0, t1, L);  // tiles_per_split covers the whole cache here
       const int nt = t1 - t0;
@@ -1180,10 +1210,13 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer
-    const uint32_t idesc2 = idesc_bf16_f32(128, static_cast<uint32_t>(p.NQ16));
-    int g = 0, n = 0, commits = 0;
+    int g = 0, commits = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < (p.stall ? 0 : p.U) && ok; u += G, ++n) {
+    for (int n = 0; !p.stall && ok; ++n) {
+      const SubUnit w = sub_unit(p, n, G, kRows, ngrp);
+      const int u = w.u;
+      if (u >= p.U) break;
+      const uint32_t idesc2 = idesc_bf16_f32(128, static_cast<uint32_t>(w.nq16));
       int t0, t1, L;
       split_tiles(p, u, 0, t0, t1, L);
       const int nt = t1 - t0;
@@ -1199,11 +1232,13 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
           const uint32_t dt = tbase + b * kBufCols;
           const uint32_t kbase = smem_u32(stages + st * kStageBytes);
           if (i < nt) {
-            // pass 1: D[row][key] = Q[row] . K[key], one M = 128 block per row block
+            // pass 1: D[row][key] = Q[row] . K[key], one M = 128 block per row
+            // block that holds rows
 #pragma unroll
             for (int blk = 0; blk < NR; ++blk)
 #pragma unroll
               for (int part2 = 0; part2 < 2; ++part2) {
+                if (blk >= w.nblk) continue;
                 const uint32_t qbase = smem_u32(part2 ? q_lo : q_hi) + blk * 128 * 128;
 #pragma unroll
                 for (int a = 0; a < D / 64; ++a)
@@ -1268,14 +1303,18 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(b0 + o));
       }
     };
-    int n = 1;
-    int u = blockIdx.x + G;
     int32_t cur = 0;
-    if (u < p.U) {
-      pull_rows(u);
-      cur = p.cur_pos[u];
+    {
+      const SubUnit w1 = sub_unit(p, 1, G, kRows, ngrp);
+      if (w1.u < p.U) {
+        if (w1.grp == 0) pull_rows(w1.u);
+        cur = p.cur_pos[w1.u];
+      }
     }
-    for (; u < p.U; u += G, ++n) {
+    for (int n = 1;; ++n) {
+      const SubUnit w = sub_unit(p, n, G, kRows, ngrp);
+      const int u = w.u;
+      if (u >= p.U) break;
       bool ok = n < 2 || warp_wait(&bars->edone[n & 1], ((n - 2) >> 1) & 1, &bars->abort_flag,
                                    p.wait_ns);
       // both builder warps leave together (they meet at named barriers)
@@ -1283,9 +1322,9 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       int32_t* rp = row_pos + (n & 1) * kRows;
       build_cs_table<D>(p, cur, cs, bt, 64);
       uint4 va[kB], vb[kB];
-      load_query_batch<D, kB>(p, u, 0, kTotal, bt, 64, va, vb);
+      load_query_batch<D, kB>(p, u, w.row0, kTotal, bt, 64, va, vb);
       const int nb = p.M > 0 ? min(max(p.n_beacons[u], 0), p.M) : 0;
-      for (int r = bt; r < kRows; r += 64) rp[r] = row_position(p, u, r, nb, cur);
+      for (int r = bt; r < kRows; r += 64) rp[r] = row_position(p, u, w.row0 + r, nb, cur);
       named_sync(5, 64);
       if (warp == 2) {
         if (lane == 0) bars->cur[n & 1] = cur;
@@ -1295,22 +1334,26 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       if (named_sync_or(5, 64, !ok)) break;
 #pragma unroll 1
       for (int k = 0; k < kPer; k += kB) {
-        if (k > 0) load_query_batch<D, kB>(p, u, 0, kTotal, bt + k * 64, 64, va, vb);
+        if (k > 0) load_query_batch<D, kB>(p, u, w.row0, kTotal, bt + k * 64, 64, va, vb);
         store_query_batch<D, kB>(p, kRows, kTotal, bt + k * 64, 64, va, vb, rp, cs, cur, q_hi,
                                  q_lo);
       }
       fence_proxy_async_shared();  // generic smem writes -> visible to the tensor core
       named_sync(5, 64);
       if (bt == 0) mbar_arrive(&bars->qfull[n & 1]);
-      if (u + G < p.U) {
-        pull_rows(u + G);
-        cur = p.cur_pos[u + G];
+      const SubUnit wn = sub_unit(p, n + 1, G, kRows, ngrp);
+      if (wn.u < p.U) {
+        if (wn.grp == 0) pull_rows(wn.u);
+        cur = p.cur_pos[wn.u];
       }
     }
   } else {
     // ---------------- epilogue (warps 4..11)
-    int g0 = 0, n = 0;
-    for (int u = blockIdx.x; u < p.U; u += G, ++n) {
+    int g0 = 0;
+    for (int n = 0;; ++n) {
+      const SubUnit w = sub_unit(p, n, G, kRows, ngrp);
+      const int u = w.u;
+      if (u >= p.U) break;
       int t0, t1, L;
       split_tiles(p, u, 0, t0, t1, L);
       const int nt = t1 - t0;
@@ -1322,19 +1365,24 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       const int32_t* tm = tmax + (n & 1) * kTmaxTiles;
       const int32_t minrow = bars->minrow[n & 1], minpos = bars->minpos[n & 1];
       fused_epilogue<D, NR, kBufCols, kNBuf, kMax>(p, u, nt, L, g0, tbase, bars, rp, lse, mz, kp,
-                                                   tm, minrow, minpos);
+                                                   tm, minrow, minpos, w.nq16, w.nblk, w.grp);
       g0 += 2 * nt;
-      // the epilogue's share of the next unit's query build (items
+      // the epilogue's share of the next work item's query build (items
       // [kX, total)); the builders have placed the table and row positions
-      if (u + G < p.U) {
+      const SubUnit wn = sub_unit(p, n + 1, G, kRows, ngrp);
+      if (wn.u < p.U) {
         constexpr int kTotal = kRows * (D / 16);
         constexpr int kX = kTotal * kBuildSplitNum / kBuildSplitDen;
         constexpr int kEB = (kTotal - kX + kFusedEpi - 1) / kFusedEpi;
         const int nn = n + 1, et = threadIdx.x - 128;
-        if (warp_wait(&bars->bready[nn & 1], (nn >> 1) & 1, &bars->abort_flag, p.wait_ns)) {
+        // The MMAs of this work item must be done with the image: each half
+        // waited only for its own tiles, and the other half's last tile may
+        // still be in the tensor core.  qempty completes once per work item.
+        if (warp_wait(&bars->qempty, n & 1, &bars->abort_flag, p.wait_ns) &&
+            warp_wait(&bars->bready[nn & 1], (nn >> 1) & 1, &bars->abort_flag, p.wait_ns)) {
           const int32_t cur = bars->cur[nn & 1];
           uint4 va[kEB], vb[kEB];
-          load_query_batch<D, kEB>(p, u + G, 0, kTotal, kX + et, kFusedEpi, va, vb);
+          load_query_batch<D, kEB>(p, wn.u, wn.row0, kTotal, kX + et, kFusedEpi, va, vb);
           store_query_batch<D, kEB>(p, kRows, kTotal, kX + et, kFusedEpi, va, vb,
                                     row_pos + (nn & 1) * kRows, cs, cur, q_hi, q_lo);
           fence_proxy_async_shared();  // generic smem writes -> visible to the tensor core

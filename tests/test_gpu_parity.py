@@ -598,17 +598,22 @@ def test_score_parity_single_pass_cluster_shapes(L_cap, Ls, causal):
         assert np.all(sg[u, n:] == -1.0), "wrote past L"
 
 
-@pytest.mark.parametrize("shape,U,L_cap", [("c1", 600, None), ("c3", 400, None),
-                                             ("c4m16", 300, 640)])
-def test_score_parity_persistent_fused(shape, U, L_cap):
+@pytest.mark.parametrize("shape,U,L_cap,agg", [("c1", 600, None, "max"), ("c3", 400, None, "max"),
+                                                 ("c4m16", 300, 640, "max"),
+                                                 ("c4m64", 300, 640, "max"),
+                                                 ("c4m32", 200, 384, "mean")])
+def test_score_parity_persistent_fused(shape, U, L_cap, agg):
     """The two-pass kernel is persistent: CTA b scores units b, b + G, ...
     (G CTAs, at most one per SM), overlapping one unit's tail with the next
     unit's key loads and query build.  Up to five units per CTA (64-, 128-
     and 256-row operands, head dims 64 and 128), ragged lengths including
     empty units, one key and full caches, against the oracle on every unit,
-    and the same bits on a second call.  Units are a tiled pool of distinct
-    seeded units."""
-    cfg = {"c1": wl.CONFIGS[1], "c3": wl.CONFIGS[3], "c4m16": wl.config4(16)}[shape]
+    and the same bits on a second call.  More than 256 rows (the R1-Distill
+    sweep at M = 32 and 64: 336 and 560 rows) are scored in row groups of
+    256, one after another in the same CTA, folded into the score by max
+    or sum.  Units are a tiled pool of distinct seeded units."""
+    cfg = {"c1": wl.CONFIGS[1], "c3": wl.CONFIGS[3], "c4m16": wl.config4(16),
+           "c4m64": wl.config4(64), "c4m32": wl.config4(32)}[shape]
     pool = 24
     base = wl.make_units(cfg, range(pool))
     if L_cap is not None:
@@ -622,7 +627,7 @@ def test_score_parity_persistent_fused(shape, U, L_cap):
     Ls = rng.integers(1, n + 1, size=U)
     Ls[:6] = [n, 0, 1, 128, 129, n - 1]
     units["L"] = Ls.astype(np.int32)
-    st = DeviceState(units, cfg)
+    st = DeviceState(units, cfg, agg=bkv.AGG_MAX if agg == "max" else bkv.AGG_MEAN)
     beacons = {}
     for u in range(pool):
         un = _unit(base, u)
@@ -635,7 +640,7 @@ def test_score_parity_persistent_fused(shape, U, L_cap):
             st.beac[u, : len(vec)] = dev(vec.reshape(len(vec), cfg.G, cfg.d))
     st.score()
     assert st.status() == 0
-    _score_check(cfg, units, st)
+    _score_check(cfg, units, st, agg)
     sg = st.scores.cpu().numpy()
     for u, n_ in enumerate(Ls):
         assert np.all(sg[u, n_:] == -1.0), "wrote past L"
