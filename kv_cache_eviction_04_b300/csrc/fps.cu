@@ -82,21 +82,23 @@ __device__ __forceinline__ void item_sync() { asm volatile("bar.sync 1, %0;" ::"
 // Top2 over the items (thread t < 256 = item t, every item thread calls)
 // under the order "smaller value first, then smaller item"; the result is
 // valid in every item thread.  Warps reduce order-preserving keys with
-// redux.sync; one barrier, then every thread merges the eight warp
-// results.  Consecutive calls alternate between two buffers (`par` = call
-// count & 1), so a call never overwrites what a thread of the previous call
-// may still read.
+// redux.sync; one barrier; then lane q of every warp takes warp q's entry
+// and three more reductions merge the eight: the smallest key, the lowest
+// item holding it, and the runner-up (the winner's own second, or another
+// warp's best).  Consecutive calls alternate between two buffers (`par` =
+// call count & 1), so a call never overwrites what a thread of the previous
+// call may still read.
 __device__ Top2 block_top2(float v, FpsShared* sh, int par) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const KeyTop2 w = warp_key_top2(fkey(v), warp * 32);
   if (lane == 0) sh->red[par][warp] = make_uint4(w.k1, static_cast<uint32_t>(w.i1), w.k2, 0u);
   item_sync();
-  uint64_t best = ~0ull;
-  uint32_t second = 0xffffffffu;
-#pragma unroll
-  for (int q = 0; q < kItemWarps; ++q) key_top2_merge(best, second, sh->red[par][q]);
-  return Top2{fkey_value(static_cast<uint32_t>(best >> 32)),
-              static_cast<int>(best & 0xffffffffu), fkey_value(second)};
+  const uint4 e = lane < kItemWarps ? sh->red[par][lane]
+                                    : make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0u);
+  const uint32_t k1 = __reduce_min_sync(0xffffffffu, e.x);
+  const uint32_t i1 = __reduce_min_sync(0xffffffffu, e.x == k1 ? e.y : 0xffffffffu);
+  const uint32_t k2 = __reduce_min_sync(0xffffffffu, (e.x == k1 && e.y == i1) ? e.z : e.x);
+  return Top2{fkey_value(k1), static_cast<int>(i1), fkey_value(k2)};
 }
 
 // Ordered list of the items whose flag is set (item threads): writes them

@@ -73,18 +73,6 @@ __device__ __forceinline__ KeyTop2 warp_key_top2(uint32_t key, int base) {
   const uint32_t k2 = __reduce_min_sync(0xffffffffu, lane == l1 ? 0xffffffffu : key);
   return KeyTop2{k1, base + l1, k2};
 }
-// Merge of per-warp KeyTop2 entries {k1, i1, k2, -} in any order: the
-// result is the top-2 of the union.
-__device__ __forceinline__ void key_top2_merge(uint64_t& best, uint32_t& second, uint4 e) {
-  const uint64_t c = (static_cast<uint64_t>(e.x) << 32) | e.y;
-  if (c < best) {
-    second = min(static_cast<uint32_t>(best >> 32), e.z);
-    best = c;
-  } else {
-    second = min(second, e.x);
-  }
-}
-
 // Warp-wide Top2 by xor shuffles (every lane gets the result).
 __device__ __forceinline__ Top2 warp_top2(Top2 t) {
 #pragma unroll
