@@ -93,12 +93,10 @@ __device__ Top2 block_top2(float v, FpsShared* sh, int par) {
   const KeyTop2 w = warp_key_top2(fkey(v), warp * 32);
   if (lane == 0) sh->red[par][warp] = make_uint4(w.k1, static_cast<uint32_t>(w.i1), w.k2, 0u);
   item_sync();
-  const uint4 e = lane < kItemWarps ? sh->red[par][lane]
-                                    : make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0u);
-  const uint32_t k1 = __reduce_min_sync(0xffffffffu, e.x);
-  const uint32_t i1 = __reduce_min_sync(0xffffffffu, e.x == k1 ? e.y : 0xffffffffu);
-  const uint32_t k2 = __reduce_min_sync(0xffffffffu, (e.x == k1 && e.y == i1) ? e.z : e.x);
-  return Top2{fkey_value(k1), static_cast<int>(i1), fkey_value(k2)};
+  const uint4 r = merge_key_top2(lane < kItemWarps ? sh->red[par][lane]
+                                                  : make_uint4(0xffffffffu, 0xffffffffu,
+                                                               0xffffffffu, 0u));
+  return Top2{fkey_value(r.x), static_cast<int>(r.y), fkey_value(r.z)};
 }
 
 // Ordered list of the items whose flag is set (item threads): writes them

@@ -56,48 +56,34 @@ struct __align__(16) ClShared {
   double cont_val[128];
   double pair64[kMaxPairsC];
   int16_t pair_a[kMaxPairsC], pair_s[kMaxPairsC];
-  float red_v1[2][kCW], red_v2[2][kCW];
-  int32_t red_i1[2][kCW];
+  uint4 red4[2][kCW];  // per-warp {key, item, runner-up key, -} of a CTA top-2
   // posts read by the other CTAs of the cluster, double-buffered by the
   // parity of the exchange count
-  float mb_v1[2], mb_v2[2];
-  int32_t mb_i1[2];
+  uint4 mbk[2];  // this CTA's {key, item, runner-up key, -}
   double mb_cv[2];
   int32_t mb_ci[2];
 };
 
-// Top-2 of the CTA (one barrier; alternating buffers, as in fps.cu).
-__device__ Top2 cta_top2(Top2 t, ClShared* sh, int par) {
+// Top-2 of the CTA as keys (one barrier; alternating buffers, as in
+// fps.cu).  v is this thread's value; its item is i = base + threadIdx.x.
+__device__ uint4 cta_top2(float v, int i, ClShared* sh, int par) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  t = warp_top2(t);
-  if (lane == 0) {
-    sh->red_v1[par][warp] = t.v1;
-    sh->red_i1[par][warp] = t.i1;
-    sh->red_v2[par][warp] = t.v2;
-  }
+  const KeyTop2 w = warp_key_top2(fkey(v), i - lane);
+  if (lane == 0) sh->red4[par][warp] = make_uint4(w.k1, static_cast<uint32_t>(w.i1), w.k2, 0u);
   __syncthreads();
-  Top2 r{sh->red_v1[par][0], sh->red_i1[par][0], sh->red_v2[par][0]};
-  for (int w = 1; w < kCW; ++w)
-    r = top2_merge(r, Top2{sh->red_v1[par][w], sh->red_i1[par][w], sh->red_v2[par][w]});
-  return r;
+  return merge_key_top2(lane < kCW ? sh->red4[par][lane]
+                                   : make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0u));
 }
 
-// Cluster-wide top-2: post the CTA's, meet, merge every CTA's in rank order.
-__device__ Top2 cluster_top2(Top2 local, ClShared* sh, int par, int R) {
-  if (threadIdx.x == 0) {
-    sh->mb_v1[par] = local.v1;
-    sh->mb_i1[par] = local.i1;
-    sh->mb_v2[par] = local.v2;
-  }
+// Cluster-wide top-2: post the CTA's, meet, and lane q of every warp reads
+// CTA q's post; the merge does not depend on the order.
+__device__ Top2 cluster_top2(uint4 local, ClShared* sh, int par, int R) {
+  if (threadIdx.x == 0) sh->mbk[par] = local;
   cluster_sync();
-  Top2 r{INFINITY, 0x7fffffff, INFINITY};
-  for (int q = 0; q < R; ++q) {
-    const Top2 o{ld_cluster_f32(cluster_map(&sh->mb_v1[par], q)),
-                 ld_cluster_s32(cluster_map(&sh->mb_i1[par], q)),
-                 ld_cluster_f32(cluster_map(&sh->mb_v2[par], q))};
-    r = q == 0 ? o : top2_merge(r, o);
-  }
-  return r;
+  const int lane = threadIdx.x & 31;
+  const uint4 r = merge_key_top2(lane < R ? ld_cluster_u32x4(cluster_map(&sh->mbk[par], lane))
+                                          : make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0u));
+  return Top2{fkey_value(r.x), static_cast<int>(r.y), fkey_value(r.z)};
 }
 
 // Cluster-wide best contender: the largest value (or smallest, `maximize`
@@ -271,7 +257,7 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
     }
     if (live_item) mean = (acc.hi + acc.lo) * inv_i / static_cast<float>(n - 1);
   }
-  Top2 t = cluster_top2(cta_top2(Top2{mean, i, INFINITY}, sh, tb++ & 1), sh, xc++ & 1, R);
+  Top2 t = cluster_top2(cta_top2(mean, i, sh, tb++ & 1), sh, xc++ & 1, R);
   int seed = t.i1;
   if (!(t.v2 - t.v1 > 2.f * taum)) {
     // near-tie: as in fps.cu, sum_j cos(a, j) = r_a (x_a . T), T = sum_j r_j x_j
@@ -358,8 +344,7 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
   for (int k = 1; k < m; ++k) {
     const bool live = live_item && !chosen;
     const Top2 r =
-        cluster_top2(cta_top2(Top2{live ? -dist : INFINITY, i, INFINITY}, sh, tb++ & 1), sh,
-                     xc++ & 1, R);
+        cluster_top2(cta_top2(live ? -dist : INFINITY, i, sh, tb++ & 1), sh, xc++ & 1, R);
     int win = r.i1;
     if (!(r.v2 - r.v1 > 2.f * tauc)) {
       const bool cont = live && -dist <= r.v1 + 2.f * tauc;

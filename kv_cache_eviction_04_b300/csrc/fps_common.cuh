@@ -33,20 +33,6 @@ struct Top2 {
   int i1;
   float v2;
 };
-__device__ __forceinline__ Top2 top2_merge(Top2 a, Top2 b) {
-  const bool a_first = a.v1 < b.v1 || (a.v1 == b.v1 && a.i1 < b.i1);
-  Top2 r;
-  if (a_first) {
-    r.v1 = a.v1;
-    r.i1 = a.i1;
-    r.v2 = fminf(a.v2, b.v1);
-  } else {
-    r.v1 = b.v1;
-    r.i1 = b.i1;
-    r.v2 = fminf(b.v2, a.v1);
-  }
-  return r;
-}
 // Order-preserving integer key of a float (smaller value -> smaller key,
 // -0 counts as +0) and its inverse: the top-2 reductions compare keys with
 // redux.sync.
@@ -73,17 +59,16 @@ __device__ __forceinline__ KeyTop2 warp_key_top2(uint32_t key, int base) {
   const uint32_t k2 = __reduce_min_sync(0xffffffffu, lane == l1 ? 0xffffffffu : key);
   return KeyTop2{k1, base + l1, k2};
 }
-// Warp-wide Top2 by xor shuffles (every lane gets the result).
-__device__ __forceinline__ Top2 warp_top2(Top2 t) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    Top2 o2;
-    o2.v1 = __shfl_xor_sync(0xffffffffu, t.v1, o);
-    o2.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
-    o2.v2 = __shfl_xor_sync(0xffffffffu, t.v2, o);
-    t = top2_merge(t, o2);
-  }
-  return t;
+// Merge of up to 32 {key, item, runner-up key, -} entries, one per lane
+// (lanes without one hold all-ones keys), under the order "smaller key
+// first, then smaller item": the smallest key, the lowest item holding it,
+// and the runner-up (the winner's own second, or another entry's best).
+// Every lane gets the result.
+__device__ __forceinline__ uint4 merge_key_top2(uint4 e) {
+  const uint32_t k1 = __reduce_min_sync(0xffffffffu, e.x);
+  const uint32_t i1 = __reduce_min_sync(0xffffffffu, e.x == k1 ? e.y : 0xffffffffu);
+  const uint32_t k2 = __reduce_min_sync(0xffffffffu, (e.x == k1 && e.y == i1) ? e.z : e.x);
+  return make_uint4(k1, i1, k2, 0u);
 }
 
 // ---- exact-product dot products for the near-tie rechecks.
