@@ -507,11 +507,15 @@ def run_ours(args, rank, world):
     }
     kfile = {"fps_update": "fps_cluster.cu" if cfg.C > 256 else "fps.cu", "score": "score.cu",
              "select_compact": "select_compact.cu"}
-    # the library runs scoring as one launch per unit when its rows fit one
-    # CTA and the units fill the GPU (or the cache is short), else as two
     nq16 = ((cfg.W + M) * cfg.G + 15) // 16 * 16
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    fused = nq16 <= 256 and (2 * U >= sms or (cfg.L + 127) // 128 <= 24)
+    # the library's choice of scoring path: one launch on a cluster (a round
+    # whose clusters fit one wave) or in the persistent two-pass kernel,
+    # else the two launches of the split path
+    ntiles = (cfg.L + 127) // 128
+    ncl = (ntiles + 3) // 4
+    cluster = nq16 <= 128 and ncl <= 8 and U * ncl <= sms
+    fused = cluster or 2 * U >= sms or (nq16 <= 256 and ntiles <= 24)
     launches = {"fps_update": 1, "score": 1 if fused else 2, "select_compact": 1}
     # scoring FLOPs: 2 N_q L d per unit (N_q = (W + M) G rows; the hi/lo
     # split, the second pass and row padding are executed work, not counted)
