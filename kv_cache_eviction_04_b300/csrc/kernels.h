@@ -31,7 +31,7 @@ struct ScoreParams {
   int32_t nsplit;           // key-range splits per unit
   int32_t tiles_per_split;  // 128-key tiles per split
   int32_t agg, causal;
-  int32_t fused;            // 1: one CTA per unit runs both passes (NQ16 <= 256)
+  int32_t fused;            // 1: the persistent two-pass kernel (row groups of 256)
   int32_t cluster;          // > 0: one pass on a cluster of this many CTAs per unit
                             // (max aggregation, NQ16 <= 128, at most 4 key tiles per CTA)
   int32_t early_reads;      // 1: the previous kernel of the stream is the beacon selection,

@@ -7,14 +7,22 @@
 // maximum over queries (max beats mean); inkeast.github.io reading, section
 // 三, scoring with the union of recent and beacon queries.
 //
-// Two launches per call, both tcgen05 kernels fed by TMA:
-//   score_stats  (pass 1): rows on the 128 TMEM lanes, keys on the columns:
-//                D = Q * K^T; each thread owns one row and keeps a running
-//                max and sum of exp2 over its keys -> per-split (m, z).
-//   score_final  (pass 2): keys on the TMEM lanes, rows on the columns:
-//                D = K * Q^T; each thread owns one key, merges the splits'
-//                (m, z) into each row's log-sum-exp and takes the max (or
-//                mean) of the normalised probability over rows in registers.
+// Three paths, all tcgen05 kernels fed by TMA:
+//   score_fused_kernel    both passes in one persistent kernel (one CTA per
+//                         SM takes units in turn; more than 256 rows in
+//                         groups of 256);
+//   score_stats + final   the keys of a unit split over CTAs: pass 1 writes
+//                         per-split (m, z), pass 2 merges them (few units
+//                         with long caches);
+//   score_cluster_kernel  one pass on a cluster, the logits kept in TMEM
+//                         (small rounds, at most 128 rows).
+// The two-pass kernels put, in
+//   pass 1  rows on the 128 TMEM lanes, keys on the columns: D = Q * K^T;
+//           each thread owns one row and keeps a running max and sum of
+//           exp2 over its keys;
+//   pass 2  keys on the TMEM lanes, rows on the columns: D = K * Q^T; each
+//           thread owns one key and takes the max (or mean) of the
+//           normalised probability over rows in registers.
 // Queries are rotated in fp32 (angles reduced in extended precision) and
 // carried as q = q_hi + q_lo, two bf16 terms; both terms run through the
 // tensor core into one fp32 accumulator, so the logits carry ~2^-17
@@ -700,21 +708,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // --------------------------------------------------------------- fused
-// Both passes in one CTA per unit, for up to 256 scoring rows: the queries
-// are rotated once, pass 1 runs over every key tile of the unit, each row's
-// log2-sum-exp is formed locally (no partials, no second launch), and pass 2
-// streams the same tiles again through TMA (a unit's keys are then usually
-// still in L2).  NR = 128-row blocks of the query image (1 or 2).
-//
-// Ten warps: warp 0 issues TMA, warp 1 issues MMAs, warps 2..9 are the
-// epilogue.  The two TMEM accumulators alternate between tiles, and each
-// half of the epilogue (warps 2..5 and 6..9, one warp per TMEM lane quarter
-// and per SM sub-partition) owns one of them: half h takes the tiles
-// i with i % 2 == h, whole.  Two tiles are in the epilogue at once and no
-// tile needs a barrier across the halves.  In pass 1 a thread keeps the
-// running max and sum of exp2 of its row over its half's tiles (the halves
-// are merged once at the end); in pass 2 a thread reduces its key over all
-// rows and writes its score.
+// Both passes in one CTA for a unit's rows (or a group of 256 of them): the
+// queries are rotated once, pass 1 runs over every key tile of the unit,
+// each row's log2-sum-exp is formed locally (no partials, no second
+// launch), and pass 2 streams the same tiles again through TMA (a unit's
+// keys are then usually still in L2).  NR = 128-row blocks of the query
+// image (1 or 2).  score_fused_kernel (below) runs it persistently; its
+// epilogue is fused_epilogue.  The cluster kernel uses the thread count
+// and epilogue width here.
 constexpr int kFusedThreads = 320;
 constexpr int kFusedEpi = 256;
 
