@@ -254,34 +254,54 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
     FF* T = Tp + static_cast<size_t>(ngrp) * D;       // [D]
     if (tid < ngrp * noct) {
       const int g = tid / noct, o = tid - g * noct;
-      FF acc[8];
+      FF2 acc2[4];  // octet values 2h, 2h + 1 in halves 0, 1 of acc2[h]
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = FF{0.f, 0.f};
+      for (int e = 0; e < 4; ++e) acc2[e] = FF2{0ull, 0ull};
       const uint4* col = reinterpret_cast<const uint4*>(X) + o;
-      // eight items' loads in flight before any is used; items past n are
-      // zero and add exactly nothing
-#pragma unroll 1
-      for (int j0 = g; j0 < n; j0 += 8 * ngrp) {
-        uint4 v[8];
-        float2 r[8];
+      // eight items' loads in flight before any is used, and the next
+      // eight's issued before this eight's products are summed (the pass
+      // waits on L2 otherwise); items past n are zero and add exactly nothing
+      auto load8 = [&](int j0, uint4 (&v)[8]) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const int j = j0 + q * ngrp;
           v[q] = j < n ? col[static_cast<size_t>(j) * noct] : make_uint4(0u, 0u, 0u, 0u);
+        }
+      };
+      uint4 v[8];
+      load8(g, v);
+#pragma unroll 1
+      for (int j0 = g; j0 < n; j0 += 8 * ngrp) {
+        uint4 vn[8];
+        load8(j0 + 8 * ngrp, vn);
+        float2 r[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int j = j0 + q * ngrp;
           r[q] = j < n ? sh->rr[j] : make_float2(0.f, 0.f);
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const uint32_t wv[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+          const uint64_t rh2 = f2_pack(r[q].x, r[q].x), rl2 = f2_pack(r[q].y, r[q].y);
 #pragma unroll
-          for (int hh = 0; hh < 4; ++hh) {
-            ff_add_scaled(acc[2 * hh], __uint_as_float(wv[hh] << 16), r[q].x, r[q].y);
-            ff_add_scaled(acc[2 * hh + 1], __uint_as_float(wv[hh] & 0xFFFF0000u), r[q].x, r[q].y);
-          }
+          for (int hh = 0; hh < 4; ++hh)
+            ff2_add_scaled(acc2[hh],
+                           f2_pack(__uint_as_float(wv[hh] << 16),
+                                   __uint_as_float(wv[hh] & 0xFFFF0000u)),
+                           rh2, rl2);
         }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = vn[q];
       }
 #pragma unroll
-      for (int e = 0; e < 8; ++e) Tp[static_cast<size_t>(g) * D + 8 * o + e] = acc[e];
+      for (int e = 0; e < 4; ++e) {
+        FF a, b;
+        f2_unpack(acc2[e].hi, a.hi, b.hi);
+        f2_unpack(acc2[e].lo, a.lo, b.lo);
+        Tp[static_cast<size_t>(g) * D + 8 * o + 2 * e] = a;
+        Tp[static_cast<size_t>(g) * D + 8 * o + 2 * e + 1] = b;
+      }
     }
     item_sync();
     for (int k = tid; k < D; k += kItems) {
@@ -481,13 +501,14 @@ __device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bm
   // staged chunks.  A stage is refilled once its MMAs have completed and
   // all eight item warps are done with it; the producer refills without
   // waiting while it still has landed chunks to multiply.
-  FF n2p[8];  // eight independent partial sums, one per 16-byte piece of a row
+  // eight independent partial sums, one per 16-byte piece of a row: pieces
+  // 2h and 2h + 1 in halves 0 and 1 of n2p2[h]
+  FF2 n2p2[4];
   float f2[8];  // lazy: fp32 partial sums of the exact squares, the same pieces
 #pragma unroll
-  for (int lc = 0; lc < 8; ++lc) {
-    n2p[lc] = FF{0.f, 0.f};
-    f2[lc] = 0.f;
-  }
+  for (int lc = 0; lc < 8; ++lc) f2[lc] = 0.f;
+#pragma unroll
+  for (int h = 0; h < 4; ++h) n2p2[h] = FF2{0ull, 0ull};
   if (warp == kItemWarps) {
     if (lane == 0) {
       bool ok = true;
@@ -553,9 +574,10 @@ __device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bm
           }
         } else {
 #pragma unroll
-          for (int lc = 0; lc < 8; ++lc) {
-            const uint4 v = *reinterpret_cast<const uint4*>(row + ((lc ^ (i & 7)) << 4));
-            ff_add_products(n2p[lc], v, v);
+          for (int h = 0; h < 4; ++h) {
+            const uint4 v0 = *reinterpret_cast<const uint4*>(row + (((2 * h) ^ (i & 7)) << 4));
+            const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((2 * h + 1) ^ (i & 7)) << 4));
+            ff2_add_squares(n2p2[h], v0, v1);
           }
         }
       }
@@ -579,6 +601,12 @@ __device__ __noinline__ int fps_select(const FpsParams& p, const CUtensorMap* bm
       sh->n2h[i] = i < n ? -1.f : 0.f;
       sh->n2l[i] = 0.f;
     } else {
+      FF n2p[8];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        f2_unpack(n2p2[h].hi, n2p[2 * h].hi, n2p[2 * h + 1].hi);
+        f2_unpack(n2p2[h].lo, n2p[2 * h].lo, n2p[2 * h + 1].lo);
+      }
       const FF n2 = ff_merge(ff_merge(ff_merge(n2p[0], n2p[1]), ff_merge(n2p[2], n2p[3])),
                              ff_merge(ff_merge(n2p[4], n2p[5]), ff_merge(n2p[6], n2p[7])));
       nn = n2.hi + n2.lo;

