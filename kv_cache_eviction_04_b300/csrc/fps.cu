@@ -65,7 +65,7 @@ struct __align__(16) FpsShared {
   int32_t wcount[kItemWarps];
   int32_t cont[kItems];      // contenders of a recheck, ascending item index
   double cont_val[kItems];
-  double rn64[kItems];       // seed recheck: fp64 1/||x_i||
+  double cont_err[kItems];   // seed filter: error bound of a contender's fp32-pass value
   float2 rr[kItems];         // seed recheck: 1/||x_i|| as an unevaluated float pair
   double pair64[kMaxPairs];
   int16_t pair_a[kMaxPairs];  // item of a pair's contender
@@ -234,7 +234,10 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
     // independent float pairs (exact bf16 x fp32 products by TwoProd,
     // TwoSum sums); the groups' partial sums are merged in a fixed order.
     // One warp per contender then forms x_a . T.  Two identical items get
-    // bit-identical values, so the lowest slot wins an exact tie.
+    // bit-identical values, so the lowest slot wins an exact tie.  An fp32
+    // pass with a proven error bound comes first and settles the seed on
+    // its own when one contender is certainly the lowest; the float-float
+    // pass runs only when it is not (as for exact ties).
     const int nc = collect_contenders(i < n && mean <= t.v1 + 2.f * taum, sh);
     if (lazy && i < n) {  // (a template parameter)
       // the exact norms were not formed in the Gram phase: every item's now
@@ -244,110 +247,239 @@ __device__ void fps_pick(const FpsParams& p, FpsShared* sh, uint8_t* stages, uin
     }
     {
       const FF r = i < n ? ff_rsqrt(FF{sh->n2h[i], sh->n2l[i]}) : FF{0.f, 0.f};
-      sh->rn64[i] = ff_value(r);
       sh->rr[i] = make_float2(r.hi, r.lo);
     }
     item_sync();
     const int noct = D / 8;               // 16-byte column octets: 8..256
     const int ngrp = kItems / noct;       // item groups: 1..32
-    FF* Tp = reinterpret_cast<FF*>(stages);           // [ngrp][D] partial sums
-    FF* T = Tp + static_cast<size_t>(ngrp) * D;       // [D]
-    if (tid < ngrp * noct) {
-      const int g = tid / noct, o = tid - g * noct;
-      FF2 acc2[4];  // octet values 2h, 2h + 1 in halves 0, 1 of acc2[h]
+    const uint4* Xv = reinterpret_cast<const uint4*>(X);
+    // ---- fp32 filter.  T and A = sum_j |x_j| r_j are first formed in
+    // plain fp32 (fma, r_j rounded to its high part), in the same item
+    // groups, in blocks of eight items summed into a running total, and the
+    // groups merged in order; the sum a term passes through is at most
+    // m = 8 + (blocks per group) + (ngrp - 1) roundings deep, so
+    // |T32_k - T_k| <= (gamma_m + 2^-23.9) A_k (Higham, Accuracy and
+    // Stability of Numerical Algorithms, 2nd ed., 4.2; 2^-23.9 for r_j's
+    // low part).  A contender's value S_a = r_a (x_a . T32) - 1 (float-float
+    // dot) is then within E_a = 1.01 (gamma_m + 2^-22) r_a (|x_a| . A32)
+    // of its exact value (the factor covers 1 / (1 - gamma_m), A32's own
+    // rounding and the dot's).  When the lowest value's interval lies below
+    // every other contender's, it is the exact minimum, unique; otherwise
+    // the exact float-float pass below decides.
+    {
+      float* T32p = reinterpret_cast<float*>(stages);  // [ngrp][D]
+      float* A32p = T32p + static_cast<size_t>(ngrp) * D;
+      float* T32 = A32p + static_cast<size_t>(ngrp) * D;  // [D]
+      float* A32 = T32 + D;                                // [D]
+      if (tid < ngrp * noct) {
+        const int g = tid / noct, o = tid - g * noct;
+        uint64_t ta[4] = {0ull, 0ull, 0ull, 0ull}, aa[4] = {0ull, 0ull, 0ull, 0ull};
+        // the next block's loads are issued before this block is summed
+        auto load8 = [&](int j0, uint4 (&v)[8]) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc2[e] = FF2{0ull, 0ull};
-      const uint4* col = reinterpret_cast<const uint4*>(X) + o;
-      // eight items' loads in flight before any is used, and the next
-      // eight's issued before this eight's products are summed (the pass
-      // waits on L2 otherwise); items past n are zero and add exactly nothing
-      auto load8 = [&](int j0, uint4 (&v)[8]) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int j = j0 + q * ngrp;
-          v[q] = j < n ? col[static_cast<size_t>(j) * noct] : make_uint4(0u, 0u, 0u, 0u);
-        }
-      };
-      uint4 v[8];
-      load8(g, v);
+          for (int q = 0; q < 8; ++q) {
+            const int j = j0 + q * ngrp;
+            v[q] = j < n ? Xv[static_cast<size_t>(j) * noct + o] : make_uint4(0u, 0u, 0u, 0u);
+          }
+        };
+        uint4 v[8];
+        load8(g, v);
 #pragma unroll 1
-      for (int j0 = g; j0 < n; j0 += 8 * ngrp) {
-        uint4 vn[8];
-        load8(j0 + 8 * ngrp, vn);
-        float2 r[8];
+        for (int j0 = g; j0 < n; j0 += 8 * ngrp) {
+          uint4 vn[8];
+          load8(j0 + 8 * ngrp, vn);
+          float rh[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int j = j0 + q * ngrp;
-          r[q] = j < n ? sh->rr[j] : make_float2(0.f, 0.f);
+          for (int q = 0; q < 8; ++q) {
+            const int j = j0 + q * ngrp;
+            rh[q] = j < n ? sh->rr[j].x : 0.f;
+          }
+          uint64_t tb[4] = {0ull, 0ull, 0ull, 0ull}, ab[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t wv[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+            const uint64_t r2 = f2_pack(rh[q], rh[q]);
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+              const uint32_t lo = wv[hh] << 16, hi = wv[hh] & 0xFFFF0000u;
+              tb[hh] = f2_fma(f2_pack(__uint_as_float(lo), __uint_as_float(hi)), r2, tb[hh]);
+              ab[hh] = f2_fma(f2_pack(__uint_as_float(lo & 0x7FFFFFFFu),
+                                      __uint_as_float(hi & 0x7FFFFFFFu)),
+                              r2, ab[hh]);
+            }
+          }
+#pragma unroll
+          for (int hh = 0; hh < 4; ++hh) {
+            ta[hh] = f2_add(ta[hh], tb[hh]);
+            aa[hh] = f2_add(aa[hh], ab[hh]);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = vn[q];
         }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t wv[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-          const uint64_t rh2 = f2_pack(r[q].x, r[q].x), rl2 = f2_pack(r[q].y, r[q].y);
-#pragma unroll
-          for (int hh = 0; hh < 4; ++hh)
-            ff2_add_scaled(acc2[hh],
-                           f2_pack(__uint_as_float(wv[hh] << 16),
-                                   __uint_as_float(wv[hh] & 0xFFFF0000u)),
-                           rh2, rl2);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = vn[q];
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        FF a, b;
-        f2_unpack(acc2[e].hi, a.hi, b.hi);
-        f2_unpack(acc2[e].lo, a.lo, b.lo);
-        Tp[static_cast<size_t>(g) * D + 8 * o + 2 * e] = a;
-        Tp[static_cast<size_t>(g) * D + 8 * o + 2 * e + 1] = b;
-      }
-    }
-    item_sync();
-    for (int k = tid; k < D; k += kItems) {
-      FF tk = Tp[k];
-      for (int g = 1; g < ngrp; ++g) tk = ff_merge(tk, Tp[static_cast<size_t>(g) * D + k]);
-      T[k] = tk;
-    }
-    item_sync();
-    for (int cc = warp; cc < nc; cc += kItemWarps) {
-      const int a = sh->cont[cc];
-      const uint32_t* xa = reinterpret_cast<const uint32_t*>(X + static_cast<size_t>(a) * D);
-      FF d{0.f, 0.f};
-      for (int k2 = 2 * lane; k2 < D; k2 += 64) {
-        const uint32_t w = xa[k2 / 2];
-        ff_add_scaled(d, __uint_as_float(w << 16), T[k2].hi, T[k2].lo);
-        ff_add_scaled(d, __uint_as_float(w & 0xFFFF0000u), T[k2 + 1].hi, T[k2 + 1].lo);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const FF other{__shfl_xor_sync(0xffffffffu, d.hi, o), __shfl_xor_sync(0xffffffffu, d.lo, o)};
-        d = ff_merge(d, other);
-      }
-      if (lane == 0) {
-        // sum over j != a of cos(a, j) = r_a (x_a . T) - 1 for a nonzero
-        // item (its own term r_a^2 ||x_a||^2 is 1), 0 for a zero one; the
-        // common factor 1 / (n - 1) of the mean does not change the order
-        const float2 ra = sh->rr[a];
-        FF v = ff_mul(d, FF{ra.x, ra.y});
-        if (ra.x != 0.f) ff_add(v, -1.f);
-        sh->cont_val[cc] = ff_value(v);
-      }
-    }
-    item_sync();
-    if (tid == 0) {
-      int best = -1;
-      double bv = 0.0;
-      for (int c = 0; c < nc; ++c) {  // ascending index: strict < keeps the lowest
-        const double v = sh->cont_val[c];
-        if (best < 0 || v < bv) {
-          best = sh->cont[c];
-          bv = v;
+        for (int hh = 0; hh < 4; ++hh) {
+          const size_t at = static_cast<size_t>(g) * D + 8 * o + 2 * hh;
+          f2_unpack(ta[hh], T32p[at], T32p[at + 1]);
+          f2_unpack(aa[hh], A32p[at], A32p[at + 1]);
         }
       }
-      sh->winner = best;
+      item_sync();
+      for (int k = tid; k < D; k += kItems) {
+        float tk = T32p[k], ak = A32p[k];
+        for (int gg = 1; gg < ngrp; ++gg) {
+          tk += T32p[static_cast<size_t>(gg) * D + k];
+          ak += A32p[static_cast<size_t>(gg) * D + k];
+        }
+        T32[k] = tk;
+        A32[k] = ak;
+      }
+      item_sync();
+      const int per = (n + ngrp - 1) / ngrp;
+      const double m = 8.0 + (per + 7) / 8 + (ngrp - 1);
+      const double gm = m * 0x1p-24 / (1.0 - m * 0x1p-24);
+      for (int cc = warp; cc < nc; cc += kItemWarps) {
+        const int a = sh->cont[cc];
+        const uint32_t* xa = reinterpret_cast<const uint32_t*>(X + static_cast<size_t>(a) * D);
+        FF d{0.f, 0.f};
+        float bs = 0.f;
+        for (int k2 = 2 * lane; k2 < D; k2 += 64) {
+          const uint32_t w = xa[k2 / 2];
+          const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+          ff_add_scaled(d, x0, T32[k2], 0.f);
+          ff_add_scaled(d, x1, T32[k2 + 1], 0.f);
+          bs = fmaf(fabsf(x0), A32[k2], bs);
+          bs = fmaf(fabsf(x1), A32[k2 + 1], bs);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const FF other{__shfl_xor_sync(0xffffffffu, d.hi, o),
+                         __shfl_xor_sync(0xffffffffu, d.lo, o)};
+          d = ff_merge(d, other);
+          bs += __shfl_xor_sync(0xffffffffu, bs, o);
+        }
+        if (lane == 0) {
+          const float2 ra = sh->rr[a];
+          FF v = ff_mul(d, FF{ra.x, ra.y});
+          if (ra.x != 0.f) ff_add(v, -1.f);
+          sh->cont_val[cc] = ff_value(v);
+          sh->cont_err[cc] = 1.01 * (gm + 0x1p-22) * static_cast<double>(ra.x) * bs;
+        }
+      }
+      item_sync();
+      if (tid == 0) {
+        int best = 0;
+        for (int c = 1; c < nc; ++c)
+          if (sh->cont_val[c] < sh->cont_val[best]) best = c;
+        bool sure = true;
+        const double hi_best = sh->cont_val[best] + sh->cont_err[best];
+        for (int c = 0; c < nc; ++c)
+          if (c != best && !(sh->cont_val[c] - sh->cont_err[c] > hi_best)) sure = false;
+        sh->winner = sure ? sh->cont[best] : -1;
+      }
+      item_sync();
     }
-    item_sync();
+    if (sh->winner < 0) {  // block-uniform (read after the barrier above)
+      // ---- exact float-float pass
+      FF* Tp = reinterpret_cast<FF*>(stages);           // [ngrp][D] partial sums
+      FF* T = Tp + static_cast<size_t>(ngrp) * D;       // [D]
+      item_sync();  // every thread has read the winner before it is written again
+      if (tid < ngrp * noct) {
+        const int g = tid / noct, o = tid - g * noct;
+        FF2 acc2[4];  // octet values 2h, 2h + 1 in halves 0, 1 of acc2[h]
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc2[e] = FF2{0ull, 0ull};
+        const uint4* col = reinterpret_cast<const uint4*>(X) + o;
+        // eight items' loads in flight before any is used, and the next
+        // eight's issued before this eight's products are summed (the pass
+        // waits on L2 otherwise); items past n are zero and add exactly nothing
+        auto load8 = [&](int j0, uint4 (&v)[8]) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int j = j0 + q * ngrp;
+            v[q] = j < n ? col[static_cast<size_t>(j) * noct] : make_uint4(0u, 0u, 0u, 0u);
+          }
+        };
+        uint4 v[8];
+        load8(g, v);
+#pragma unroll 1
+        for (int j0 = g; j0 < n; j0 += 8 * ngrp) {
+          uint4 vn[8];
+          load8(j0 + 8 * ngrp, vn);
+          float2 r[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int j = j0 + q * ngrp;
+            r[q] = j < n ? sh->rr[j] : make_float2(0.f, 0.f);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t wv[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+            const uint64_t rh2 = f2_pack(r[q].x, r[q].x), rl2 = f2_pack(r[q].y, r[q].y);
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh)
+              ff2_add_scaled(acc2[hh],
+                             f2_pack(__uint_as_float(wv[hh] << 16),
+                                     __uint_as_float(wv[hh] & 0xFFFF0000u)),
+                             rh2, rl2);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = vn[q];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          FF a, b;
+          f2_unpack(acc2[e].hi, a.hi, b.hi);
+          f2_unpack(acc2[e].lo, a.lo, b.lo);
+          Tp[static_cast<size_t>(g) * D + 8 * o + 2 * e] = a;
+          Tp[static_cast<size_t>(g) * D + 8 * o + 2 * e + 1] = b;
+        }
+      }
+      item_sync();
+      for (int k = tid; k < D; k += kItems) {
+        FF tk = Tp[k];
+        for (int g = 1; g < ngrp; ++g) tk = ff_merge(tk, Tp[static_cast<size_t>(g) * D + k]);
+        T[k] = tk;
+      }
+      item_sync();
+      for (int cc = warp; cc < nc; cc += kItemWarps) {
+        const int a = sh->cont[cc];
+        const uint32_t* xa = reinterpret_cast<const uint32_t*>(X + static_cast<size_t>(a) * D);
+        FF d{0.f, 0.f};
+        for (int k2 = 2 * lane; k2 < D; k2 += 64) {
+          const uint32_t w = xa[k2 / 2];
+          ff_add_scaled(d, __uint_as_float(w << 16), T[k2].hi, T[k2].lo);
+          ff_add_scaled(d, __uint_as_float(w & 0xFFFF0000u), T[k2 + 1].hi, T[k2 + 1].lo);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const FF other{__shfl_xor_sync(0xffffffffu, d.hi, o), __shfl_xor_sync(0xffffffffu, d.lo, o)};
+          d = ff_merge(d, other);
+        }
+        if (lane == 0) {
+          // sum over j != a of cos(a, j) = r_a (x_a . T) - 1 for a nonzero
+          // item (its own term r_a^2 ||x_a||^2 is 1), 0 for a zero one; the
+          // common factor 1 / (n - 1) of the mean does not change the order
+          const float2 ra = sh->rr[a];
+          FF v = ff_mul(d, FF{ra.x, ra.y});
+          if (ra.x != 0.f) ff_add(v, -1.f);
+          sh->cont_val[cc] = ff_value(v);
+        }
+      }
+      item_sync();
+      if (tid == 0) {
+        int best = -1;
+        double bv = 0.0;
+        for (int c = 0; c < nc; ++c) {  // ascending index: strict < keeps the lowest
+          const double v = sh->cont_val[c];
+          if (best < 0 || v < bv) {
+            best = sh->cont[c];
+            bv = v;
+          }
+        }
+        sh->winner = best;
+      }
+      item_sync();
+    }
     seed = sh->winner;
     // the staged chunks were overwritten by the partial sums: none is
     // resident any more (the greedy steps read the buffer from global memory)
