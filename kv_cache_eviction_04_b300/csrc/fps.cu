@@ -16,7 +16,8 @@
 //      in TMEM columns [0, 256) and [256, 512) with fp32 accumulation.  The
 //      Gram stays in TMEM for the whole selection.
 //      While a chunk is staged, thread i also accumulates the exact squared
-//      norm of item i from it (exact bf16 products, TwoSum sums).
+//      norm of item i from it (exact bf16 products, TwoSum sums, two float
+//      pairs per packed f32x2 instruction).
 //   2. Thread i owns item i (its TMEM lane): its mean cosine to the others
 //      from its TMEM row (pairwise fp32 sum) -> seed = argmin.
 //   3. Greedy: each step reads the new pick's Gram column (one TMEM column:
@@ -27,7 +28,9 @@
 //      the runner-up by more than twice a bound on the fp32 error; otherwise
 //      every contender within that band is re-evaluated from the bf16 inputs
 //      with exact products and error-free (TwoSum) sums, ~2^-44 accurate,
-//      and those values decide (ties: lowest index).  The indices then equal
+//      and those values decide (ties: lowest index).  For the seed an fp32
+//      pass with a proven error bound comes first and settles the choice
+//      when one contender is certainly the lowest.  The indices then equal
 //      those of an fp64 evaluation except where two candidates' exact values
 //      differ by less than ~1e-12; identical items tie exactly.
 #include "common.cuh"

@@ -159,12 +159,14 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
   // ---- Gram rows of this CTA's items against all items; exact norms of all
   // items (thread t: items t and t + 256) from the staged chunks
   // squared norms of items t and t + 256: four partial sums each
-  // (independent chains), merged in order at the end
-  FF n2p[2][4];
+  // (independent chains; sum e takes pieces e and e + 4 of every chunk),
+  // merged in order at the end; sums 2h and 2h + 1 ride in halves 0 and 1
+  // of n2p2[half][h] (packed f32x2 arithmetic, the same bits)
+  FF2 n2p2[2][2];
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) n2p[hh][e] = FF{0.f, 0.f};
+    for (int e = 0; e < 2; ++e) n2p2[hh][e] = FF2{0ull, 0ull};
   const uint32_t id1 = idesc_bf16_f32(128, static_cast<uint32_t>(N1));
   const uint32_t id2 = idesc_bf16_f32(128, static_cast<uint32_t>(N2 > 0 ? N2 : 16));
   auto load_chunk = [&](int c, int st) {
@@ -200,9 +202,10 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
       if (j < n) {
         const uint8_t* row = sb + j * 128;
 #pragma unroll
-        for (int lc = 0; lc < 8; ++lc) {
-          const uint4 v = *reinterpret_cast<const uint4*>(row + ((lc ^ (j & 7)) << 4));
-          ff_add_products(n2p[half][lc & 3], v, v);
+        for (int q = 0; q < 4; ++q) {  // pieces 2q and 2q + 1 -> sums (2q, 2q + 1) mod 4
+          const uint4 v0 = *reinterpret_cast<const uint4*>(row + (((2 * q) ^ (j & 7)) << 4));
+          const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((2 * q + 1) ^ (j & 7)) << 4));
+          ff2_add_squares(n2p2[half][q & 1], v0, v1);
         }
       }
     }
@@ -226,7 +229,13 @@ __device__ int fps_select_cl(const FpsParams& p, const CUtensorMap* bmap, ClShar
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int j = tid + 256 * half;
-    const FF n2 = ff_merge(ff_merge(n2p[half][0], n2p[half][1]), ff_merge(n2p[half][2], n2p[half][3]));
+    FF n2p[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      f2_unpack(n2p2[half][h].hi, n2p[2 * h].hi, n2p[2 * h + 1].hi);
+      f2_unpack(n2p2[half][h].lo, n2p[2 * h].lo, n2p[2 * h + 1].lo);
+    }
+    const FF n2 = ff_merge(ff_merge(n2p[0], n2p[1]), ff_merge(n2p[2], n2p[3]));
     const FF r = j < n ? ff_rsqrt(n2) : FF{0.f, 0.f};
     sh->rn64[j] = ff_value(r);
     sh->n2_64[j] = j < n ? ff_value(n2) : 0.0;
