@@ -56,7 +56,7 @@ def parse():
                     help="skip the 128-step decode cycle (appends + compress + round)")
     ap.add_argument("--e2e-max-gb", type=float, default=12.0,
                     help="largest host staging for the end-to-end leg")
-    ap.add_argument("--e2e-chunks", type=int, default=8,
+    ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="unit chunks of the pipelined end-to-end leg (copies in, rounds and "
                          "copies out of successive chunks overlap on three streams)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -556,9 +556,9 @@ def run_ours(args, rank, world):
         e2e = {"value": world * 1e3 / e2e_ms, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "chunks": nch,
                "serial_value": world * 1e3 / serial_ms,
-               "note": f"{nch} unit chunks, one bkv_round each; copy in, round and copy out "
-                       "overlap on three streams (serial_value: one round between one copy "
-                       "in and one copy out)"}
+               "note": f"units in {nch} chunk(s), one bkv_round each; copy in, round and copy "
+                       "out overlap on three streams (serial_value: one round between one "
+                       "copy in and one copy out)"}
 
     cycle = run_cycle(args, cfg, dims, pristine, work, cur, step, bidx, beac, nb, scores, kept,
                       ws, stream, restore) if not args.no_cycle else None
