@@ -45,10 +45,11 @@ def twins(rng, n, D):
     return X
 
 
-def seed_tie(rng, X, tau):
+def seed_tie(rng, X, tau, band=(0.5, 4.0)):
     """Make the seed decision a near-tie: a copy b of the lowest-mean item a
     (a's own near twin replaced first) is moved one ulp at a time until
-    mean_b - mean_a, or its negative, lies in [0.5 tau, 4 tau]."""
+    mean_b - mean_a, or its negative, lies in [band[0] tau, band[1] tau]
+    (elements whose one-ulp move overshoots the band are left alone)."""
     n, D = X.shape
     Xh = _unit_rows(X)
     T = Xh.sum(0)
@@ -70,7 +71,7 @@ def seed_tie(rng, X, tau):
     X[b] = X[a]
     Xh[b] = Xh[a]
     sgn = 1.0 if rng.integers(2) else -1.0
-    lo, hi = 0.5 * tau, 4.0 * tau
+    lo, hi = band[0] * tau, band[1] * tau
     target = rng.uniform(lo, hi)
 
     def gap():
@@ -87,6 +88,8 @@ def seed_tie(rng, X, tau):
         w = np.abs(g) * np.abs(xb)
         if w.sum() <= 0:
             break
+        if band[1] < 0.5:  # a fine band: small moves first (uniform over elements)
+            w = (w > 0).astype(float)
         k = int(rng.choice(D, p=w / w.sum()))
         old, old_row = X[b, k], Xh[b].copy()
         X[b, k] = _bump(X[b, k], g[k] > 0)
@@ -121,16 +124,17 @@ def decision_gaps(X, m):
     return out
 
 
-def near_tie_units(seed, U, n, D, m):
-    """U buffers of n items (twins plus a seed near-tie) and the count of
-    seed and greedy decisions whose fp64 gap lies in [0.5 tau, 4 tau]."""
+def near_tie_units(seed, U, n, D, m, band=(0.5, 4.0)):
+    """U buffers of n items (twins plus a seed near-tie whose gap is aimed
+    at [band[0] tau, band[1] tau]) and the count of seed and greedy
+    decisions whose fp64 gap lies in that band."""
     rng = np.random.default_rng(seed)
     tau = tau_cos(D)
     bufs, in_band = [], {"seed": 0, "greedy": 0}
     for _ in range(U):
-        X = seed_tie(rng, twins(rng, n, D), tau)
+        X = seed_tie(rng, twins(rng, n, D), tau, band)
         for kind, g in decision_gaps(X, m):
-            if 0.5 * tau <= g <= 4 * tau:
+            if band[0] * tau <= g <= band[1] * tau:
                 in_band[kind] += 1
         bufs.append(X)
     return np.stack(bufs), in_band
