@@ -338,6 +338,15 @@ def traffic_for(kernel_file, kernel, wkey):
     return None
 
 
+def e2e_chunk_cuts(U: int, step_bytes: int, max_chunks: int) -> list:
+    """Unit boundaries of the pipelined end-to-end leg: at most max_chunks
+    chunks of near-equal unit counts, each carrying at least ~16 MB of the
+    step's host copies (smaller chunks pay a whole round's launches for
+    little transfer), never an empty chunk."""
+    nch = max(1, min(max_chunks, U, int(step_bytes // (16 << 20))))
+    return [U * c // nch for c in range(nch + 1)]
+
+
 def max_over_ranks(ms: float, world: int, device) -> float:
     """The slowest rank's elapsed time (every rank gets it)."""
     if world <= 1:
@@ -493,10 +502,8 @@ def run_ours(args, rank, world):
         # (stream s_out) overlap chunk c + 1's copy in and chunk c - 1's copy
         # out; the link carries both directions at once.  Every byte of the
         # serial step still crosses it.
-        # chunks of at least ~16 MB of copies each: smaller ones pay a whole
-        # round's launches for little transfer
-        nch = max(1, min(args.e2e_chunks, U, int((h2d + d2h) // (16 << 20))))
-        cuts = [U * c // nch for c in range(nch + 1)]
+        cuts = e2e_chunk_cuts(U, h2d + d2h, args.e2e_chunks)
+        nch = len(cuts) - 1
         cdims = [bkv.Dims.from_config(cfg, U=cuts[c + 1] - cuts[c], compact=dims.compact)
                  for c in range(nch)]
         cws = [bkv.make_workspace(cd, dev) for cd in cdims]
